@@ -1,0 +1,167 @@
+"""CPU oracle for the routed MoE expert layer.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+(``routed_grouped_gemm_routing_gb300``) never imports it and shares no code
+with it.
+
+The numerical work is plain C (``moe_oracle.c``), built here with gcc and
+called through ctypes.  See ``moe_oracle.c`` for the definitions and where
+each comes from (Primus-Turbo "Mega MoE" README, "Pipeline" and
+"Implementation Map"; DeepGEMM Mega-MoE article, "Block-M Alignment").
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+(brute force, closed-form special cases, invariants, finite differences).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_LOCK = threading.Lock()
+_LIB = None
+
+
+def lib_path() -> str:
+    return os.path.join(_BUILD, f"liboracle_{platform.machine()}.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP) into oracle/_build/."""
+    out = lib_path()
+    src = os.path.join(_HERE, "moe_oracle.c")
+    body = os.path.join(_HERE, "moe_oracle_body.h")
+    if not force and os.path.exists(out):
+        newest = max(os.path.getmtime(src), os.path.getmtime(body))
+        if os.path.getmtime(out) >= newest:
+            return out
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+            L.oracle_rows_cap.argtypes = [i32, i32, i32, i32]
+            L.oracle_rows_cap.restype = i64
+            L.oracle_route.argtypes = [i32, i32, i32, i32] + [vp] * 7
+            L.oracle_route.restype = None
+            for suf in ("b16", "f64"):
+                getattr(L, f"oracle_forward_{suf}").argtypes = [i32] * 5 + [vp] * 5 + [i32, vp, vp]
+                getattr(L, f"oracle_backward_tokens_{suf}").argtypes = [i32] * 5 + [vp] * 6 + [i32, vp, vp, vp]
+                getattr(L, f"oracle_backward_experts_{suf}").argtypes = [i32] * 5 + [vp] * 6 + [i32, vp, vp, vp]
+                for n in ("forward", "backward_tokens", "backward_experts"):
+                    getattr(L, f"oracle_{n}_{suf}").restype = None
+            L.oracle_num_threads.restype = ctypes.c_int
+            _LIB = L
+    return _LIB
+
+
+def _p(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def num_threads() -> int:
+    return int(_lib().oracle_num_threads())
+
+
+def rows_cap(T: int, E: int, k: int, bm: int) -> int:
+    return int(_lib().oracle_rows_cap(T, E, k, bm))
+
+
+def route(topk_idx: np.ndarray, E: int, bm: int = 128) -> dict:
+    """Routing tables from topk_idx [T, k] (int32).  Returns a dict of numpy
+    int32 arrays: counts, offs, perm, inv, tiles, and ints mpad, num_tiles,
+    n_invalid."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    cap = rows_cap(T, E, k, bm)
+    counts = np.zeros(E, np.int32)
+    offs = np.zeros(E + 1, np.int32)
+    perm = np.zeros(max(cap, 1), np.int32)
+    inv = np.zeros(max(T * k, 1), np.int32)
+    tiles = np.zeros(max(cap // bm, 1), np.int32)
+    scal = np.zeros(3, np.int32)
+    _lib().oracle_route(T, E, k, bm, _p(idx), _p(counts), _p(offs), _p(perm), _p(inv), _p(tiles), _p(scal))
+    return dict(counts=counts, offs=offs, perm=perm[:cap], inv=inv[: T * k], tiles=tiles[: cap // bm],
+                mpad=int(scal[0]), num_tiles=int(scal[1]), n_invalid=int(scal[2]))
+
+
+def _prep(precision, x, W1, W2, topk_idx, topk_w, dY=None):
+    if precision == "b16":
+        conv = lambda a: np.ascontiguousarray(a, dtype=np.uint16)  # noqa: E731
+        wconv = lambda a: np.ascontiguousarray(a, dtype=np.float32)  # noqa: E731
+        rdt = np.float32
+    elif precision == "f64":
+        conv = wconv = lambda a: np.ascontiguousarray(a, dtype=np.float64)  # noqa: E731
+        rdt = np.float64
+    else:
+        raise ValueError(precision)
+    out = [conv(x), conv(W1), conv(W2), np.ascontiguousarray(topk_idx, dtype=np.int32), wconv(topk_w)]
+    if dY is not None:
+        out.append(conv(dY))
+    return out, rdt
+
+
+def _dims(x, W1, W2, topk_idx):
+    T, H = x.shape
+    E, H1, I2 = W1.shape
+    assert H1 == H and I2 % 2 == 0
+    I = I2 // 2
+    assert W2.shape == (E, I, H)
+    k = topk_idx.shape[1]
+    return T, H, I, E, k
+
+
+def forward(x, W1, W2, topk_idx, topk_w, tokens=None, precision="b16"):
+    """y rows [len(tokens), H] for the listed tokens (all tokens by default).
+
+    precision "b16": x, W1, W2 are bfloat16 bit patterns (uint16 arrays),
+    topk_w float32, FP32 arithmetic.  precision "f64": everything float64."""
+    (x, W1, W2, idx, w), rdt = _prep(precision, x, W1, W2, topk_idx, topk_w)
+    T, H, I, E, k = _dims(x, W1, W2, idx)
+    toks = np.ascontiguousarray(np.arange(T) if tokens is None else tokens, dtype=np.int32)
+    y = np.zeros((len(toks), H), rdt)
+    fn = getattr(_lib(), f"oracle_forward_{precision}")
+    fn(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), len(toks), _p(toks), _p(y))
+    return y
+
+
+def backward_tokens(x, W1, W2, topk_idx, topk_w, dY, tokens=None, precision="b16"):
+    """(dx [n, H], dtopk_w [n, k]) for the listed tokens."""
+    (x, W1, W2, idx, w, dY), rdt = _prep(precision, x, W1, W2, topk_idx, topk_w, dY)
+    T, H, I, E, k = _dims(x, W1, W2, idx)
+    toks = np.ascontiguousarray(np.arange(T) if tokens is None else tokens, dtype=np.int32)
+    dx = np.zeros((len(toks), H), rdt)
+    dw = np.zeros((len(toks), k), rdt)
+    fn = getattr(_lib(), f"oracle_backward_tokens_{precision}")
+    fn(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), _p(dY), len(toks), _p(toks), _p(dx), _p(dw))
+    return dx, dw
+
+
+def backward_experts(x, W1, W2, topk_idx, topk_w, dY, experts=None, precision="b16"):
+    """(dW1 [n, H, 2I], dW2 [n, I, H]) for the listed experts."""
+    (x, W1, W2, idx, w, dY), rdt = _prep(precision, x, W1, W2, topk_idx, topk_w, dY)
+    T, H, I, E, k = _dims(x, W1, W2, idx)
+    exps = np.ascontiguousarray(np.arange(E) if experts is None else experts, dtype=np.int32)
+    dW1 = np.zeros((len(exps), H, 2 * I), rdt)
+    dW2 = np.zeros((len(exps), I, H), rdt)
+    fn = getattr(_lib(), f"oracle_backward_experts_{precision}")
+    fn(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), _p(dY), len(exps), _p(exps), _p(dW1), _p(dW2))
+    return dW1, dW2

@@ -1,0 +1,136 @@
+/*
+ * CPU oracle for the routed MoE expert layer (routing tables, forward,
+ * backward).  TEST INFRASTRUCTURE ONLY: it is compiled and called by the
+ * tests, by the package's smoke check and by the benchmark's CPU-baseline
+ * leg, never by the product path.  It shares no code, header or constant
+ * with the CUDA library; the two are written independently from the same
+ * definitions.
+ *
+ * Sources of each definition:
+ *  - routing tables: Primus-Turbo "Mega MoE" README, "Implementation Map"
+ *    (a dispatch prologue builds routing tables from topk_idx) and the
+ *    DeepGEMM Mega-MoE article, "Block-M Alignment for Irregular Token
+ *    Counts" (per-expert token counts are padded to the GEMM block M).
+ *  - forward / backward: the Mega MoE README, "Pipeline" (dispatch, L1
+ *    grouped GEMM, SwiGLU, L2 grouped GEMM, top-k weighted combine, and the
+ *    conjugate backward).
+ *
+ * Two instantiations of the numerical body:
+ *   *_b16 : x, W1, W2, dY given as bfloat16 bit patterns (widened exactly),
+ *           routing weights FP32, all arithmetic FP32.  This is the oracle
+ *           the GPU results are compared with.
+ *   *_f64 : every input and all arithmetic in FP64 (used for finite
+ *           differences and the oracle's own pins).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- routing */
+
+/* Row capacity of the block-M padded layout: the padded row count
+ *   Mpad = sum_e ceil(c_e / bm) * bm
+ * never exceeds T*k + min(E, T*k) * (bm - 1), and is a multiple of bm, so it
+ * never exceeds that bound rounded down to a multiple of bm. */
+int64_t oracle_rows_cap(int T, int E, int k, int bm) {
+    int64_t tk = (int64_t)T * k;
+    int64_t ne = tk < E ? tk : E;
+    int64_t bound = tk + ne * (bm - 1);
+    return (bound / bm) * bm;
+}
+
+/*
+ * Routing tables for slots s = t*k + j (topk_idx is [T, k], row-major):
+ *   counts[e]  number of slots with topk_idx[s] == e
+ *   offs[e]    exclusive prefix sum of ceil(counts[e]/bm)*bm ; offs[E] = Mpad
+ *   perm[r]    slot held by padded row r, -1 for padding rows and for every
+ *              row r >= Mpad (array length = oracle_rows_cap)
+ *              rows of expert e hold its slots in increasing s
+ *   inv[s]     padded row of slot s, -1 when the slot is dropped
+ *   tiles[m]   expert owning rows [m*bm, (m+1)*bm), -1 for m >= Mpad/bm
+ *              (array length = oracle_rows_cap / bm)
+ *   scal[0] = Mpad, scal[1] = Mpad / bm, scal[2] = number of slots whose id
+ *   is neither -1 nor in [0, E) (they are dropped like -1).
+ */
+void oracle_route(int T, int E, int k, int bm, const int32_t* topk_idx,
+                  int32_t* counts, int32_t* offs, int32_t* perm, int32_t* inv,
+                  int32_t* tiles, int32_t* scal) {
+    int64_t tk = (int64_t)T * k;
+    int64_t cap = oracle_rows_cap(T, E, k, bm);
+    int32_t n_invalid = 0;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t s = 0; s < tk; ++s) {
+        int32_t e = topk_idx[s];
+        if (e >= 0 && e < E) counts[e] += 1;
+        else if (e != -1) n_invalid += 1;
+    }
+    offs[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int32_t padded = ((counts[e] + bm - 1) / bm) * bm;
+        offs[e + 1] = offs[e] + padded;
+    }
+    int32_t mpad = offs[E];
+    for (int64_t r = 0; r < cap; ++r) perm[r] = -1;
+    for (int64_t s = 0; s < tk; ++s) inv[s] = -1;
+    /* next free row of each expert; visiting slots in increasing s gives
+     * the stable order within an expert */
+    int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e) next[e] = offs[e];
+    for (int64_t s = 0; s < tk; ++s) {
+        int32_t e = topk_idx[s];
+        if (e < 0 || e >= E) continue;
+        int32_t r = next[e]++;
+        perm[r] = (int32_t)s;
+        inv[s] = r;
+    }
+    free(next);
+    int64_t ntiles_cap = cap / bm;
+    for (int64_t m = 0; m < ntiles_cap; ++m) tiles[m] = -1;
+    for (int e = 0; e < E; ++e)
+        for (int32_t m = offs[e] / bm; m < offs[e + 1] / bm; ++m) tiles[m] = e;
+    scal[0] = mpad;
+    scal[1] = mpad / bm;
+    scal[2] = n_invalid;
+}
+
+/* ---------------------------------------------- numerical instantiations */
+
+static inline float bf16_widen(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+#define SUF b16
+#define IN_T uint16_t
+#define W_T float
+#define REAL float
+#define LD(p, i) bf16_widen((p)[(i)])
+#include "moe_oracle_body.h"
+#undef SUF
+#undef IN_T
+#undef W_T
+#undef REAL
+#undef LD
+
+#define SUF f64
+#define IN_T double
+#define W_T double
+#define REAL double
+#define LD(p, i) ((p)[(i)])
+#include "moe_oracle_body.h"
+#undef SUF
+#undef IN_T
+#undef W_T
+#undef REAL
+#undef LD
+
+/* Threads the OpenMP runtime will use (reported next to CPU timings). */
+#ifdef _OPENMP
+#include <omp.h>
+int oracle_num_threads(void) { return omp_get_max_threads(); }
+#else
+int oracle_num_threads(void) { return 1; }
+#endif
