@@ -1,0 +1,142 @@
+/*
+ * moe_layer.h - C ABI of the GB300 (sm_103a) routed MoE expert layer.
+ *
+ * The layer (Primus-Turbo "Mega MoE" README, sections "Key points" and
+ * "Pipeline"): for every token t and each of its k routing slots j, with
+ * expert e = topk_idx[t,j] and weight w = topk_weights[t,j],
+ *
+ *     h      = x[t] . W1[e]                  (L1 grouped GEMM, H -> 2I)
+ *     a      = silu(h[:I]) * h[I:]           (SwiGLU; gate columns first)
+ *     o      = w * (a . W2[e])               (L2 grouped GEMM, I -> H)
+ *     y[t]   = sum_j o                       (combine: per-token sum over k)
+ *
+ * and its backward (same page: "L2 dgrad + SwiGLU^T + dW2 (variable-K)",
+ * "L1 dgrad + combine + dW1", with the dispatched x recomputed rather than
+ * stored, section "Recompute dispatched x in backward").  Cross-rank
+ * dispatch/combine of the pages become an on-device permutation of routed
+ * rows (one GPU).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous,
+ *    16-byte aligned.  "bf16" means IEEE bfloat16 bit patterns.
+ *  - The caller owns every buffer and every stream.  The library never
+ *    allocates, frees or synchronises (except moe_read_status, which says so).
+ *    Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream).  No call reads device data on the host, so
+ *    every enqueueing call can be captured in a CUDA graph.
+ *  - Return value: MOE_OK (0) on success, or a negative MOE_E* code; then
+ *    moe_last_error() gives a message (thread-local).  On an error return
+ *    nothing has been enqueued unless the code is MOE_ECUDA.
+ *  - Data-dependent problems are never checked on the host: an expert id
+ *    outside [0, E) other than -1 is counted in the status words and the slot
+ *    is dropped (it contributes nothing), exactly like -1.
+ *  - Shapes: T >= 0; H, I > 0 and multiples of 64; 1 <= k <= E <= 1024;
+ *    block_m == 128; T*k < 2^31.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Layer shape.  T tokens, hidden H, intermediate I, E experts, top-k k,
+ * block_m = row alignment of each expert's group (DeepGEMM Mega-MoE article,
+ * "Block-M Alignment for Irregular Token Counts"; only 128 is supported). */
+typedef struct moe_shape {
+    int32_t T, H, I, E, k, block_m;
+} moe_shape;
+
+enum {
+    MOE_OK = 0,
+    MOE_EINVAL = -1,       /* null pointer, bad dimension, k > E, ... */
+    MOE_EUNSUPPORTED = -2, /* H or I not a multiple of 64, block_m != 128, misaligned pointer */
+    MOE_ECUDA = -3         /* a CUDA runtime/driver call or launch failed */
+};
+
+/* Status words inside route_ws (int32 each), see moe_read_status. */
+enum {
+    MOE_STATUS_MPAD = 0,      /* padded routed rows, a multiple of block_m */
+    MOE_STATUS_NUM_TILES = 1, /* MOE_STATUS_MPAD / block_m */
+    MOE_STATUS_N_INVALID = 2, /* slots whose id was neither -1 nor in [0, E) */
+    MOE_STATUS_FLAGS = 3,     /* bit 0: a kernel gave up on a bounded wait */
+    MOE_STATUS_WORDS = 16
+};
+
+/* Byte offsets of every table inside the three caller-owned workspaces.
+ *  route_ws (written by moe_route_prologue, read by forward/backward):
+ *    counts  int32[E]          slots per expert
+ *    offs    int32[E+1]        block_m-padded exclusive prefix sum; offs[E] = Mpad
+ *    perm    int32[rows_cap]   slot s = t*k+j held by padded row r; -1 = padding
+ *                              (and every r >= Mpad); an expert's rows hold its
+ *                              slots in increasing s
+ *    inv     int32[T*k]        padded row of slot s; -1 = dropped slot
+ *    tiles   int32[tiles_cap]  expert owning rows [m*block_m, (m+1)*block_m);
+ *                              -1 for m >= Mpad/block_m
+ *    status  int32[16]         MOE_STATUS_* words
+ *  saved (written by moe_forward, read by moe_backward):
+ *    h  bf16[rows_cap, 2I]     L1 output per padded row (gate | up); 0 on padding
+ *    a  bf16[rows_cap, I]      SwiGLU output per padded row; 0 on padding
+ *    o  bf16[rows_cap, H]      weighted L2 output per padded row
+ *  bwd_ws (scratch of moe_backward):
+ *    dh      bf16[rows_cap, 2I]          gradient at h; 0 on padding
+ *    aw      bf16[rows_cap, I]           w * a per padded row; 0 on padding
+ *    dxp     bf16[rows_cap, H]           per-row gradient at the dispatched x
+ *    dw_part f32[rows_cap, dw_part_cols] partial sums of d(topk_weights)
+ * rows_cap = floor((T*k + min(E, T*k)*(block_m-1)) / block_m) * block_m bounds
+ * Mpad for any routing, so no buffer depends on device data. */
+typedef struct moe_layout {
+    int64_t rows_cap, tiles_cap;
+    size_t route_bytes, counts, offs, perm, inv, tiles, status;
+    size_t saved_bytes, h, a, o;
+    size_t bwd_bytes, dh, aw, dxp, dw_part;
+    int32_t dw_part_cols;
+} moe_layout;
+
+/* Sizes and offsets of the three workspaces for `shape`.  Host only; touches
+ * no device.  Errors: MOE_EINVAL / MOE_EUNSUPPORTED for a bad shape. */
+int moe_workspace_layout(const moe_shape* shape, moe_layout* out);
+
+/* Routing prologue (Primus-Turbo Mega MoE README, "Implementation Map":
+ * dispatch prologue that builds routing tables; DeepGEMM Mega-MoE article,
+ * "Block-M Alignment").  Reads topk_idx int32[T, k] (device), writes every
+ * route_ws table and status word listed above.  route_ws must hold
+ * route_bytes.  Bit-exact and deterministic; no host synchronisation. */
+int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* route_ws, void* stream);
+
+/* Forward (Mega MoE README, "Pipeline"): x bf16[T,H], W1 bf16[E,H,2I]
+ * (columns [0,I) gate, [I,2I) up), W2 bf16[E,I,H], topk_w f32[T,k],
+ * route_ws from moe_route_prologue on the same topk_idx (its status words
+ * may be updated).  Writes saved (saved_bytes) and y bf16[T,H]; y is
+ * overwritten.  The combine sums a token's k contributions in FP32 in slot
+ * order j = 0..k-1 and rounds once to bf16 (deterministic, no atomics). */
+int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2,
+                const float* topk_w, void* route_ws, void* saved, void* y, void* stream);
+
+/* Backward of moe_forward given dY bf16[T,H] (Mega MoE README, "Pipeline",
+ * backward paragraph).  Inputs as for moe_forward plus `saved` from it.
+ * Overwrites (never accumulates into) dx bf16[T,H], dW1 bf16[E,H,2I],
+ * dW2 bf16[E,I,H] and dtopk_w f32[T,k]; an expert with no routed slot gets
+ * dW1 = dW2 = 0 and a dropped slot gets dtopk_w = 0.  bwd_ws must hold
+ * bwd_bytes.  The dispatched x is re-gathered from x, never stored. */
+int moe_backward(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
+                 const float* topk_w, void* route_ws, const void* saved, void* bwd_ws,
+                 void* dx, void* dW1, void* dW2, float* dtopk_w, void* stream);
+
+/* Copies the MOE_STATUS_WORDS status words of route_ws to host memory
+ * `out` (int32[16]).  SYNCHRONISES `stream`; not for use under capture. */
+int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, void* stream);
+
+/* Message for the last non-zero return on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LAYER_H */

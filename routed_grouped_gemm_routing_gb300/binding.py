@@ -1,0 +1,182 @@
+"""Thin Python binding of the C ABI in include/moe_layer.h.
+
+Argument marshalling only: every entry point takes torch tensors (device
+memory owned by the caller), checks dtype / device / contiguity / size, and
+passes raw pointers plus the current CUDA stream to the library.  All work
+runs in the library's kernels.  There is no fallback: if the library has not
+been built, or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+_LOCK = threading.Lock()
+_LIB = None
+
+HEADER = os.path.join(_build.INCLUDE, "moe_layer.h")
+MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA = 0, -1, -2, -3
+STATUS_MPAD, STATUS_NUM_TILES, STATUS_N_INVALID, STATUS_FLAGS, STATUS_WORDS = 0, 1, 2, 3, 16
+BLOCK_M = 128
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "block_m")]
+
+
+class MoeLayout(ctypes.Structure):
+    _fields_ = [("rows_cap", ctypes.c_int64), ("tiles_cap", ctypes.c_int64)] + [
+        (n, ctypes.c_size_t)
+        for n in ("route_bytes", "counts", "offs", "perm", "inv", "tiles", "status",
+                  "saved_bytes", "h", "a", "o", "bwd_bytes", "dh", "aw", "dxp", "dw_part")
+    ] + [("dw_part_cols", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"moe error {code}: {msg}")
+        self.code = code
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/moe_layer.h declares."""
+    text = open(HEADER).read()
+    return re.findall(r"^(?:int|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = _build.lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is not built; run routed_grouped_gemm_routing_gb300.build.build()")
+            L = ctypes.CDLL(path)
+            vp, P = ctypes.c_void_p, ctypes.POINTER
+            L.moe_workspace_layout.argtypes = [P(MoeShape), P(MoeLayout)]
+            L.moe_route_prologue.argtypes = [P(MoeShape), vp, vp, vp]
+            L.moe_forward.argtypes = [P(MoeShape)] + [vp] * 8
+            L.moe_backward.argtypes = [P(MoeShape)] + [vp] * 13
+            L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
+            for n in ("moe_workspace_layout", "moe_route_prologue", "moe_forward", "moe_backward", "moe_read_status"):
+                getattr(L, n).restype = ctypes.c_int
+            L.moe_last_error.restype = ctypes.c_char_p
+            L.moe_last_error.argtypes = []
+            L.moe_version.restype = ctypes.c_char_p
+            L.moe_version.argtypes = []
+            _LIB = L
+    return _LIB
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        raise MoeError(rc, lib().moe_last_error().decode())
+
+
+def shape_of(T: int, H: int, I: int, E: int, k: int, block_m: int = BLOCK_M) -> MoeShape:
+    return MoeShape(T, H, I, E, k, block_m)
+
+
+def moe_workspace_layout(shape: MoeShape) -> MoeLayout:
+    out = MoeLayout()
+    _check(lib().moe_workspace_layout(ctypes.byref(shape), ctypes.byref(out)))
+    return out
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t, dtype, numel=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def moe_route_prologue(shape: MoeShape, topk_idx, route_ws, stream=None):
+    L = moe_workspace_layout(shape)
+    _check(lib().moe_route_prologue(
+        ctypes.byref(shape), _ptr(topk_idx, torch.int32, shape.T * shape.k, "topk_idx"),
+        _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), _stream(stream)))
+
+
+def moe_forward(shape: MoeShape, x, W1, W2, topk_w, route_ws, saved, y, stream=None):
+    L = moe_workspace_layout(shape)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    bf = torch.bfloat16
+    _check(lib().moe_forward(
+        ctypes.byref(shape), _ptr(x, bf, T * H, "x"), _ptr(W1, bf, E * H * 2 * I, "W1"), _ptr(W2, bf, E * I * H, "W2"),
+        _ptr(topk_w, torch.float32, T * k, "topk_w"), _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"),
+        _ptr(saved, torch.uint8, L.saved_bytes, "saved"), _ptr(y, bf, T * H, "y"), _stream(stream)))
+
+
+def moe_backward(shape: MoeShape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, dW1, dW2, dtopk_w,
+                 stream=None):
+    L = moe_workspace_layout(shape)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    bf = torch.bfloat16
+    _check(lib().moe_backward(
+        ctypes.byref(shape), _ptr(dY, bf, T * H, "dY"), _ptr(x, bf, T * H, "x"), _ptr(W1, bf, E * H * 2 * I, "W1"),
+        _ptr(W2, bf, E * I * H, "W2"), _ptr(topk_w, torch.float32, T * k, "topk_w"),
+        _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), _ptr(saved, torch.uint8, L.saved_bytes, "saved"),
+        _ptr(bwd_ws, torch.uint8, L.bwd_bytes, "bwd_ws"), _ptr(dx, bf, T * H, "dx"),
+        _ptr(dW1, bf, E * H * 2 * I, "dW1"), _ptr(dW2, bf, E * I * H, "dW2"),
+        _ptr(dtopk_w, torch.float32, T * k, "dtopk_w"), _stream(stream)))
+
+
+def moe_read_status(shape: MoeShape, route_ws, stream=None) -> list[int]:
+    """Status words (synchronises the stream)."""
+    L = moe_workspace_layout(shape)
+    out = (ctypes.c_int32 * STATUS_WORDS)()
+    _check(lib().moe_read_status(ctypes.byref(shape), _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"),
+                                 ctypes.cast(out, ctypes.c_void_p), _stream(stream)))
+    return list(out)
+
+
+def moe_last_error() -> str:
+    return lib().moe_last_error().decode()
+
+
+def moe_version() -> str:
+    return lib().moe_version().decode()
+
+
+def route_tables(shape: MoeShape, route_ws) -> dict:
+    """Device views of the routing tables inside route_ws (no copy)."""
+    L = moe_workspace_layout(shape)
+
+    def view(off, n):
+        return route_ws[off: off + 4 * n].view(torch.int32)
+
+    return dict(counts=view(L.counts, shape.E), offs=view(L.offs, shape.E + 1), perm=view(L.perm, L.rows_cap),
+                inv=view(L.inv, shape.T * shape.k), tiles=view(L.tiles, L.tiles_cap),
+                status=view(L.status, STATUS_WORDS))
+
+
+def saved_tensors(shape: MoeShape, saved) -> dict:
+    """Device views of h, a, o inside the forward's saved buffer (no copy)."""
+    L = moe_workspace_layout(shape)
+    R, H, I = L.rows_cap, shape.H, shape.I
+
+    def view(off, rows, cols):
+        return saved[off: off + 2 * rows * cols].view(torch.bfloat16).view(rows, cols)
+
+    return dict(h=view(L.h, R, 2 * I), a=view(L.a, R, I), o=view(L.o, R, H))

@@ -1,0 +1,14 @@
+// Instantiations of the grouped GEMM engine: L1_FWD and L2_FWD.
+#include "grouped_gemm.cuh"
+
+namespace moe {
+
+int launch_gemm_l1_fwd(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+    return launch_gemm_flavour<L1_FWD>(a, mA, mB, grid, st);
+}
+
+int launch_gemm_l2_fwd(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+    return launch_gemm_flavour<L2_FWD>(a, mA, mB, grid, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,517 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators) for the six GEMMs of the routed MoE layer.
+//
+// The pages' design (Primus-Turbo "Mega MoE" README, "Pipeline") runs each
+// grouped GEMM tile by tile over the routed rows of every expert, with the
+// token dispatch folded into the GEMM.  Here one launch covers every expert:
+//
+//  * Tiles are 128 routed rows x 256 output columns.  Row-grouped GEMMs walk
+//    (M-tile, N-tile) with the M-tile's expert read from the routing tile
+//    table; weight-gradient GEMMs walk (expert, M-tile, N-tile) with K running
+//    over that expert's block-M padded rows ("variable-K").
+//  * The A operand of L1 / L2-dgrad and the token-side operand of dW1 / dW2
+//    are GATHERED straight from x or dY by the permutation table (16-byte
+//    cp.async into the 128-byte-swizzled layout the MMA reads), so the
+//    dispatched activations are never written to memory, in forward or when
+//    backward recomputes them (README, "Recompute dispatched x").
+//  * Dense operands (weights, saved activations) arrive by TMA.
+//  * Warp roles: warps 0-3 epilogue (TMEM -> registers -> global), warp 4 TMA
+//    producer, warp 5 gather producer, warp 6 MMA issuer and TMEM owner.  A
+//    4-stage shared-memory ring (full/empty mbarriers) feeds the MMA; two
+//    256-column TMEM accumulators let the epilogue of one tile overlap the
+//    main loop of the next.
+//  * Epilogues fuse SwiGLU (L1), the top-k weight (L2), SwiGLU^T with the
+//    routing-weight gradient partials (L2 dgrad).
+//  * Every wait is bounded; on a timeout the CTA raises a status flag,
+//    drains what it issued, frees TMEM and returns.
+#pragma once
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+template <int F>
+struct GemmTraits;
+template <>
+struct GemmTraits<L1_FWD> {
+    static constexpr bool kAGather = true, kBGather = false, kAMN = false, kBMN = true, kWgrad = false;
+};
+template <>
+struct GemmTraits<L2_FWD> {
+    static constexpr bool kAGather = false, kBGather = false, kAMN = false, kBMN = true, kWgrad = false;
+};
+template <>
+struct GemmTraits<L2_DGRAD> {
+    static constexpr bool kAGather = true, kBGather = false, kAMN = false, kBMN = false, kWgrad = false;
+};
+template <>
+struct GemmTraits<L1_DGRAD> {
+    static constexpr bool kAGather = false, kBGather = false, kAMN = false, kBMN = false, kWgrad = false;
+};
+template <>
+struct GemmTraits<DW1> {
+    static constexpr bool kAGather = true, kBGather = false, kAMN = true, kBMN = true, kWgrad = true;
+};
+template <>
+struct GemmTraits<DW2> {
+    static constexpr bool kAGather = false, kBGather = true, kAMN = true, kBMN = true, kWgrad = true;
+};
+
+struct TileCoord {
+    int e;      // expert
+    int m0;     // first routed row (row-grouped) / first output row (weight gradients)
+    int n0;     // first output column (L1_FWD: first gate column)
+    int nt;     // column tile index
+    int nkb;    // number of 64-wide K blocks
+    int krow0;  // first routed row of the expert (weight gradients)
+};
+
+template <int F>
+__device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
+    TileCoord t;
+    if constexpr (GemmTraits<F>::kWgrad) {
+        const int per_e = p.m_tiles * p.n_tiles;
+        t.e = tile / per_e;
+        const int rem = tile - t.e * per_e;
+        const int mt = rem / p.n_tiles;
+        t.nt = rem - mt * p.n_tiles;
+        t.m0 = mt * kBM;
+        t.n0 = t.nt * kBN;
+        const int cnt = __ldg(p.counts + t.e);
+        t.nkb = (cnt + kBK - 1) / kBK;
+        t.krow0 = __ldg(p.offs + t.e);
+    } else {
+        const int mt = tile / p.n_tiles;
+        t.nt = tile - mt * p.n_tiles;
+        t.e = __ldg(p.tiles + mt);
+        t.m0 = mt * kBM;
+        t.n0 = t.nt * (F == L1_FWD ? kBN / 2 : kBN);
+        t.nkb = p.K / kBK;
+        t.krow0 = 0;
+    }
+    return t;
+}
+
+template <int F>
+__device__ __forceinline__ int total_tiles(const GemmArgs& p) {
+    if constexpr (GemmTraits<F>::kWgrad) {
+        return p.E * p.m_tiles * p.n_tiles;
+    } else {
+        int nt = *reinterpret_cast<const volatile int32_t*>(p.status + MOE_STATUS_NUM_TILES);
+        nt = nt < 0 ? 0 : (nt > p.tiles_cap ? p.tiles_cap : nt);
+        return nt * p.n_tiles;
+    }
+}
+
+struct Bars {
+    uint32_t base;
+    __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * s; }
+    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (kStages + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (2 * kStages + a); }
+    __device__ __forceinline__ uint32_t tempty(int a) const { return base + 8u * (2 * kStages + 2 + a); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (2 * kStages + 4); }
+};
+constexpr int kNumBars = 2 * kStages + 5;
+
+// Every lane of the warp waits; the warp proceeds only if all lanes saw the
+// phase complete, so warp-collective instructions never run diverged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------ TMA producer
+template <int F>
+__device__ void role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, int total, uint32_t sA,
+                         uint32_t sB, Bars bars, volatile int* abort) {
+    using Tr = GemmTraits<F>;
+    constexpr uint32_t kTx = (Tr::kAGather ? 0u : (uint32_t)kStageABytes) + (Tr::kBGather ? 0u : (uint32_t)kStageBBytes);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const TileCoord t = decode_tile<F>(tile, p);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+            if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+            const uint32_t fb = bars.full(stage);
+            mbar_arrive_expect_tx(fb, kTx);
+            const uint32_t a = sA + stage * kStageABytes;
+            const uint32_t b = sB + stage * kStageBBytes;
+            const int k0 = kb * kBK;
+            if constexpr (F == L1_FWD) {
+                // W1 viewed as [E][H][2][I]: box = 64 columns of one half x 64 rows of H.
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_load_4d(b + j * 8192, mB, t.n0 + 64 * (j & 1), j >> 1, k0, t.e, fb);
+            } else if constexpr (F == L2_FWD) {
+                tma_load_2d(a, mA, k0, t.m0, fb);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_load_3d(b + j * 8192, mB, t.n0 + 64 * j, k0, t.e, fb);
+            } else if constexpr (F == L2_DGRAD) {
+                tma_load_3d(b, mB, k0, t.n0, t.e, fb);
+            } else if constexpr (F == L1_DGRAD) {
+                tma_load_2d(a, mA, k0, t.m0, fb);
+                tma_load_3d(b, mB, k0, t.n0, t.e, fb);
+            } else if constexpr (F == DW1) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_load_2d(b + j * 8192, mB, t.n0 + 64 * j, t.krow0 + k0, fb);
+            } else {  // DW2
+#pragma unroll
+                for (int j = 0; j < 2; ++j) tma_load_2d(a + j * 8192, mA, t.m0 + 64 * j, t.krow0 + k0, fb);
+            }
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------- gather producer
+// Copies 16-byte chunks of token rows into the 128-byte-swizzled tile layout:
+// chunk c of tile row r lands at r*128 + ((c ^ (r & 7)) * 16).
+template <int F>
+__device__ void role_gather(const GemmArgs& p, int total, uint32_t sA, uint32_t sB, Bars bars, volatile int* abort,
+                            int lane) {
+    using Tr = GemmTraits<F>;
+    const int c = lane & 7;
+    const int rb = lane >> 3;
+    const int H = p.H;
+    const int k = p.k;
+    const __nv_bfloat16* src = p.gsrc;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const TileCoord t = decode_tile<F>(tile, p);
+        if constexpr (!Tr::kAMN) {
+            // K-major A: the tile's 128 routed rows are fixed; K runs along H.
+            int tok[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int s = __ldg(p.perm + t.m0 + rb + 4 * jj);
+                tok[jj] = s >= 0 ? s / k : -1;
+            }
+            for (int kb = 0; kb < t.nkb; ++kb) {
+                if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                const uint32_t a = sA + stage * kStageABytes;
+                const int col = kb * kBK + c * 8;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int r = rb + 4 * jj;
+                    const int tk = tok[jj];
+                    const __nv_bfloat16* g = src + (size_t)(tk < 0 ? 0 : tk) * (size_t)H + col;
+                    cp_async_16(a + r * 128 + ((c ^ (r & 7)) << 4), g, tk < 0 ? 0u : 16u);
+                }
+                cp_async_arrive_noinc(bars.full(stage));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        } else {
+            // MN-major token operand of a weight gradient: the 64 K rows of a
+            // stage are routed rows of expert e; columns run along H.
+            constexpr int kRegions = (F == DW1) ? 2 : 4;
+            const int col0 = (F == DW1) ? t.m0 : t.n0;
+            for (int kb = 0; kb < t.nkb; ++kb) {
+                if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                const uint32_t dst0 = (F == DW1) ? (sA + stage * kStageABytes) : (sB + stage * kStageBBytes);
+                const int row0 = t.krow0 + kb * kBK;
+                const int s0 = __ldg(p.perm + row0 + lane);
+                const int s1 = __ldg(p.perm + row0 + 32 + lane);
+                const int t0 = s0 >= 0 ? s0 / k : -1;
+                const int t1 = s1 >= 0 ? s1 / k : -1;
+                int tq[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) tq[q] = __shfl_sync(0xffffffffu, q < 8 ? t0 : t1, (rb + 4 * q) & 31);
+#pragma unroll
+                for (int g = 0; g < kRegions; ++g) {
+                    const int colg = col0 + 64 * g + 8 * c;
+                    const bool okc = colg < H;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int r = rb + 4 * q;
+                        const bool ok = okc && tq[q] >= 0;
+                        const __nv_bfloat16* gp = src + (ok ? (size_t)tq[q] * (size_t)H + colg : (size_t)0);
+                        cp_async_16(dst0 + g * 8192 + r * 128 + ((c ^ (r & 7)) << 4), gp, ok ? 16u : 0u);
+                    }
+                }
+                cp_async_arrive_noinc(bars.full(stage));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------- MMA issuer
+template <int F>
+__device__ void role_mma(const GemmArgs& p, int total, uint32_t sA, uint32_t sB, Bars bars, uint32_t tmem_base,
+                         volatile int* abort) {
+    using Tr = GemmTraits<F>;
+    constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN, Tr::kAMN, Tr::kBMN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+        const TileCoord t = decode_tile<F>(tile, p);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+            if (!mbar_wait(bars.full(stage), phase, abort)) return;
+            tc_fence_after();
+            if constexpr (Tr::kAGather || Tr::kBGather) fence_proxy_async_smem();
+            const uint32_t a = sA + stage * kStageABytes;
+            const uint32_t b = sB + stage * kStageBBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                // K-major: 16 elements = 32 bytes along the swizzled row.
+                // MN-major: 16 K rows = 2 KiB; LBO = stride of 64-wide MN slabs.
+                const uint64_t ad = Tr::kAMN ? make_sdesc_sw128(a + kk * 2048, 8192, 1024)
+                                             : make_sdesc_sw128(a + kk * 32, 16, 1024);
+                const uint64_t bd = Tr::kBMN ? make_sdesc_sw128(b + kk * 2048, 8192, 1024)
+                                             : make_sdesc_sw128(b + kk * 32, 16, 1024);
+                tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit(bars.empty(stage));
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        tc_commit(bars.tfull(acc));
+    }
+}
+
+// ---------------------------------------------------------------- epilogue
+template <int F>
+__device__ void role_epilogue(const GemmArgs& p, int total, Bars bars, uint32_t tmem_base, volatile int* abort,
+                              int warp, int lane) {
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+        const TileCoord t = decode_tile<F>(tile, p);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!warp_wait(bars.tfull(acc), acc_phase, abort)) return;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(warp * 32) << 16);
+        const int row = t.m0 + warp * 32 + lane;
+
+        if constexpr (F == L1_FWD) {
+            // SwiGLU: accumulator columns [0,128) are gate, [128,256) up.
+            const int I = p.I;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col = t.n0 + 32 * cc;
+                if (col >= I) break;
+                float g[32], u[32];
+                tmem_ld32(tacc + 32 * cc, g);
+                tmem_ld32(tacc + 128 + 32 * cc, u);
+                __nv_bfloat16* hrow = p.out0 + (size_t)row * (size_t)(2 * I);
+                store_bf16x32(hrow + col, g);
+                store_bf16x32(hrow + I + col, u);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) g[j] = g[j] / (1.0f + __expf(-g[j])) * u[j];
+                store_bf16x32(p.out1 + (size_t)row * (size_t)I + col, g);
+            }
+        } else if constexpr (F == L2_FWD) {
+            const int s = __ldg(p.perm + row);
+            const float wv = s >= 0 ? __ldg(p.topk_w + s) : 0.0f;
+            const int H = p.H;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                const int col = t.n0 + 32 * cc;
+                if (col >= H) break;
+                float v[32];
+                tmem_ld32(tacc + 32 * cc, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= wv;
+                store_bf16x32(p.out0 + (size_t)row * (size_t)H + col, v);
+            }
+        } else if constexpr (F == L2_DGRAD) {
+            // g = dY . W2^T at this row; da = w * g; SwiGLU^T from the saved h.
+            const int s = __ldg(p.perm + row);
+            const float wv = s >= 0 ? __ldg(p.topk_w + s) : 0.0f;
+            const int I = p.I;
+            const size_t hoff = (size_t)row * (size_t)(2 * I);
+            const size_t aoff = (size_t)row * (size_t)I;
+            float dws = 0.0f;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                const int col = t.n0 + 32 * cc;
+                if (col >= I) break;
+                float g[32];
+                tmem_ld32(tacc + 32 * cc, g);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c8 = col + 8 * q;
+                    float hg[8], hu[8], av[8];
+                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.h_in + hoff + c8)), hg);
+                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.h_in + hoff + I + c8)), hu);
+                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.a_in + aoff + c8)), av);
+                    float dg[8], du[8], aw[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float gj = g[8 * q + j];
+                        const float da = wv * gj;
+                        const float sg = 1.0f / (1.0f + __expf(-hg[j]));
+                        dg[j] = da * hu[j] * sg * (1.0f + hg[j] * (1.0f - sg));
+                        du[j] = da * hg[j] * sg;
+                        aw[j] = wv * av[j];
+                        dws += gj * av[j];
+                    }
+                    uint4 o;
+                    o.x = pack_bf16x2(dg[0], dg[1]); o.y = pack_bf16x2(dg[2], dg[3]);
+                    o.z = pack_bf16x2(dg[4], dg[5]); o.w = pack_bf16x2(dg[6], dg[7]);
+                    *reinterpret_cast<uint4*>(p.out0 + hoff + c8) = o;
+                    o.x = pack_bf16x2(du[0], du[1]); o.y = pack_bf16x2(du[2], du[3]);
+                    o.z = pack_bf16x2(du[4], du[5]); o.w = pack_bf16x2(du[6], du[7]);
+                    *reinterpret_cast<uint4*>(p.out0 + hoff + I + c8) = o;
+                    o.x = pack_bf16x2(aw[0], aw[1]); o.y = pack_bf16x2(aw[2], aw[3]);
+                    o.z = pack_bf16x2(aw[4], aw[5]); o.w = pack_bf16x2(aw[6], aw[7]);
+                    *reinterpret_cast<uint4*>(p.out1 + aoff + c8) = o;
+                }
+            }
+            p.outf[(size_t)row * (size_t)p.dw_cols + t.nt] = dws;
+        } else if constexpr (F == L1_DGRAD) {
+            const int H = p.H;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                const int col = t.n0 + 32 * cc;
+                if (col >= H) break;
+                float v[32];
+                tmem_ld32(tacc + 32 * cc, v);
+                store_bf16x32(p.out0 + (size_t)row * (size_t)H + col, v);
+            }
+        } else {
+            // Weight gradient of expert e: output rows = H (dW1) or I (dW2).
+            const int M_out = (F == DW1) ? p.H : p.I;
+            const int N_out = (F == DW1) ? 2 * p.I : p.H;
+            const int m = t.m0 + warp * 32 + lane;
+            __nv_bfloat16* dst = p.out0 + (size_t)t.e * (size_t)M_out * (size_t)N_out + (size_t)m * (size_t)N_out;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                const int col = t.n0 + 32 * cc;
+                if (col >= N_out) break;
+                float v[32];
+                if (t.nkb > 0) {
+                    tmem_ld32(tacc + 32 * cc, v);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                }
+                if (m < M_out) store_bf16x32(dst + col, v);
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.tempty(acc));
+    }
+}
+
+template <int F>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const GemmArgs p) {
+    using Tr = GemmTraits<F>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + kStages * kStageABytes;
+    const uint32_t bar_base = sB + kStages * kStageBBytes;
+    uint8_t* tail = base_ptr + kStages * (kStageABytes + kStageBBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * kNumBars);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const Bars bars{bar_base};
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        constexpr uint32_t kFullCount = 1u + ((Tr::kAGather || Tr::kBGather) ? 32u : 0u);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bars.full(s), kFullCount);
+            mbar_init(bars.empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bars.tfull(a), 1);
+            mbar_init(bars.tempty(a), 4);
+        }
+        mbar_init(bars.drain(), 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 6) {
+        tmem_alloc(smem_addr(tmem_slot), 2 * kBN);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        if constexpr (!Tr::kAGather) tma_prefetch_map(&mapA);
+        if constexpr (!Tr::kBGather) tma_prefetch_map(&mapB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = total_tiles<F>(p);
+
+    if (warp == 4) {
+        if (lane == 0) role_tma<F>(&mapA, &mapB, p, total, sA, sB, bars, abort);
+    } else if (warp == 5) {
+        if constexpr (Tr::kAGather || Tr::kBGather) role_gather<F>(p, total, sA, sB, bars, abort, lane);
+        cp_async_wait_all();
+    } else if (warp == 6) {
+        if (lane == 0) {
+            role_mma<F>(p, total, sA, sB, bars, tmem_base, abort);
+            if (*abort) {
+                // let every MMA already issued finish before TMEM is released
+                tc_commit(bars.drain());
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else {
+        role_epilogue<F>(p, total, bars, tmem_base, abort, warp, lane);
+    }
+    if (warp == 4 && lane == 0 && *abort) {
+        // bulk copies already issued land within microseconds; give them time
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 2000000ull) {
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 6) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * kBN);
+    }
+    if (threadIdx.x == 0 && *abort) atomicOr(reinterpret_cast<int*>(p.status + MOE_STATUS_FLAGS), 1);
+}
+
+template <int F>
+int launch_gemm_flavour(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+    // The shared-memory opt-in is a per-device function attribute: set it
+    // once per device (outside any stream capture, on the first call).
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(moe_gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+        if (e != cudaSuccess) return (int)e;
+        done[dev] = true;
+    }
+    moe_gemm_kernel<F><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(mA, mB, a);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,414 @@
+// Host side of the C ABI declared in include/moe_layer.h: argument checks,
+// workspace layout, TMA descriptors and the launch sequence of the layer.
+// No allocation, no synchronisation (except moe_read_status), no host read
+// of device data.
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+int launch_gemm_l1_fwd(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+int launch_gemm_l2_fwd(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+int launch_gemm_l2_dgrad(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+int launch_gemm_l1_dgrad(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+int launch_gemm_dw1(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+int launch_gemm_dw2(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+
+int launch_gemm(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+    switch (f) {
+        case L1_FWD: return launch_gemm_l1_fwd(a, mA, mB, grid, st);
+        case L2_FWD: return launch_gemm_l2_fwd(a, mA, mB, grid, st);
+        case L2_DGRAD: return launch_gemm_l2_dgrad(a, mA, mB, grid, st);
+        case L1_DGRAD: return launch_gemm_l1_dgrad(a, mA, mB, grid, st);
+        case DW1: return launch_gemm_dw1(a, mA, mB, grid, st);
+        case DW2: return launch_gemm_dw2(a, mA, mB, grid, st);
+        default: return (int)cudaErrorInvalidValue;
+    }
+}
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+    g_err = msg;
+    return code;
+}
+
+int cuda_fail(int cerr, const char* what) {
+    g_err = std::string(what) + ": " + cudaGetErrorName((cudaError_t)cerr) + " (" +
+            cudaGetErrorString((cudaError_t)cerr) + ")";
+    return MOE_ECUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int check_shape(const moe_shape* s) {
+    if (!s) return fail(MOE_EINVAL, "shape is NULL");
+    if (s->T < 0) return fail(MOE_EINVAL, "T must be >= 0");
+    if (s->H <= 0 || s->I <= 0) return fail(MOE_EINVAL, "H and I must be > 0");
+    if (s->E < 1 || s->E > 1024) return fail(MOE_EINVAL, "E must be in [1, 1024]");
+    if (s->k < 1 || s->k > s->E) return fail(MOE_EINVAL, "k must be in [1, E]");
+    if (s->H % 64 || s->I % 64) return fail(MOE_EUNSUPPORTED, "H and I must be multiples of 64");
+    if (s->block_m != kBM) return fail(MOE_EUNSUPPORTED, "block_m must be 128");
+    if ((long long)s->T * s->k >= (1ll << 31)) return fail(MOE_EINVAL, "T*k must be < 2^31");
+    const long long tk = (long long)s->T * s->k;
+    const long long cap = tk + (long long)(tk < s->E ? tk : s->E) * (s->block_m - 1);
+    if (cap * (long long)(2 * s->I) >= (1ll << 40) || cap >= (1ll << 31))
+        return fail(MOE_EUNSUPPORTED, "routed rows exceed the supported range");
+    return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- devices
+int num_sms_current(int* out) {
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return 0;
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return 0;
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn(std::string* err) {
+    static EncodeTiledFn fn = nullptr;
+    if (fn) return fn;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+        *err = "cuTensorMapEncodeTiled is not available from the driver";
+        return nullptr;
+    }
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
+// bytes for dims 1..rank-1.
+int make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+             const cuuint32_t* box, const char* what) {
+    std::string err;
+    EncodeTiledFn fn = encode_fn(&err);
+    if (!fn) return fail(MOE_ECUDA, err);
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed for %s (CUresult %d)", what, (int)r);
+        return fail(MOE_ECUDA, buf);
+    }
+    return MOE_OK;
+}
+
+// rows x cols bf16 matrix, box = box_cols x box_rows
+int map_2d(CUtensorMap* m, const void* p, long long rows, int cols, int box_cols, int box_rows, const char* what) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t str[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    return make_map(m, p, 2, dims, str, box, what);
+}
+
+// [E][R][C] bf16, box = box_c x box_r x 1
+int map_3d(CUtensorMap* m, const void* p, int E, int R, int C, int box_c, int box_r, const char* what) {
+    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)R, (cuuint64_t)E};
+    cuuint64_t str[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 2 * (cuuint64_t)R};
+    cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)box_r, 1};
+    return make_map(m, p, 3, dims, str, box, what);
+}
+
+// W1 [E][H][2I] viewed as [E][H][2][I] so that the gate and up halves are
+// addressed separately and a tile never spills from one half into the other.
+int map_w1_halves(CUtensorMap* m, const void* p, int E, int H, int I) {
+    cuuint64_t dims[4] = {(cuuint64_t)I, 2, (cuuint64_t)H, (cuuint64_t)E};
+    cuuint64_t str[3] = {(cuuint64_t)I * 2, (cuuint64_t)I * 4, (cuuint64_t)I * 4 * (cuuint64_t)H};
+    cuuint32_t box[4] = {64, 1, 64, 1};
+    return make_map(m, p, 4, dims, str, box, "W1 (gate/up halves)");
+}
+
+struct Ctx {
+    moe_layout L;
+    int sms;
+};
+
+int prepare(const moe_shape* s, Ctx* c) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    c->sms = 0;
+    return compute_layout(s, &c->L);
+}
+
+// Called after every host-side argument check has passed.
+int query_device(Ctx* c) {
+    int e = num_sms_current(&c->sms);
+    if (e) return cuda_fail(e, "querying the device");
+    return MOE_OK;
+}
+
+int grid_for(int sms, long long tiles) {
+    if (tiles <= 0) return 0;
+    return (int)(tiles < sms ? tiles : sms);
+}
+
+GemmArgs base_args(const moe_shape* s, const moe_layout& L, uint8_t* route) {
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.T = s->T;
+    a.H = s->H;
+    a.I = s->I;
+    a.E = s->E;
+    a.k = s->k;
+    a.tiles_cap = (int)L.tiles_cap;
+    a.dw_cols = L.dw_part_cols;
+    a.perm = reinterpret_cast<const int32_t*>(route + L.perm);
+    a.offs = reinterpret_cast<const int32_t*>(route + L.offs);
+    a.counts = reinterpret_cast<const int32_t*>(route + L.counts);
+    a.tiles = reinterpret_cast<const int32_t*>(route + L.tiles);
+    a.status = reinterpret_cast<int32_t*>(route + L.status);
+    return a;
+}
+
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+int compute_layout(const moe_shape* s, moe_layout* L) {
+    memset(L, 0, sizeof *L);
+    const long long tk = (long long)s->T * s->k;
+    const long long ne = tk < s->E ? tk : s->E;
+    const long long bound = tk + ne * (s->block_m - 1);
+    L->rows_cap = bound / s->block_m * s->block_m;
+    L->tiles_cap = L->rows_cap / s->block_m;
+    const size_t R = (size_t)L->rows_cap;
+    const size_t A = 256;
+    size_t o = 0;
+    L->counts = o; o = align_up(o + 4 * (size_t)s->E, A);
+    L->offs = o; o = align_up(o + 4 * (size_t)(s->E + 1), A);
+    L->perm = o; o = align_up(o + 4 * R, A);
+    L->inv = o; o = align_up(o + 4 * (size_t)tk, A);
+    L->tiles = o; o = align_up(o + 4 * (size_t)L->tiles_cap, A);
+    L->status = o; o = align_up(o + 4 * (size_t)MOE_STATUS_WORDS, A);
+    L->route_bytes = o;
+    o = 0;
+    L->h = o; o = align_up(o + 2 * R * 2 * (size_t)s->I, A);
+    L->a = o; o = align_up(o + 2 * R * (size_t)s->I, A);
+    L->o = o; o = align_up(o + 2 * R * (size_t)s->H, A);
+    L->saved_bytes = o;
+    L->dw_part_cols = (s->I + kBN - 1) / kBN;
+    o = 0;
+    L->dh = o; o = align_up(o + 2 * R * 2 * (size_t)s->I, A);
+    L->aw = o; o = align_up(o + 2 * R * (size_t)s->I, A);
+    L->dxp = o; o = align_up(o + 2 * R * (size_t)s->H, A);
+    L->dw_part = o; o = align_up(o + 4 * R * (size_t)L->dw_part_cols, A);
+    L->bwd_bytes = o;
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_workspace_layout(const moe_shape* shape, moe_layout* out) {
+    if (!out) return fail(MOE_EINVAL, "out is NULL");
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    return compute_layout(shape, out);
+}
+
+int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* route_ws, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!route_ws || (shape->T > 0 && !topk_idx)) return fail(MOE_EINVAL, "NULL pointer argument");
+    if (!aligned16(route_ws) || !aligned16(topk_idx)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if ((rc = query_device(&c))) return rc;
+    int e = launch_route_prologue(*shape, c.L, topk_idx, static_cast<uint8_t*>(route_ws), (cudaStream_t)stream);
+    if (e) return cuda_fail(e, "route prologue launch");
+    return MOE_OK;
+}
+
+int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2, const float* topk_w,
+                void* route_ws, void* saved, void* y, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!W1 || !W2 || !route_ws || !saved || (shape->T > 0 && (!x || !topk_w || !y)))
+        return fail(MOE_EINVAL, "NULL pointer argument");
+    const void* ptrs[] = {x, W1, W2, topk_w, route_ws, saved, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if ((rc = query_device(&c))) return rc;
+    if (shape->T == 0) return MOE_OK;
+    const moe_layout& L = c.L;
+    const int H = shape->H, I = shape->I, E = shape->E;
+    uint8_t* route = static_cast<uint8_t*>(route_ws);
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    auto* h = reinterpret_cast<__nv_bfloat16*>(sv + L.h);
+    auto* a = reinterpret_cast<__nv_bfloat16*>(sv + L.a);
+    auto* o = reinterpret_cast<__nv_bfloat16*>(sv + L.o);
+    cudaStream_t st = (cudaStream_t)stream;
+    CUtensorMap none;
+    memset(&none, 0, sizeof none);
+
+    // L1 grouped GEMM (gathered x) + SwiGLU -> h, a
+    CUtensorMap mW1;
+    if ((rc = map_w1_halves(&mW1, W1, E, H, I))) return rc;
+    GemmArgs g1 = base_args(shape, L, route);
+    g1.K = H;
+    g1.n_tiles = cdiv(I, kBN / 2);
+    g1.gsrc = static_cast<const __nv_bfloat16*>(x);
+    g1.out0 = h;
+    g1.out1 = a;
+    int e = launch_gemm(L1_FWD, g1, none, mW1, grid_for(c.sms, L.tiles_cap * g1.n_tiles), st);
+    if (e) return cuda_fail(e, "L1 grouped GEMM launch");
+
+    // L2 grouped GEMM + routing-weight epilogue -> o
+    CUtensorMap mA, mW2;
+    if ((rc = map_2d(&mA, a, L.rows_cap, I, 64, kBM, "a"))) return rc;
+    if ((rc = map_3d(&mW2, W2, E, I, H, 64, 64, "W2"))) return rc;
+    GemmArgs g2 = base_args(shape, L, route);
+    g2.K = I;
+    g2.n_tiles = cdiv(H, kBN);
+    g2.topk_w = topk_w;
+    g2.out0 = o;
+    e = launch_gemm(L2_FWD, g2, mA, mW2, grid_for(c.sms, L.tiles_cap * g2.n_tiles), st);
+    if (e) return cuda_fail(e, "L2 grouped GEMM launch");
+
+    // combine: y[t] = sum_j o[inv[t, j]]
+    e = launch_combine(o, reinterpret_cast<const int32_t*>(route + L.inv), shape->T, shape->k, H,
+                       static_cast<__nv_bfloat16*>(y), c.sms, st);
+    if (e) return cuda_fail(e, "combine launch");
+    return MOE_OK;
+}
+
+int moe_backward(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
+                 const float* topk_w, void* route_ws, const void* saved, void* bwd_ws, void* dx, void* dW1,
+                 void* dW2, float* dtopk_w, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!W1 || !W2 || !route_ws || !saved || !bwd_ws || !dW1 || !dW2 ||
+        (shape->T > 0 && (!dY || !x || !topk_w || !dx || !dtopk_w)))
+        return fail(MOE_EINVAL, "NULL pointer argument");
+    const void* ptrs[] = {dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, dW1, dW2, dtopk_w};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if ((rc = query_device(&c))) return rc;
+    const moe_layout& L = c.L;
+    const int H = shape->H, I = shape->I, E = shape->E;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (shape->T == 0) {
+        cudaError_t ce = cudaMemsetAsync(dW1, 0, (size_t)E * H * 2 * I * 2, st);
+        if (ce == cudaSuccess) ce = cudaMemsetAsync(dW2, 0, (size_t)E * I * H * 2, st);
+        if (ce != cudaSuccess) return cuda_fail((int)ce, "zeroing weight gradients");
+        return MOE_OK;
+    }
+    uint8_t* route = static_cast<uint8_t*>(route_ws);
+    const uint8_t* sv = static_cast<const uint8_t*>(saved);
+    uint8_t* ws = static_cast<uint8_t*>(bwd_ws);
+    auto* h = reinterpret_cast<const __nv_bfloat16*>(sv + L.h);
+    auto* a = reinterpret_cast<const __nv_bfloat16*>(sv + L.a);
+    auto* dh = reinterpret_cast<__nv_bfloat16*>(ws + L.dh);
+    auto* aw = reinterpret_cast<__nv_bfloat16*>(ws + L.aw);
+    auto* dxp = reinterpret_cast<__nv_bfloat16*>(ws + L.dxp);
+    auto* dwp = reinterpret_cast<float*>(ws + L.dw_part);
+    const auto* inv = reinterpret_cast<const int32_t*>(route + L.inv);
+    CUtensorMap none;
+    memset(&none, 0, sizeof none);
+
+    // L2 dgrad (gathered dY) + SwiGLU^T -> dh, aw, dw_part
+    CUtensorMap mW2k;
+    if ((rc = map_3d(&mW2k, W2, E, I, H, 64, kBN, "W2 (K-major)"))) return rc;
+    GemmArgs g = base_args(shape, L, route);
+    g.K = H;
+    g.n_tiles = cdiv(I, kBN);
+    g.gsrc = static_cast<const __nv_bfloat16*>(dY);
+    g.topk_w = topk_w;
+    g.h_in = h;
+    g.a_in = a;
+    g.out0 = dh;
+    g.out1 = aw;
+    g.outf = dwp;
+    int e = launch_gemm(L2_DGRAD, g, none, mW2k, grid_for(c.sms, L.tiles_cap * g.n_tiles), st);
+    if (e) return cuda_fail(e, "L2 dgrad launch");
+
+    // dW2[e] = aw_e^T . dY_e (variable K)
+    CUtensorMap mAw;
+    if ((rc = map_2d(&mAw, aw, L.rows_cap, I, 64, 64, "aw"))) return rc;
+    GemmArgs g3 = base_args(shape, L, route);
+    g3.m_tiles = cdiv(I, kBM);
+    g3.n_tiles = cdiv(H, kBN);
+    g3.gsrc = static_cast<const __nv_bfloat16*>(dY);
+    g3.out0 = static_cast<__nv_bfloat16*>(dW2);
+    e = launch_gemm(DW2, g3, mAw, none, grid_for(c.sms, (long long)E * g3.m_tiles * g3.n_tiles), st);
+    if (e) return cuda_fail(e, "dW2 launch");
+
+    // dW1[e] = x_e^T . dh_e (variable K, x re-gathered)
+    CUtensorMap mDh64, mDh128;
+    if ((rc = map_2d(&mDh64, dh, L.rows_cap, 2 * I, 64, 64, "dh (rows)"))) return rc;
+    GemmArgs g4 = base_args(shape, L, route);
+    g4.m_tiles = cdiv(H, kBM);
+    g4.n_tiles = cdiv(2 * I, kBN);
+    g4.gsrc = static_cast<const __nv_bfloat16*>(x);
+    g4.out0 = static_cast<__nv_bfloat16*>(dW1);
+    e = launch_gemm(DW1, g4, none, mDh64, grid_for(c.sms, (long long)E * g4.m_tiles * g4.n_tiles), st);
+    if (e) return cuda_fail(e, "dW1 launch");
+
+    // L1 dgrad: dxp = dh . W1[e]^T
+    CUtensorMap mW1k;
+    if ((rc = map_2d(&mDh128, dh, L.rows_cap, 2 * I, 64, kBM, "dh (tiles)"))) return rc;
+    if ((rc = map_3d(&mW1k, W1, E, H, 2 * I, 64, kBN, "W1 (K-major)"))) return rc;
+    GemmArgs g5 = base_args(shape, L, route);
+    g5.K = 2 * I;
+    g5.n_tiles = cdiv(H, kBN);
+    g5.out0 = dxp;
+    e = launch_gemm(L1_DGRAD, g5, mDh128, mW1k, grid_for(c.sms, L.tiles_cap * g5.n_tiles), st);
+    if (e) return cuda_fail(e, "L1 dgrad launch");
+
+    // backward combine and the routing-weight gradient
+    e = launch_combine(dxp, inv, shape->T, shape->k, H, static_cast<__nv_bfloat16*>(dx), c.sms, st);
+    if (e) return cuda_fail(e, "backward combine launch");
+    e = launch_dw_reduce(dwp, L.dw_part_cols, inv, (long long)shape->T * shape->k, dtopk_w, c.sms, st);
+    if (e) return cuda_fail(e, "d(topk_weights) reduce launch");
+    return MOE_OK;
+}
+
+int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!route_ws || !out) return fail(MOE_EINVAL, "NULL pointer argument");
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(out, static_cast<const uint8_t*>(route_ws) + c.L.status,
+                                    sizeof(int32_t) * MOE_STATUS_WORDS, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail((int)e, "reading status words");
+    return MOE_OK;
+}
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a, tcgen05)"; }
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Internal definitions shared by the library's host code and kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_layer.h"
+
+namespace moe {
+
+// Grouped-GEMM tile: 128 routed rows x 256 output columns x 64 of K per stage.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kStageABytes = kBM * kBK * 2;  // 16 KiB
+constexpr int kStageBBytes = kBN * kBK * 2;  // 32 KiB
+constexpr int kGemmThreads = 224;            // 4 epilogue warps, TMA warp, gather warp, MMA warp
+constexpr int kMaxDevices = 64;
+constexpr int kGemmSmemBytes = 1024 + kStages * (kStageABytes + kStageBBytes) + 256;
+
+// The six grouped GEMMs of the layer.
+//   L1_FWD    h = gather(x) . W1[e]            + SwiGLU epilogue -> h, a
+//   L2_FWD    o = w * (a . W2[e])              (weight epilogue)
+//   L2_DGRAD  g = gather(dY) . W2[e]^T         + SwiGLU^T epilogue -> dh, aw, dw_part
+//   L1_DGRAD  dxp = dh . W1[e]^T
+//   DW1       dW1[e] = gather(x)^T . dh        (K = the expert's rows)
+//   DW2       dW2[e] = aw^T . gather(dY)       (K = the expert's rows)
+enum Flavour : int { L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5 };
+
+struct GemmArgs {
+    int T, H, I, E, k;
+    int K;          // contraction length (row-grouped flavours)
+    int n_tiles;    // output column tiles
+    int m_tiles;    // output row tiles per expert (weight-gradient flavours)
+    int tiles_cap;  // bound on routed-row tiles (row-grouped flavours)
+    int dw_cols;    // columns of dw_part
+    const int32_t* perm;
+    const int32_t* offs;
+    const int32_t* counts;
+    const int32_t* tiles;
+    int32_t* status;
+    const __nv_bfloat16* gsrc;  // gathered source rows [T, H] (x or dY)
+    const float* topk_w;
+    const __nv_bfloat16* h_in;  // saved h (L2_DGRAD epilogue)
+    const __nv_bfloat16* a_in;  // saved a (L2_DGRAD epilogue)
+    __nv_bfloat16* out0;
+    __nv_bfloat16* out1;
+    __nv_bfloat16* out2;
+    float* outf;
+};
+
+// Layout of the three workspaces (host only).
+int compute_layout(const moe_shape* s, moe_layout* L);
+
+// Kernel launchers (return a cudaError_t as int).
+int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t* topk_idx, uint8_t* route,
+                          cudaStream_t st);
+int launch_gemm(int flavour, const GemmArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB, int grid,
+                cudaStream_t st);
+int launch_combine(const __nv_bfloat16* rows, const int32_t* inv, int T, int k, int H, __nv_bfloat16* out,
+                   int num_sms, cudaStream_t st);
+int launch_dw_reduce(const float* dw_part, int cols, const int32_t* inv, long long slots, float* out, int num_sms,
+                     cudaStream_t st);
+
+}  // namespace moe

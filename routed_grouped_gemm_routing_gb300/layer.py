@@ -1,0 +1,107 @@
+"""User-facing routed MoE expert layer.
+
+``moe_layer(x, W1, W2, topk_idx, topk_weights)`` is the single autograd op of
+the pages' design (Primus-Turbo "Mega MoE" README, "Key points": one op that
+takes external routing).  Forward calls the routing prologue and the
+forward entry point of the C ABI; backward calls the backward entry point.
+PyTorch only allocates the buffers and supplies the stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class MoEWorkspace:
+    """Caller-owned device buffers of one layer shape (reused across steps)."""
+
+    def __init__(self, T: int, H: int, I: int, E: int, k: int, device=None):
+        self.shape = B.shape_of(T, H, I, E, k)
+        self.layout = B.moe_workspace_layout(self.shape)
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        L = self.layout
+        self.route = torch.empty(max(L.route_bytes, 16), dtype=torch.uint8, device=dev)
+        self.saved = torch.empty(max(L.saved_bytes, 16), dtype=torch.uint8, device=dev)
+        self._bwd = None
+        self.device = dev
+
+    @property
+    def bwd(self):
+        if self._bwd is None:
+            self._bwd = torch.empty(max(self.layout.bwd_bytes, 16), dtype=torch.uint8, device=self.device)
+        return self._bwd
+
+
+def _dims(x, W1, W2, topk_idx):
+    T, H = x.shape
+    E, H1, I2 = W1.shape
+    if H1 != H or I2 % 2 or tuple(W2.shape) != (E, I2 // 2, H):
+        raise ValueError("expected x [T,H], W1 [E,H,2I], W2 [E,I,H]")
+    return T, H, I2 // 2, E, topk_idx.shape[1]
+
+
+class MoEFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, W1, W2, topk_idx, topk_weights, ws=None):
+        T, H, I, E, k = _dims(x, W1, W2, topk_idx)
+        if ws is None or (ws.shape.T, ws.shape.H, ws.shape.I, ws.shape.E, ws.shape.k) != (T, H, I, E, k):
+            ws = MoEWorkspace(T, H, I, E, k, device=x.device)
+        idx = topk_idx if topk_idx.dtype == torch.int32 else topk_idx.to(torch.int32)
+        idx = idx.contiguous()
+        w = topk_weights.to(torch.float32).contiguous()
+        x = x.contiguous()
+        y = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+        B.moe_route_prologue(ws.shape, idx, ws.route)
+        B.moe_forward(ws.shape, x, W1.contiguous(), W2.contiguous(), w, ws.route, ws.saved, y)
+        ctx.save_for_backward(x, W1, W2, w)
+        ctx.ws = ws
+        ctx.w_dtype = topk_weights.dtype
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, W1, W2, w = ctx.saved_tensors
+        ws = ctx.ws
+        s = ws.shape
+        dev = x.device
+        dx = torch.empty_like(x)
+        dW1 = torch.empty_like(W1)
+        dW2 = torch.empty_like(W2)
+        dw = torch.empty(s.T, s.k, dtype=torch.float32, device=dev)
+        B.moe_backward(s, dy.to(torch.bfloat16).contiguous(), x, W1.contiguous(), W2.contiguous(), w, ws.route,
+                       ws.saved, ws.bwd, dx, dW1, dW2, dw)
+        return dx, dW1, dW2, None, dw.to(ctx.w_dtype), None
+
+
+def moe_layer(x, W1, W2, topk_idx, topk_weights, workspace: MoEWorkspace | None = None):
+    """y = sum_j topk_weights[:, j] * SwiGLU-MLP_{topk_idx[:, j]}(x), bf16.
+
+    x bf16 [T,H]; W1 bf16 [E,H,2I] (gate | up); W2 bf16 [E,I,H];
+    topk_idx int32/int64 [T,k] (-1 = dropped slot); topk_weights float [T,k].
+    Differentiable in x, W1, W2 and topk_weights."""
+    return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace)
+
+
+def train_step_from_host(x_h, topk_idx_h, topk_w_h, dY_h, W1, W2, ws: MoEWorkspace, outs: dict):
+    """One forward+backward of the layer fed from pinned HOST buffers.
+
+    Copies x, topk_idx, topk_weights and dY host->device, runs the routing
+    prologue, forward and backward through the C ABI, and copies y, dx and
+    d(topk_weights) back to pinned host buffers (outs['y_h'], outs['dx_h'],
+    outs['dw_h']).  The weight gradients stay on the device (outs['dW1'],
+    outs['dW2']) where an optimizer would consume them.  All on the current
+    stream; returns without synchronising."""
+    s = ws.shape
+    x = outs["x"]
+    x.copy_(x_h, non_blocking=True)
+    outs["idx"].copy_(topk_idx_h, non_blocking=True)
+    outs["w"].copy_(topk_w_h, non_blocking=True)
+    outs["dY"].copy_(dY_h, non_blocking=True)
+    B.moe_route_prologue(s, outs["idx"], ws.route)
+    B.moe_forward(s, x, W1, W2, outs["w"], ws.route, ws.saved, outs["y"])
+    B.moe_backward(s, outs["dY"], x, W1, W2, outs["w"], ws.route, ws.saved, ws.bwd, outs["dx"], outs["dW1"],
+                   outs["dW2"], outs["dw"])
+    outs["y_h"].copy_(outs["y"], non_blocking=True)
+    outs["dx_h"].copy_(outs["dx"], non_blocking=True)
+    outs["dw_h"].copy_(outs["dw"], non_blocking=True)

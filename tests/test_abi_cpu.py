@@ -1,0 +1,78 @@
+"""CPU-only checks of the C-ABI library: it builds for sm_103a, loads, exports
+every function include/moe_layer.h declares, computes the workspace layout on
+the host, and rejects bad shapes and pointers without touching a GPU."""
+import ctypes
+
+import pytest
+
+import oracle
+from routed_grouped_gemm_routing_gb300 import binding as B
+from routed_grouped_gemm_routing_gb300 import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = B.declared_functions()
+    assert set(names) >= {"moe_workspace_layout", "moe_route_prologue", "moe_forward", "moe_backward",
+                          "moe_read_status", "moe_last_error", "moe_version"}
+    for n in names:
+        assert hasattr(lib, n), f"{n} is declared but not exported"
+    assert "sm_103a" in B.moe_version()
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(64, 128, 64, 8, 2), (4096, 2048, 1408, 64, 6), (8192, 7168, 2048, 256, 8),
+                                       (4096, 7168, 3072, 384, 6), (1, 64, 64, 1024, 3), (0, 64, 64, 4, 2)])
+def test_layout(lib, T, H, I, E, k):
+    L = B.moe_workspace_layout(B.shape_of(T, H, I, E, k))
+    assert L.rows_cap == oracle.rows_cap(T, E, k, 128)
+    assert L.tiles_cap == L.rows_cap // 128
+    assert L.dw_part_cols == (I + 255) // 256
+    offs = [L.counts, L.offs, L.perm, L.inv, L.tiles, L.status]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert L.offs >= L.counts + 4 * E and L.perm >= L.offs + 4 * (E + 1)
+    assert L.inv >= L.perm + 4 * L.rows_cap and L.tiles >= L.inv + 4 * T * k
+    assert L.status >= L.tiles + 4 * L.tiles_cap and L.route_bytes >= L.status + 64
+    R = L.rows_cap
+    assert L.a >= L.h + 2 * R * 2 * I and L.o >= L.a + 2 * R * I and L.saved_bytes >= L.o + 2 * R * H
+    assert L.aw >= L.dh + 2 * R * 2 * I and L.dxp >= L.aw + 2 * R * I
+    assert L.dw_part >= L.dxp + 2 * R * H and L.bwd_bytes >= L.dw_part + 4 * R * L.dw_part_cols
+
+
+@pytest.mark.parametrize("bad,code", [((64, 100, 64, 8, 2, 128), B.MOE_EUNSUPPORTED),
+                                      ((64, 128, 96, 8, 2, 128), B.MOE_EUNSUPPORTED),
+                                      ((64, 128, 64, 8, 9, 128), B.MOE_EINVAL),
+                                      ((64, 128, 64, 2000, 2, 128), B.MOE_EINVAL),
+                                      ((-1, 128, 64, 8, 2, 128), B.MOE_EINVAL),
+                                      ((64, 128, 64, 8, 2, 64), B.MOE_EUNSUPPORTED),
+                                      ((64, 0, 64, 8, 2, 128), B.MOE_EINVAL)])
+def test_bad_shapes_rejected_on_host(lib, bad, code):
+    s = B.MoeShape(*bad)
+    out = B.MoeLayout()
+    assert lib.moe_workspace_layout(ctypes.byref(s), ctypes.byref(out)) == code
+    assert B.moe_last_error() != ""
+    # entry points reject the shape before touching any device
+    assert lib.moe_route_prologue(ctypes.byref(s), None, None, None) == code
+    assert lib.moe_forward(ctypes.byref(s), *([None] * 8)) == code
+
+
+def test_null_shape_and_null_pointers(lib):
+    assert lib.moe_workspace_layout(None, None) == B.MOE_EINVAL
+    s = B.shape_of(64, 128, 64, 8, 2)
+    out = B.MoeLayout()
+    assert lib.moe_workspace_layout(ctypes.byref(s), None) == B.MOE_EINVAL
+
+
+def test_null_and_misaligned_pointers_rejected_before_device_use(lib):
+    s = B.shape_of(64, 128, 64, 8, 2)
+    assert lib.moe_route_prologue(ctypes.byref(s), None, None, None) == B.MOE_EINVAL
+    assert lib.moe_forward(ctypes.byref(s), *([None] * 8)) == B.MOE_EINVAL
+    assert lib.moe_backward(ctypes.byref(s), *([None] * 13)) == B.MOE_EINVAL
+    fake = [4096 * (i + 1) for i in range(13)]
+    fake[3] += 4  # misaligned topk_w
+    assert lib.moe_backward(ctypes.byref(s), *fake) == B.MOE_EUNSUPPORTED
+    assert "aligned" in B.moe_last_error()
