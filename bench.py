@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE expert layer on GB300: one step = routing
+prologue + forward + backward of the whole layer through the C ABI.
+
+Default workload: the DeepSeek-V3-shaped layer (T=8192 tokens, hidden 7168,
+intermediate 2048, 256 experts, top-8; 22.5 GB of bf16 weights), synthetic
+seeded inputs.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config v3]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Metric: useful FLOPs per second (padding excluded: 6*H*I per routed slot
+forward, 12*H*I backward), also routed tokens/s and the fraction of the
+measured BF16 dense peak.  Under torchrun each rank runs an independent
+replica of the layer on its own GPU (the layer does not shard on one GPU;
+scaling is weak) and the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_FLOP_FACTOR = {  # useful FLOPs per routed slot, in units of H*I
+    "gemm_l1_fwd": 4.0, "gemm_l2_fwd": 2.0, "gemm_l2_dgrad": 2.0, "gemm_dw2": 2.0, "gemm_dw1": 4.0,
+    "gemm_l1_dgrad": 4.0,
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "routed_grouped_gemm_routing_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(shape, inputs, n_tok, seed=0):
+    """Host copies of a bounded sample of the workload for the CPU oracle:
+    n_tok tokens (forward, dx, d topk_weights) and the weight gradients of one
+    typically loaded expert.  Returns (callable running it, useful FLOPs,
+    description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from routed_grouped_gemm_routing_gb300.workloads import bf16_bits
+
+    E, k, H, I = shape.E, shape.k, shape.H, shape.I
+    idx_all = inputs["topk_idx"].cpu().numpy()
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(shape.T, size=n_tok, replace=False))
+    idx = idx_all[toks].astype(np.int64)
+    involved = np.unique(idx[(idx >= 0) & (idx < E)])
+    remap = np.full(E, -1, np.int64)
+    remap[involved] = np.arange(len(involved))
+    idx_t = np.where((idx >= 0) & (idx < E), remap[np.clip(idx, 0, E - 1)], -1).astype(np.int32)
+    it = torch.as_tensor(involved, device=inputs["x"].device)
+    tt = torch.as_tensor(toks, device=inputs["x"].device)
+    W1t, W2t = bf16_bits(inputs["W1"][it]), bf16_bits(inputs["W2"][it])
+    xt, dYt = bf16_bits(inputs["x"][tt]), bf16_bits(inputs["dY"][tt])
+    wt = inputs["topk_w"][tt].cpu().numpy().astype(np.float32)
+    counts = np.bincount(idx_all.ravel()[idx_all.ravel() >= 0], minlength=E)
+    e = int(np.argsort(counts, kind="stable")[E // 2])  # median-loaded expert
+    remap_e = np.full(E, -1, np.int64)
+    remap_e[e] = 0
+    valid = (idx_all >= 0) & (idx_all < E)
+    idx_e = np.where(valid, remap_e[np.clip(idx_all, 0, E - 1)], -1).astype(np.int32)
+    et = torch.as_tensor([e], device=inputs["x"].device)
+    W1e, W2e = bf16_bits(inputs["W1"][et]), bf16_bits(inputs["W2"][et])
+    xa, dYa = bf16_bits(inputs["x"]), bf16_bits(inputs["dY"])
+    wa = inputs["topk_w"].cpu().numpy().astype(np.float32)
+
+    def run():
+        oracle.forward(xt, W1t, W2t, idx_t, wt)
+        oracle.backward_tokens(xt, W1t, W2t, idx_t, wt, dYt)
+        oracle.backward_experts(xa, W1e, W2e, idx_e, wa, dYa)
+
+    slots = int(((idx >= 0) & (idx < E)).sum())
+    flops = 6.0 * H * I * slots + 6.0 * H * I * slots + 6.0 * H * I * int(counts[e])
+    desc = (f"{n_tok} tokens ({slots} routed slots): forward, dx, d topk_weights; plus dW1/dW2 of one "
+            f"median-loaded expert ({int(counts[e])} rows); oracle FP32, useful FLOPs counted as in the metric")
+    return run, flops, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+METRIC = "MoE layer fwd+bwd TFLOP/s (useful FLOPs) & routed tokens/s; % of GB300 BF16 dense peak"
+
+
+def config_dict(shape, world):
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    label = " (DeepSeek-V3-shaped expert layer)" if shape.name == "v3" else ""
+    return {"workload": f"{shape.name}: T={T} H={H} I={I} E={E} k={k}{label}",
+            "T": T, "H": H, "I": I, "E": E, "k": k, "block_m": 128,
+            "l2": "inputs larger than L2 (weights alone are many times the 129 MB L2)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+# -------------------------------------------------------------- main arms
+def run_reference(args):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from routed_grouped_gemm_routing_gb300.workloads import CONFIGS, make_layer_inputs
+
+    shape = CONFIGS[args.config]
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inputs = make_layer_inputs(shape, seed=args.seed, device=dev)
+    run, flops, desc = oracle_sample(shape, inputs, n_tok=args.ref_tokens, seed=args.seed)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = flops * args.steps / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": config_dict(shape, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from routed_grouped_gemm_routing_gb300 import binding as B
+    from routed_grouped_gemm_routing_gb300 import build
+    from routed_grouped_gemm_routing_gb300.layer import MoEWorkspace, train_step_from_host
+    from routed_grouped_gemm_routing_gb300.workloads import CONFIGS, make_layer_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    B.lib()
+    peaks, peaks_src = load_peaks()
+
+    shape = CONFIGS[args.config]
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    inp = make_layer_inputs(shape, seed=args.seed + rank, device=dev)
+    ws = MoEWorkspace(T, H, I, E, k, device=dev)
+    s = ws.shape
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty_like(y)
+    dW1 = torch.empty_like(inp["W1"])
+    dW2 = torch.empty_like(inp["W2"])
+    dw = torch.empty(T, k, dtype=torch.float32, device=dev)
+
+    def step():
+        B.moe_route_prologue(s, inp["topk_idx"], ws.route)
+        B.moe_forward(s, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
+        B.moe_backward(s, inp["dY"], inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, ws.bwd,
+                       dx, dW1, dW2, dw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = B.moe_read_status(s, ws.route)
+    if status[B.STATUS_FLAGS] != 0:
+        raise RuntimeError(f"kernel status flags {status[B.STATUS_FLAGS]:#x} after warm-up")
+
+    # timed region: K steps, every kernel bracketed by events for per-kernel times
+    trace = B.KernelTrace(max_launches=16 * args.steps)
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    time.sleep(0.3)
+    stream = torch.cuda.current_stream()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    with trace:
+        for _ in range(args.steps):
+            step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = B.moe_read_status(s, ws.route)
+    if status[B.STATUS_FLAGS] != 0:
+        raise RuntimeError(f"kernel status flags {status[B.STATUS_FLAGS]:#x} in the timed region")
+
+    flops_step = shape.flops_forward() + shape.flops_backward()
+    secs = ms / 1e3
+    value = world * flops_step * args.steps / secs / 1e12
+    tok_s = world * shape.slots * args.steps / secs
+
+    # per-kernel device times (rank-local)
+    per = {}
+    for name, d in trace.durations_ms():
+        per.setdefault(name, []).append(d)
+    launches_per_step = trace.count / args.steps
+    kernels = {n: {"launches": len(v), "avg_ms": statistics.mean(v), "total_ms": sum(v),
+                   "share": sum(v) / ms} for n, v in per.items()}
+    gemms = {n: v for n, v in kernels.items() if n in GEMM_FLOP_FACTOR}
+    dom = max(gemms, key=lambda n: gemms[n]["total_ms"])
+    dom_flops = GEMM_FLOP_FACTOR[dom] * H * I * shape.slots
+    achieved = dom_flops / (gemms[dom]["avg_ms"] / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        ent = tj.get(args.config, {}).get(dom)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            traffic = ent["bytes_per_launch"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops_sustained ({peaks_src}); burst {float(peaks['bf16_tflops']):.1f}",
+                "algorithmic_flops_per_launch": dom_flops}
+
+    # end to end through the public API, from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        outs = dict(x=torch.empty_like(inp["x"]), idx=torch.empty_like(inp["topk_idx"]),
+                    w=torch.empty_like(inp["topk_w"]), dY=torch.empty_like(inp["dY"]), y=y, dx=dx, dW1=dW1,
+                    dW2=dW2, dw=dw)
+        host = {n: inp[n].cpu().pin_memory() for n in ("x", "topk_idx", "topk_w", "dY")}
+        outs["y_h"] = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        outs["dx_h"] = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        outs["dw_h"] = torch.empty(T, k, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            train_step_from_host(host["x"], host["topk_idx"], host["topk_w"], host["dY"], inp["W1"], inp["W2"], ws,
+                                 outs)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+        d2h = sum(outs[n].numel() * outs[n].element_size() for n in ("y_h", "dx_h", "dw_h"))
+        e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps,
+               "note": "x, topk_idx, topk_weights, dY copied in from pinned host memory and y, dx, "
+                       "d topk_weights copied out every step; dW1/dW2 stay on the device"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        run, flops, desc = oracle_sample(shape, inp, n_tok=args.cpu_tokens, seed=args.seed)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            reps += 1
+            if time.perf_counter() - t0 >= args.cpu_seconds:
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": flops * reps / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "host_cores_available": cpu_cores(), "kind": "oracle", "sample": f"{reps} x ({desc})",
+               "seconds": dt}
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded Gaussian inputs and weights, Gaussian-logit top-k routing)",
+        "config": config_dict(shape, world),
+        "routed_tokens_per_s": tok_s,
+        "pct_bf16_peak_burst": 100.0 * value / world / float(peaks["bf16_tflops"]),
+        "pct_bf16_peak_sustained": 100.0 * value / world / float(peaks["bf16_tflops_sustained"]),
+        "peaks_source": peaks_src,
+        "clocks": clk,
+        "gpu_launches": int(trace.count),
+        "launches_per_step": launches_per_step,
+        "kernels": kernels,
+        "roofline": roofline,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="v3")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-tokens", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

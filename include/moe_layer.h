@@ -130,6 +130,19 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
  * `out` (int32[16]).  SYNCHRONISES `stream`; not for use under capture. */
 int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, void* stream);
 
+/* Tracing.  moe_trace_begin hands the library `capacity` CUDA events
+ * (cudaEvent_t passed as void*, created by the caller with timing enabled).
+ * Until moe_trace_end, each kernel the library launches from this thread is
+ * bracketed by two of them, recorded on the launch stream: events[2i] just
+ * before and events[2i+1] just after the i-th launch, so the caller can read
+ * each kernel's device time with cudaEventElapsedTime.  Launches beyond
+ * capacity/2 are counted but not recorded.  moe_trace_end returns the number
+ * of launches since moe_trace_begin; moe_trace_kernel(i) names the i-th
+ * ("" when out of range).  Host only; no synchronisation. */
+int moe_trace_begin(void* const* events, int capacity);
+int moe_trace_end(void);
+const char* moe_trace_kernel(int i);
+
 /* Message for the last non-zero return on this thread ("" if none). */
 const char* moe_last_error(void);
 

@@ -157,57 +157,74 @@ void FN(oracle_backward_tokens_)(int T, int H, int I, int E, int k,
 }
 
 /* Full weight gradients of the listed experts (each sums over every slot
- * routed to it, in token order):
+ * routed to it, in increasing slot order s = t*k + j):
  *   dW2[e,i,c]   = sum_slots a[i] * w * dY[t,c]
  *   dW1[e,h,i]   = sum_slots x[t,h] * dhg[i]
  *   dW1[e,h,I+i] = sum_slots x[t,h] * dhu[i]
- * An expert that receives no slot gets exactly zero. */
+ * An expert that receives no slot gets exactly zero.  The per-slot terms are
+ * computed first; each output row is then summed over the slots in order
+ * (rows are independent, so they are spread over threads). */
 void FN(oracle_backward_experts_)(int T, int H, int I, int E, int k,
                                   const IN_T* x, const IN_T* W1, const IN_T* W2,
                                   const int32_t* topk_idx, const W_T* topk_w, const IN_T* dY,
                                   int n_exp, const int32_t* exp_list,
                                   REAL* dW1_out, REAL* dW2_out) {
+    int32_t* slots = (int32_t*)malloc(sizeof(int32_t) * (size_t)((int64_t)T * k + 1));
+    for (int n = 0; n < n_exp; ++n) {
+        int e = exp_list[n];
+        REAL* dW1 = dW1_out + (size_t)n * H * 2 * I;
+        REAL* dW2 = dW2_out + (size_t)n * I * H;
+        int ns = 0;
+        if (e >= 0 && e < E)
+            for (int64_t s = 0; s < (int64_t)T * k; ++s)
+                if (topk_idx[s] == e) slots[ns++] = (int32_t)s;
+        size_t w1off = (size_t)(e < 0 ? 0 : e) * H * 2 * I, w2off = (size_t)(e < 0 ? 0 : e) * I * H;
+        /* per-slot terms: a (times w), dhg, dhu */
+        REAL* aw = (REAL*)malloc(sizeof(REAL) * ((size_t)ns * I + 1));
+        REAL* dh = (REAL*)malloc(sizeof(REAL) * ((size_t)ns * 2 * I + 1));
 #pragma omp parallel
-    {
-        REAL* hg = (REAL*)malloc(sizeof(REAL) * (size_t)I);
-        REAL* hu = (REAL*)malloc(sizeof(REAL) * (size_t)I);
-        REAL* a = (REAL*)malloc(sizeof(REAL) * (size_t)I);
-        REAL* o = (REAL*)malloc(sizeof(REAL) * (size_t)H);
-        REAL* da = (REAL*)malloc(sizeof(REAL) * (size_t)I);
-        REAL* dhg = (REAL*)malloc(sizeof(REAL) * (size_t)I);
-        REAL* dhu = (REAL*)malloc(sizeof(REAL) * (size_t)I);
+        {
+            REAL* hg = (REAL*)malloc(sizeof(REAL) * (size_t)I);
+            REAL* hu = (REAL*)malloc(sizeof(REAL) * (size_t)I);
+            REAL* a = (REAL*)malloc(sizeof(REAL) * (size_t)I);
+            REAL* o = (REAL*)malloc(sizeof(REAL) * (size_t)H);
+            REAL* da = (REAL*)malloc(sizeof(REAL) * (size_t)I);
 #pragma omp for schedule(dynamic, 1)
-        for (int n = 0; n < n_exp; ++n) {
-            int e = exp_list[n];
-            REAL* dW1 = dW1_out + (size_t)n * H * 2 * I;
-            REAL* dW2 = dW2_out + (size_t)n * I * H;
-            for (size_t q = 0; q < (size_t)H * 2 * I; ++q) dW1[q] = 0;
-            for (size_t q = 0; q < (size_t)I * H; ++q) dW2[q] = 0;
-            if (e < 0 || e >= E) continue;
-            size_t w1off = (size_t)e * H * 2 * I, w2off = (size_t)e * I * H;
-            for (int t = 0; t < T; ++t) {
-                for (int j = 0; j < k; ++j) {
-                    if (topk_idx[(size_t)t * k + j] != e) continue;
-                    FN(slot_forward_)(H, I, x, (size_t)t * H, W1, w1off, W2, w2off, hg, hu, a, o);
-                    REAL wv = (REAL)topk_w[(size_t)t * k + j];
-                    FN(slot_backward_)(H, I, dY, (size_t)t * H, wv, W2, w2off, hg, hu, da, dhg, dhu);
-                    for (int i = 0; i < I; ++i) {
-                        REAL* row = dW2 + (size_t)i * H;
-                        for (int c = 0; c < H; ++c) row[c] += a[i] * wv * LD(dY, (size_t)t * H + (size_t)c);
-                    }
-                    for (int h = 0; h < H; ++h) {
-                        REAL xv = LD(x, (size_t)t * H + (size_t)h);
-                        REAL* row = dW1 + (size_t)h * 2 * I;
-                        for (int i = 0; i < I; ++i) {
-                            row[i] += xv * dhg[i];
-                            row[I + i] += xv * dhu[i];
-                        }
-                    }
-                }
+            for (int q = 0; q < ns; ++q) {
+                int64_t s = slots[q];
+                int t = (int)(s / k);
+                FN(slot_forward_)(H, I, x, (size_t)t * H, W1, w1off, W2, w2off, hg, hu, a, o);
+                REAL wv = (REAL)topk_w[s];
+                REAL* dhq = dh + (size_t)q * 2 * I;
+                FN(slot_backward_)(H, I, dY, (size_t)t * H, wv, W2, w2off, hg, hu, da, dhq, dhq + I);
+                for (int i = 0; i < I; ++i) aw[(size_t)q * I + i] = a[i] * wv;
+            }
+            free(hg); free(hu); free(a); free(o); free(da);
+        }
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < I; ++i) {
+            REAL* row = dW2 + (size_t)i * H;
+            for (int c = 0; c < H; ++c) row[c] = 0;
+            for (int q = 0; q < ns; ++q) {
+                int t = (int)(slots[q] / k);
+                REAL av = aw[(size_t)q * I + i];
+                for (int c = 0; c < H; ++c) row[c] += av * LD(dY, (size_t)t * H + (size_t)c);
             }
         }
-        free(hg); free(hu); free(a); free(o); free(da); free(dhg); free(dhu);
+#pragma omp parallel for schedule(static)
+        for (int h = 0; h < H; ++h) {
+            REAL* row = dW1 + (size_t)h * 2 * I;
+            for (int i = 0; i < 2 * I; ++i) row[i] = 0;
+            for (int q = 0; q < ns; ++q) {
+                int t = (int)(slots[q] / k);
+                REAL xv = LD(x, (size_t)t * H + (size_t)h);
+                const REAL* dhq = dh + (size_t)q * 2 * I;
+                for (int i = 0; i < 2 * I; ++i) row[i] += xv * dhq[i];
+            }
+        }
+        free(aw); free(dh);
     }
+    free(slots);
 }
 
 #undef FN

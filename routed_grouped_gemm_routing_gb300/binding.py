@@ -68,6 +68,12 @@ def lib():
             L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
             for n in ("moe_workspace_layout", "moe_route_prologue", "moe_forward", "moe_backward", "moe_read_status"):
                 getattr(L, n).restype = ctypes.c_int
+            L.moe_trace_begin.argtypes = [vp, ctypes.c_int]
+            L.moe_trace_begin.restype = ctypes.c_int
+            L.moe_trace_end.argtypes = []
+            L.moe_trace_end.restype = ctypes.c_int
+            L.moe_trace_kernel.argtypes = [ctypes.c_int]
+            L.moe_trace_kernel.restype = ctypes.c_char_p
             L.moe_last_error.restype = ctypes.c_char_p
             L.moe_last_error.argtypes = []
             L.moe_version.restype = ctypes.c_char_p
@@ -180,3 +186,31 @@ def saved_tensors(shape: MoeShape, saved) -> dict:
         return saved[off: off + 2 * rows * cols].view(torch.bfloat16).view(rows, cols)
 
     return dict(h=view(L.h, R, 2 * I), a=view(L.a, R, I), o=view(L.o, R, H))
+
+
+class KernelTrace:
+    """Brackets every kernel the library launches from this thread with a
+    pair of CUDA events (moe_trace_begin / moe_trace_end), for per-kernel
+    device times.  Events are created here with timing enabled."""
+
+    def __init__(self, max_launches: int):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_launches)]
+        for ev in self.events:  # force creation of the underlying event
+            ev.record()
+        self._arr = (ctypes.c_void_p * len(self.events))(*[ev.cuda_event for ev in self.events])
+        self.names: list[str] = []
+        self.count = 0
+
+    def __enter__(self):
+        _check(lib().moe_trace_begin(ctypes.cast(self._arr, ctypes.c_void_p), len(self.events)))
+        return self
+
+    def __exit__(self, *exc):
+        self.count = lib().moe_trace_end()
+        self.names = [lib().moe_trace_kernel(i).decode() for i in range(self.count)]
+        return False
+
+    def durations_ms(self) -> list[tuple[str, float]]:
+        """(kernel name, device ms) per traced launch; call after synchronising."""
+        n = min(self.count, len(self.events) // 2)
+        return [(self.names[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(n)]

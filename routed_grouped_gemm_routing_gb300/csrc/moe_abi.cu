@@ -17,7 +17,7 @@ int launch_gemm_l1_dgrad(const GemmArgs&, const CUtensorMap&, const CUtensorMap&
 int launch_gemm_dw1(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 int launch_gemm_dw2(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 
-int launch_gemm(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+int launch_gemm_raw(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
     switch (f) {
         case L1_FWD: return launch_gemm_l1_fwd(a, mA, mB, grid, st);
         case L2_FWD: return launch_gemm_l2_fwd(a, mA, mB, grid, st);
@@ -30,8 +30,44 @@ int launch_gemm(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorM
 }
 
 namespace {
+const char* const kGemmNames[] = {"gemm_l1_fwd", "gemm_l2_fwd", "gemm_l2_dgrad", "gemm_l1_dgrad", "gemm_dw1", "gemm_dw2"};
+void trace_pre(cudaStream_t st);
+void trace_post(cudaStream_t st, const char* name);
+}  // namespace
+
+int launch_gemm(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+    if (grid <= 0) return 0;
+    trace_pre(st);
+    const int e = launch_gemm_raw(f, a, mA, mB, grid, st);
+    trace_post(st, kGemmNames[f]);
+    return e;
+}
+
+namespace {
 
 thread_local std::string g_err;
+
+// ------------------------------------------------------------------ tracing
+constexpr int kTraceNames = 4096;
+struct Trace {
+    void* const* events = nullptr;
+    int capacity = 0;
+    int n = 0;
+    const char* names[kTraceNames];
+};
+thread_local Trace g_trace;
+
+void trace_pre(cudaStream_t st) {
+    Trace& t = g_trace;
+    if (t.events && 2 * t.n + 1 < t.capacity) cudaEventRecord((cudaEvent_t)t.events[2 * t.n], st);
+}
+void trace_post(cudaStream_t st, const char* name) {
+    Trace& t = g_trace;
+    if (!t.events) return;
+    if (2 * t.n + 1 < t.capacity) cudaEventRecord((cudaEvent_t)t.events[2 * t.n + 1], st);
+    if (t.n < kTraceNames) t.names[t.n] = name;
+    ++t.n;
+}
 
 int fail(int code, const std::string& msg) {
     g_err = msg;
@@ -157,10 +193,20 @@ int prepare(const moe_shape* s, Ctx* c) {
     return compute_layout(s, &c->L);
 }
 
-// Called after every host-side argument check has passed.
-int query_device(Ctx* c) {
-    int e = num_sms_current(&c->sms);
-    if (e) return cuda_fail(e, "querying the device");
+// Called after every host-side argument check has passed.  Makes the device
+// that owns `data` current on the calling thread (which may be a thread, such
+// as an autograd worker, on which no CUDA context is current yet: tensor-map
+// encoding needs one), then reads its SM count.
+int query_device(Ctx* c, const void* data) {
+    cudaPointerAttributes pa;
+    cudaError_t e = cudaPointerGetAttributes(&pa, data);
+    if (e != cudaSuccess) return cuda_fail((int)e, "querying the device of a workspace pointer");
+    if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged)
+        return fail(MOE_EINVAL, "workspace pointers must be device memory");
+    e = cudaSetDevice(pa.device);
+    if (e != cudaSuccess) return cuda_fail((int)e, "selecting the device");
+    int r = num_sms_current(&c->sms);
+    if (r) return cuda_fail(r, "querying the device");
     return MOE_OK;
 }
 
@@ -242,8 +288,10 @@ int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* ro
     if (rc) return rc;
     if (!route_ws || (shape->T > 0 && !topk_idx)) return fail(MOE_EINVAL, "NULL pointer argument");
     if (!aligned16(route_ws) || !aligned16(topk_idx)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
-    if ((rc = query_device(&c))) return rc;
+    if ((rc = query_device(&c, route_ws))) return rc;
+    trace_pre((cudaStream_t)stream);
     int e = launch_route_prologue(*shape, c.L, topk_idx, static_cast<uint8_t*>(route_ws), (cudaStream_t)stream);
+    trace_post((cudaStream_t)stream, "route_prologue");
     if (e) return cuda_fail(e, "route prologue launch");
     return MOE_OK;
 }
@@ -258,7 +306,7 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     const void* ptrs[] = {x, W1, W2, topk_w, route_ws, saved, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
-    if ((rc = query_device(&c))) return rc;
+    if ((rc = query_device(&c, route_ws))) return rc;
     if (shape->T == 0) return MOE_OK;
     const moe_layout& L = c.L;
     const int H = shape->H, I = shape->I, E = shape->E;
@@ -296,8 +344,10 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     if (e) return cuda_fail(e, "L2 grouped GEMM launch");
 
     // combine: y[t] = sum_j o[inv[t, j]]
+    trace_pre(st);
     e = launch_combine(o, reinterpret_cast<const int32_t*>(route + L.inv), shape->T, shape->k, H,
                        static_cast<__nv_bfloat16*>(y), c.sms, st);
+    trace_post(st, "combine_fwd");
     if (e) return cuda_fail(e, "combine launch");
     return MOE_OK;
 }
@@ -314,7 +364,7 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     const void* ptrs[] = {dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, dW1, dW2, dtopk_w};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
-    if ((rc = query_device(&c))) return rc;
+    if ((rc = query_device(&c, route_ws))) return rc;
     const moe_layout& L = c.L;
     const int H = shape->H, I = shape->I, E = shape->E;
     cudaStream_t st = (cudaStream_t)stream;
@@ -387,9 +437,13 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     if (e) return cuda_fail(e, "L1 dgrad launch");
 
     // backward combine and the routing-weight gradient
+    trace_pre(st);
     e = launch_combine(dxp, inv, shape->T, shape->k, H, static_cast<__nv_bfloat16*>(dx), c.sms, st);
+    trace_post(st, "combine_bwd");
     if (e) return cuda_fail(e, "backward combine launch");
+    trace_pre(st);
     e = launch_dw_reduce(dwp, L.dw_part_cols, inv, (long long)shape->T * shape->k, dtopk_w, c.sms, st);
+    trace_post(st, "dw_reduce");
     if (e) return cuda_fail(e, "d(topk_weights) reduce launch");
     return MOE_OK;
 }
@@ -405,6 +459,26 @@ int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, 
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail((int)e, "reading status words");
     return MOE_OK;
+}
+
+int moe_trace_begin(void* const* events, int capacity) {
+    if (capacity < 0 || (capacity > 0 && !events)) return fail(MOE_EINVAL, "bad trace event array");
+    g_trace.events = capacity > 0 ? events : nullptr;
+    g_trace.capacity = capacity;
+    g_trace.n = 0;
+    return MOE_OK;
+}
+
+int moe_trace_end(void) {
+    const int n = g_trace.n;
+    g_trace.events = nullptr;
+    g_trace.capacity = 0;
+    return n;
+}
+
+const char* moe_trace_kernel(int i) {
+    if (i < 0 || i >= g_trace.n || i >= kTraceNames) return "";
+    return g_trace.names[i];
 }
 
 const char* moe_last_error(void) { return g_err.c_str(); }
