@@ -126,6 +126,31 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
                  const float* topk_w, void* route_ws, const void* saved, void* bwd_ws,
                  void* dx, void* dW1, void* dW2, float* dtopk_w, void* stream);
 
+/* Inference forward for callers that cannot allocate device memory when
+ * they run the layer: for example a plugin inside an inference engine that
+ * gets no workspace from its host, or a serving loop that must not call
+ * cudaMalloc (it can synchronise the device).  The pages have no counterpart
+ * of this entry point.
+ * Same inputs and output as moe_route_prologue followed by moe_forward
+ * (topk_idx int32[T,k], y bf16[T,H] overwritten), but the routing tables and
+ * the per-row intermediates live in a static 32 MiB device array inside the
+ * library, which every GPU that loads the library holds until exit.  Allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - Size limit: route_bytes (rounded up to 256) + saved_bytes of
+ *    moe_workspace_layout must be <= 32 MiB (e.g. the V3 shape up to T = 1,
+ *    the T=64, H=128, I=64, E=8, k=2 shape with room to spare); larger shapes
+ *    return MOE_EUNSUPPORTED with a message naming the bytes needed.
+ *  - The first call on each device looks up the array's device address with
+ *    cudaGetSymbolAddress (the device owning W1 is made current); make that
+ *    first call before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind; each call
+ *    rewrites every table it reads first, so results never depend on an
+ *    earlier call.  Calls that overlap on the GPU (other streams, other host
+ *    threads) race on the array: serialise them.
+ *  - Forward only: the saved activations are not kept for a backward pass. */
+int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* W1, const void* W2,
+                        const int32_t* topk_idx, const float* topk_w, void* y, void* stream);
+
 /* Copies the MOE_STATUS_WORDS status words of route_ws to host memory
  * `out` (int32[16]).  SYNCHRONISES `stream`; not for use under capture. */
 int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, void* stream);

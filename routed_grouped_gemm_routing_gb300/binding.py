@@ -214,3 +214,18 @@ class KernelTrace:
         """(kernel name, device ms) per traced launch; call after synchronising."""
         n = min(self.count, len(self.events) // 2)
         return [(self.names[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(n)]
+
+
+def moe_forward_noalloc(shape: MoeShape, x, W1, W2, topk_idx, topk_w, y, stream=None):
+    """Routing prologue + forward with the library's static scratch instead of
+    caller workspaces (for callers that cannot allocate device memory; see
+    include/moe_layer.h).  Overwrites y; keeps nothing for a backward pass."""
+    L = lib()
+    fn = L.moe_forward_noalloc
+    fn.argtypes = [ctypes.POINTER(MoeShape)] + [ctypes.c_void_p] * 7
+    fn.restype = ctypes.c_int
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    bf = torch.bfloat16
+    _check(fn(ctypes.byref(shape), _ptr(x, bf, T * H, "x"), _ptr(W1, bf, E * H * 2 * I, "W1"),
+              _ptr(W2, bf, E * I * H, "W2"), _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
+              _ptr(topk_w, torch.float32, T * k, "topk_w"), _ptr(y, bf, T * H, "y"), _stream(stream)))

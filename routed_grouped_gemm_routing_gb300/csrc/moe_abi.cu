@@ -4,6 +4,7 @@
 // of device data.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "moe_internal.h"
@@ -486,3 +487,72 @@ const char* moe_last_error(void) { return g_err.c_str(); }
 const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a, tcgen05)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Inference forward for callers that cannot allocate device memory.
+//
+// The routing tables and the per-row intermediates (h, a, o) live in one
+// file-scope device array instead of caller workspaces.  Every GPU that loads
+// this library holds the array (kNoAllocScratchBytes) until the process exits.
+// Host code cannot use the array's name as a device address, so the address is
+// fetched once per device with cudaGetSymbolAddress, with that device current.
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (set-up on the
+// first call per device).
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail((int)e, "querying the current device");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_EUNSUPPORTED, "device index out of range");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return cuda_fail((int)(e != cudaSuccess ? e : cudaErrorInvalidSymbol),
+                                                     "cudaGetSymbolAddress of the static scratch");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* W1, const void* W2,
+                                   const int32_t* topk_idx, const float* topk_w, void* y, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!W1 || !W2 || (shape->T > 0 && (!x || !topk_idx || !topk_w || !y)))
+        return fail(MOE_EINVAL, "NULL pointer argument");
+    const void* ptrs[] = {x, W1, W2, topk_idx, topk_w, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    const size_t route_part = align_up(c.L.route_bytes, 256);
+    const size_t need = route_part + c.L.saved_bytes;
+    if (need > kNoAllocScratchBytes) {
+        char buf[200];
+        snprintf(buf, sizeof buf,
+                 "moe_forward_noalloc: this shape needs %zu bytes of scratch, more than the %zu-byte static "
+                 "scratch; use moe_forward with caller workspaces",
+                 need, kNoAllocScratchBytes);
+        return fail(MOE_EUNSUPPORTED, buf);
+    }
+    if ((rc = query_device(&c, W1))) return rc;
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
+    uint8_t* route = static_cast<uint8_t*>(scratch);
+    // The prologue rewrites every table and status word it owns on each call,
+    // so nothing left by an earlier call is read.
+    if ((rc = moe_route_prologue(shape, topk_idx, route, stream))) return rc;
+    return moe_forward(shape, x, W1, W2, topk_w, route, route + route_part, y, stream);
+}
