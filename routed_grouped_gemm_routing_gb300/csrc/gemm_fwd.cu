@@ -3,12 +3,12 @@
 
 namespace moe {
 
-int launch_gemm_l1_fwd(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
-    return launch_gemm_flavour<L1_FWD>(a, mA, mB, grid, st);
+int launch_gemm_l1_fwd(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
+    return launch_gemm_flavour<L1_FWD>(a, m, grid, st);
 }
 
-int launch_gemm_l2_fwd(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
-    return launch_gemm_flavour<L2_FWD>(a, mA, mB, grid, st);
+int launch_gemm_l2_fwd(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
+    return launch_gemm_flavour<L2_FWD>(a, m, grid, st);
 }
 
 }  // namespace moe

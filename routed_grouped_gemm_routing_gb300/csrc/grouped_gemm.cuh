@@ -288,18 +288,35 @@ __device__ void role_mma(const GemmArgs& p, int total, uint32_t sA, uint32_t sB,
 }
 
 // ---------------------------------------------------------------- epilogue
+// Each epilogue warp owns 32 TMEM lanes = 32 rows of the tile.  Results are
+// written into this warp's 8 KiB staging area in shared memory, in the
+// swizzled layout of the output tensor map, and leave through TMA bulk
+// stores of whole 32-row boxes (full 64- or 128-byte row segments) while the
+// warp goes on with the next chunk.
+struct OutMaps {
+    const CUtensorMap* c0;
+    const CUtensorMap* c1;
+};
+
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&p)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+}
+
 template <int F>
-__device__ void role_epilogue(const GemmArgs& p, int total, Bars bars, uint32_t tmem_base, volatile int* abort,
-                              int warp, int lane) {
+__device__ void role_epilogue(const GemmArgs& p, OutMaps om, int total, Bars bars, uint32_t tmem_base,
+                              uint32_t stage, volatile int* abort, int warp, int lane) {
     int it = 0;
+    uint32_t nstore = 0;  // 64-column boxes stored by this warp (picks the staging half)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
         const TileCoord t = decode_tile<F>(tile, p);
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        if (!warp_wait(bars.tfull(acc), acc_phase, abort)) return;
+        if (!warp_wait(bars.tfull(acc), acc_phase, abort)) break;
         tc_fence_after();
         const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(warp * 32) << 16);
-        const int row = t.m0 + warp * 32 + lane;
+        const int row0 = t.m0 + warp * 32;  // first row of this warp's box
+        const int row = row0 + lane;
 
         if constexpr (F == L1_FWD) {
             // SwiGLU: accumulator columns [0,128) are gate, [128,256) up.
@@ -311,26 +328,25 @@ __device__ void role_epilogue(const GemmArgs& p, int total, Bars bars, uint32_t 
                 float g[32], u[32];
                 tmem_ld32(tacc + 32 * cc, g);
                 tmem_ld32(tacc + 128 + 32 * cc, u);
-                __nv_bfloat16* hrow = p.out0 + (size_t)row * (size_t)(2 * I);
-                store_bf16x32(hrow + col, g);
-                store_bf16x32(hrow + I + col, u);
+                uint32_t pg[16], pu[16], pa[16];
+                pack32(g, pg);
+                pack32(u, pu);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) g[j] = g[j] / (1.0f + __expf(-g[j])) * u[j];
-                store_bf16x32(p.out1 + (size_t)row * (size_t)I + col, g);
-            }
-        } else if constexpr (F == L2_FWD) {
-            const int s = __ldg(p.perm + row);
-            const float wv = s >= 0 ? __ldg(p.topk_w + s) : 0.0f;
-            const int H = p.H;
-#pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                const int col = t.n0 + 32 * cc;
-                if (col >= H) break;
-                float v[32];
-                tmem_ld32(tacc + 32 * cc, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= wv;
-                store_bf16x32(p.out0 + (size_t)row * (size_t)H + col, v);
+                pack32(g, pa);
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                stage_row_sw64(stage, lane, pg);
+                stage_row_sw64(stage + 2048, lane, pu);
+                stage_row_sw64(stage + 4096, lane, pa);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(om.c0, col, row0, stage);
+                    tma_store_2d(om.c0, I + col, row0, stage + 2048);
+                    tma_store_2d(om.c1, col, row0, stage + 4096);
+                    bulk_commit();
+                }
             }
         } else if constexpr (F == L2_DGRAD) {
             // g = dY . W2^T at this row; da = w * g; SwiGLU^T from the saved h.
@@ -346,6 +362,7 @@ __device__ void role_epilogue(const GemmArgs& p, int total, Bars bars, uint32_t 
                 if (col >= I) break;
                 float g[32];
                 tmem_ld32(tacc + 32 * cc, g);
+                uint32_t pg[16], pu[16], pa[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int c8 = col + 8 * q;
@@ -364,58 +381,84 @@ __device__ void role_epilogue(const GemmArgs& p, int total, Bars bars, uint32_t 
                         aw[j] = wv * av[j];
                         dws += gj * av[j];
                     }
-                    uint4 o;
-                    o.x = pack_bf16x2(dg[0], dg[1]); o.y = pack_bf16x2(dg[2], dg[3]);
-                    o.z = pack_bf16x2(dg[4], dg[5]); o.w = pack_bf16x2(dg[6], dg[7]);
-                    *reinterpret_cast<uint4*>(p.out0 + hoff + c8) = o;
-                    o.x = pack_bf16x2(du[0], du[1]); o.y = pack_bf16x2(du[2], du[3]);
-                    o.z = pack_bf16x2(du[4], du[5]); o.w = pack_bf16x2(du[6], du[7]);
-                    *reinterpret_cast<uint4*>(p.out0 + hoff + I + c8) = o;
-                    o.x = pack_bf16x2(aw[0], aw[1]); o.y = pack_bf16x2(aw[2], aw[3]);
-                    o.z = pack_bf16x2(aw[4], aw[5]); o.w = pack_bf16x2(aw[6], aw[7]);
-                    *reinterpret_cast<uint4*>(p.out1 + aoff + c8) = o;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        pg[4 * q + j] = pack_bf16x2(dg[2 * j], dg[2 * j + 1]);
+                        pu[4 * q + j] = pack_bf16x2(du[2 * j], du[2 * j + 1]);
+                        pa[4 * q + j] = pack_bf16x2(aw[2 * j], aw[2 * j + 1]);
+                    }
+                }
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                stage_row_sw64(stage, lane, pg);
+                stage_row_sw64(stage + 2048, lane, pu);
+                stage_row_sw64(stage + 4096, lane, pa);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(om.c0, col, row0, stage);
+                    tma_store_2d(om.c0, I + col, row0, stage + 2048);
+                    tma_store_2d(om.c1, col, row0, stage + 4096);
+                    bulk_commit();
                 }
             }
             p.outf[(size_t)row * (size_t)p.dw_cols + t.nt] = dws;
-        } else if constexpr (F == L1_DGRAD) {
-            const int H = p.H;
-#pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                const int col = t.n0 + 32 * cc;
-                if (col >= H) break;
-                float v[32];
-                tmem_ld32(tacc + 32 * cc, v);
-                store_bf16x32(p.out0 + (size_t)row * (size_t)H + col, v);
-            }
         } else {
-            // Weight gradient of expert e: output rows = H (dW1) or I (dW2).
-            const int M_out = (F == DW1) ? p.H : p.I;
+            // One output: o (L2 fwd, times the routing weight), dxp (L1 dgrad),
+            // or the weight gradient of expert e (dW1, dW2).
+            constexpr bool kW = GemmTraits<F>::kWgrad;
             const int N_out = (F == DW1) ? 2 * p.I : p.H;
-            const int m = t.m0 + warp * 32 + lane;
-            __nv_bfloat16* dst = p.out0 + (size_t)t.e * (size_t)M_out * (size_t)N_out + (size_t)m * (size_t)N_out;
+            float wv = 1.0f;
+            if constexpr (F == L2_FWD) {
+                const int s = __ldg(p.perm + row);
+                wv = s >= 0 ? __ldg(p.topk_w + s) : 0.0f;
+            }
+            const bool have_acc = !kW || t.nkb > 0;
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                const int col = t.n0 + 32 * cc;
+            for (int c64 = 0; c64 < 4; ++c64) {
+                const int col = t.n0 + 64 * c64;
                 if (col >= N_out) break;
-                float v[32];
-                if (t.nkb > 0) {
-                    tmem_ld32(tacc + 32 * cc, v);
-                } else {
+                uint32_t pk[32];
+                {
+                    float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                    for (int h = 0; h < 2; ++h) {
+                        if (have_acc) {
+                            tmem_ld32(tacc + 64 * c64 + 32 * h, v);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pk[16 * h + j] = pack_bf16x2(wv * v[2 * j], wv * v[2 * j + 1]);
+                    }
                 }
-                if (m < M_out) store_bf16x32(dst + col, v);
+                const uint32_t buf = stage + (nstore & 1u) * 4096u;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                stage_row_sw128(buf, lane, pk);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kW) tma_store_3d(om.c0, col, row0, t.e, buf);
+                    else tma_store_2d(om.c0, col, row0, buf);
+                    bulk_commit();
+                }
+                ++nstore;
             }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.tempty(acc));
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
 }
 
 template <int F>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ CUtensorMap mapC0, const __grid_constant__ CUtensorMap mapC1,
                     const GemmArgs p) {
     using Tr = GemmTraits<F>;
     extern __shared__ uint8_t smem_raw[];
@@ -424,8 +467,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * kStageABytes;
-    const uint32_t bar_base = sB + kStages * kStageBBytes;
-    uint8_t* tail = base_ptr + kStages * (kStageABytes + kStageBBytes);
+    const uint32_t sStage = sB + kStages * kStageBBytes;  // 4 x 8 KiB epilogue staging
+    const uint32_t bar_base = sStage + kEpiWarps * kStageEpiBytes;
+    uint8_t* tail = base_ptr + (bar_base - base);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * kNumBars);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const Bars bars{bar_base};
@@ -441,7 +485,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bars.tfull(a), 1);
-            mbar_init(bars.tempty(a), 4);
+            mbar_init(bars.tempty(a), kEpiWarps);
         }
         mbar_init(bars.drain(), 1);
         *abort = 0;
@@ -454,6 +498,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 4 && lane == 0) {
         if constexpr (!Tr::kAGather) tma_prefetch_map(&mapA);
         if constexpr (!Tr::kBGather) tma_prefetch_map(&mapB);
+        tma_prefetch_map(&mapC0);
+        if constexpr (F == L1_FWD || F == L2_DGRAD) tma_prefetch_map(&mapC1);
     }
     tc_fence_before();
     __syncthreads();
@@ -478,7 +524,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     } else {
-        role_epilogue<F>(p, total, bars, tmem_base, abort, warp, lane);
+        role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, total, bars, tmem_base, sStage + warp * kStageEpiBytes, abort,
+                         warp, lane);
     }
     if (warp == 4 && lane == 0 && *abort) {
         // bulk copies already issued land within microseconds; give them time
@@ -497,7 +544,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <int F>
-int launch_gemm_flavour(const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+int launch_gemm_flavour(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (outside any stream capture, on the first call).
     static bool done[kMaxDevices] = {};
@@ -510,7 +557,7 @@ int launch_gemm_flavour(const GemmArgs& a, const CUtensorMap& mA, const CUtensor
         if (e != cudaSuccess) return (int)e;
         done[dev] = true;
     }
-    moe_gemm_kernel<F><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(mA, mB, a);
+    moe_gemm_kernel<F><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(m.a, m.b, m.c0, m.c1, a);
     return (int)cudaGetLastError();
 }
 

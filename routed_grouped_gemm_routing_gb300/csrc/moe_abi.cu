@@ -11,21 +11,21 @@
 
 namespace moe {
 
-int launch_gemm_l1_fwd(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-int launch_gemm_l2_fwd(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-int launch_gemm_l2_dgrad(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-int launch_gemm_l1_dgrad(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-int launch_gemm_dw1(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-int launch_gemm_dw2(const GemmArgs&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+int launch_gemm_l1_fwd(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_l2_fwd(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_l2_dgrad(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_l1_dgrad(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_dw1(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_dw2(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 
-int launch_gemm_raw(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     switch (f) {
-        case L1_FWD: return launch_gemm_l1_fwd(a, mA, mB, grid, st);
-        case L2_FWD: return launch_gemm_l2_fwd(a, mA, mB, grid, st);
-        case L2_DGRAD: return launch_gemm_l2_dgrad(a, mA, mB, grid, st);
-        case L1_DGRAD: return launch_gemm_l1_dgrad(a, mA, mB, grid, st);
-        case DW1: return launch_gemm_dw1(a, mA, mB, grid, st);
-        case DW2: return launch_gemm_dw2(a, mA, mB, grid, st);
+        case L1_FWD: return launch_gemm_l1_fwd(a, m, grid, st);
+        case L2_FWD: return launch_gemm_l2_fwd(a, m, grid, st);
+        case L2_DGRAD: return launch_gemm_l2_dgrad(a, m, grid, st);
+        case L1_DGRAD: return launch_gemm_l1_dgrad(a, m, grid, st);
+        case DW1: return launch_gemm_dw1(a, m, grid, st);
+        case DW2: return launch_gemm_dw2(a, m, grid, st);
         default: return (int)cudaErrorInvalidValue;
     }
 }
@@ -36,10 +36,10 @@ void trace_pre(cudaStream_t st);
 void trace_post(cudaStream_t st, const char* name);
 }  // namespace
 
-int launch_gemm(int f, const GemmArgs& a, const CUtensorMap& mA, const CUtensorMap& mB, int grid, cudaStream_t st) {
+int launch_gemm(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     if (grid <= 0) return 0;
     trace_pre(st);
-    const int e = launch_gemm_raw(f, a, mA, mB, grid, st);
+    const int e = launch_gemm_raw(f, a, m, grid, st);
     trace_post(st, kGemmNames[f]);
     return e;
 }
@@ -141,13 +141,13 @@ EncodeTiledFn encode_fn(std::string* err) {
 // bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
 // bytes for dims 1..rank-1.
 int make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-             const cuuint32_t* box, const char* what) {
+             const cuuint32_t* box, const char* what, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     std::string err;
     EncodeTiledFn fn = encode_fn(&err);
     if (!fn) return fail(MOE_ECUDA, err);
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char buf[160];
@@ -157,12 +157,14 @@ int make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, 
     return MOE_OK;
 }
 
-// rows x cols bf16 matrix, box = box_cols x box_rows
+// rows x cols bf16 matrix, box = box_cols x box_rows; a 64-byte-wide box uses
+// the 64-byte swizzle, a 128-byte-wide box the 128-byte swizzle.
 int map_2d(CUtensorMap* m, const void* p, long long rows, int cols, int box_cols, int box_rows, const char* what) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t str[1] = {(cuuint64_t)cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    return make_map(m, p, 2, dims, str, box, what);
+    return make_map(m, p, 2, dims, str, box, what,
+                    box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // [E][R][C] bf16, box = box_c x box_r x 1
@@ -317,31 +319,30 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     auto* a = reinterpret_cast<__nv_bfloat16*>(sv + L.a);
     auto* o = reinterpret_cast<__nv_bfloat16*>(sv + L.o);
     cudaStream_t st = (cudaStream_t)stream;
-    CUtensorMap none;
-    memset(&none, 0, sizeof none);
-
     // L1 grouped GEMM (gathered x) + SwiGLU -> h, a
-    CUtensorMap mW1;
-    if ((rc = map_w1_halves(&mW1, W1, E, H, I))) return rc;
+    GemmMaps m1;
+    memset(&m1, 0, sizeof m1);
+    if ((rc = map_w1_halves(&m1.b, W1, E, H, I))) return rc;
+    if ((rc = map_2d(&m1.c0, h, L.rows_cap, 2 * I, 32, 32, "h (store)"))) return rc;
+    if ((rc = map_2d(&m1.c1, a, L.rows_cap, I, 32, 32, "a (store)"))) return rc;
     GemmArgs g1 = base_args(shape, L, route);
     g1.K = H;
     g1.n_tiles = cdiv(I, kBN / 2);
     g1.gsrc = static_cast<const __nv_bfloat16*>(x);
-    g1.out0 = h;
-    g1.out1 = a;
-    int e = launch_gemm(L1_FWD, g1, none, mW1, grid_for(c.sms, L.tiles_cap * g1.n_tiles), st);
+    int e = launch_gemm(L1_FWD, g1, m1, grid_for(c.sms, L.tiles_cap * g1.n_tiles), st);
     if (e) return cuda_fail(e, "L1 grouped GEMM launch");
 
     // L2 grouped GEMM + routing-weight epilogue -> o
-    CUtensorMap mA, mW2;
-    if ((rc = map_2d(&mA, a, L.rows_cap, I, 64, kBM, "a"))) return rc;
-    if ((rc = map_3d(&mW2, W2, E, I, H, 64, 64, "W2"))) return rc;
+    GemmMaps m2;
+    memset(&m2, 0, sizeof m2);
+    if ((rc = map_2d(&m2.a, a, L.rows_cap, I, 64, kBM, "a"))) return rc;
+    if ((rc = map_3d(&m2.b, W2, E, I, H, 64, 64, "W2"))) return rc;
+    if ((rc = map_2d(&m2.c0, o, L.rows_cap, H, 64, 32, "o (store)"))) return rc;
     GemmArgs g2 = base_args(shape, L, route);
     g2.K = I;
     g2.n_tiles = cdiv(H, kBN);
     g2.topk_w = topk_w;
-    g2.out0 = o;
-    e = launch_gemm(L2_FWD, g2, mA, mW2, grid_for(c.sms, L.tiles_cap * g2.n_tiles), st);
+    e = launch_gemm(L2_FWD, g2, m2, grid_for(c.sms, L.tiles_cap * g2.n_tiles), st);
     if (e) return cuda_fail(e, "L2 grouped GEMM launch");
 
     // combine: y[t] = sum_j o[inv[t, j]]
@@ -385,12 +386,12 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     auto* dxp = reinterpret_cast<__nv_bfloat16*>(ws + L.dxp);
     auto* dwp = reinterpret_cast<float*>(ws + L.dw_part);
     const auto* inv = reinterpret_cast<const int32_t*>(route + L.inv);
-    CUtensorMap none;
-    memset(&none, 0, sizeof none);
-
     // L2 dgrad (gathered dY) + SwiGLU^T -> dh, aw, dw_part
-    CUtensorMap mW2k;
-    if ((rc = map_3d(&mW2k, W2, E, I, H, 64, kBN, "W2 (K-major)"))) return rc;
+    GemmMaps m;
+    memset(&m, 0, sizeof m);
+    if ((rc = map_3d(&m.b, W2, E, I, H, 64, kBN, "W2 (K-major)"))) return rc;
+    if ((rc = map_2d(&m.c0, dh, L.rows_cap, 2 * I, 32, 32, "dh (store)"))) return rc;
+    if ((rc = map_2d(&m.c1, aw, L.rows_cap, I, 32, 32, "aw (store)"))) return rc;
     GemmArgs g = base_args(shape, L, route);
     g.K = H;
     g.n_tiles = cdiv(I, kBN);
@@ -398,43 +399,44 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     g.topk_w = topk_w;
     g.h_in = h;
     g.a_in = a;
-    g.out0 = dh;
-    g.out1 = aw;
     g.outf = dwp;
-    int e = launch_gemm(L2_DGRAD, g, none, mW2k, grid_for(c.sms, L.tiles_cap * g.n_tiles), st);
+    int e = launch_gemm(L2_DGRAD, g, m, grid_for(c.sms, L.tiles_cap * g.n_tiles), st);
     if (e) return cuda_fail(e, "L2 dgrad launch");
 
     // dW2[e] = aw_e^T . dY_e (variable K)
-    CUtensorMap mAw;
-    if ((rc = map_2d(&mAw, aw, L.rows_cap, I, 64, 64, "aw"))) return rc;
+    GemmMaps m3;
+    memset(&m3, 0, sizeof m3);
+    if ((rc = map_2d(&m3.a, aw, L.rows_cap, I, 64, 64, "aw"))) return rc;
+    if ((rc = map_3d(&m3.c0, dW2, E, I, H, 64, 32, "dW2 (store)"))) return rc;
     GemmArgs g3 = base_args(shape, L, route);
     g3.m_tiles = cdiv(I, kBM);
     g3.n_tiles = cdiv(H, kBN);
     g3.gsrc = static_cast<const __nv_bfloat16*>(dY);
-    g3.out0 = static_cast<__nv_bfloat16*>(dW2);
-    e = launch_gemm(DW2, g3, mAw, none, grid_for(c.sms, (long long)E * g3.m_tiles * g3.n_tiles), st);
+    e = launch_gemm(DW2, g3, m3, grid_for(c.sms, (long long)E * g3.m_tiles * g3.n_tiles), st);
     if (e) return cuda_fail(e, "dW2 launch");
 
     // dW1[e] = x_e^T . dh_e (variable K, x re-gathered)
-    CUtensorMap mDh64, mDh128;
-    if ((rc = map_2d(&mDh64, dh, L.rows_cap, 2 * I, 64, 64, "dh (rows)"))) return rc;
+    GemmMaps m4;
+    memset(&m4, 0, sizeof m4);
+    if ((rc = map_2d(&m4.b, dh, L.rows_cap, 2 * I, 64, 64, "dh (rows)"))) return rc;
+    if ((rc = map_3d(&m4.c0, dW1, E, H, 2 * I, 64, 32, "dW1 (store)"))) return rc;
     GemmArgs g4 = base_args(shape, L, route);
     g4.m_tiles = cdiv(H, kBM);
     g4.n_tiles = cdiv(2 * I, kBN);
     g4.gsrc = static_cast<const __nv_bfloat16*>(x);
-    g4.out0 = static_cast<__nv_bfloat16*>(dW1);
-    e = launch_gemm(DW1, g4, none, mDh64, grid_for(c.sms, (long long)E * g4.m_tiles * g4.n_tiles), st);
+    e = launch_gemm(DW1, g4, m4, grid_for(c.sms, (long long)E * g4.m_tiles * g4.n_tiles), st);
     if (e) return cuda_fail(e, "dW1 launch");
 
     // L1 dgrad: dxp = dh . W1[e]^T
-    CUtensorMap mW1k;
-    if ((rc = map_2d(&mDh128, dh, L.rows_cap, 2 * I, 64, kBM, "dh (tiles)"))) return rc;
-    if ((rc = map_3d(&mW1k, W1, E, H, 2 * I, 64, kBN, "W1 (K-major)"))) return rc;
+    GemmMaps m5;
+    memset(&m5, 0, sizeof m5);
+    if ((rc = map_2d(&m5.a, dh, L.rows_cap, 2 * I, 64, kBM, "dh (tiles)"))) return rc;
+    if ((rc = map_3d(&m5.b, W1, E, H, 2 * I, 64, kBN, "W1 (K-major)"))) return rc;
+    if ((rc = map_2d(&m5.c0, dxp, L.rows_cap, H, 64, 32, "dxp (store)"))) return rc;
     GemmArgs g5 = base_args(shape, L, route);
     g5.K = 2 * I;
     g5.n_tiles = cdiv(H, kBN);
-    g5.out0 = dxp;
-    e = launch_gemm(L1_DGRAD, g5, mDh128, mW1k, grid_for(c.sms, L.tiles_cap * g5.n_tiles), st);
+    e = launch_gemm(L1_DGRAD, g5, m5, grid_for(c.sms, L.tiles_cap * g5.n_tiles), st);
     if (e) return cuda_fail(e, "L1 dgrad launch");
 
     // backward combine and the routing-weight gradient

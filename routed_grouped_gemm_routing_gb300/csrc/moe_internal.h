@@ -19,7 +19,9 @@ constexpr int kStageABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kStageBBytes = kBN * kBK * 2;  // 32 KiB
 constexpr int kGemmThreads = 224;            // 4 epilogue warps, TMA warp, gather warp, MMA warp
 constexpr int kMaxDevices = 64;
-constexpr int kGemmSmemBytes = 1024 + kStages * (kStageABytes + kStageBBytes) + 256;
+constexpr int kEpiWarps = 4;
+constexpr int kStageEpiBytes = 8192;  // per epilogue warp: TMA-store staging
+constexpr int kGemmSmemBytes = 1024 + kStages * (kStageABytes + kStageBBytes) + kEpiWarps * kStageEpiBytes + 256;
 
 // The six grouped GEMMs of the layer.
 //   L1_FWD    h = gather(x) . W1[e]            + SwiGLU epilogue -> h, a
@@ -46,10 +48,13 @@ struct GemmArgs {
     const float* topk_w;
     const __nv_bfloat16* h_in;  // saved h (L2_DGRAD epilogue)
     const __nv_bfloat16* a_in;  // saved a (L2_DGRAD epilogue)
-    __nv_bfloat16* out0;
-    __nv_bfloat16* out1;
-    __nv_bfloat16* out2;
-    float* outf;
+    float* outf;                // dw_part (L2_DGRAD epilogue); bf16 outputs leave by TMA store
+};
+
+// Tensor maps of one grouped-GEMM launch: operands A, B (loads) and up to
+// two outputs C0, C1 (TMA stores).  Unused maps are zero.
+struct GemmMaps {
+    CUtensorMap a, b, c0, c1;
 };
 
 // Layout of the three workspaces (host only).
@@ -58,8 +63,7 @@ int compute_layout(const moe_shape* s, moe_layout* L);
 // Kernel launchers (return a cudaError_t as int).
 int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t* topk_idx, uint8_t* route,
                           cudaStream_t st);
-int launch_gemm(int flavour, const GemmArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapB, int grid,
-                cudaStream_t st);
+int launch_gemm(int flavour, const GemmArgs& a, const GemmMaps& maps, int grid, cudaStream_t st);
 int launch_combine(const __nv_bfloat16* rows, const int32_t* inv, int T, int k, int H, __nv_bfloat16* out,
                    int num_sms, cudaStream_t st);
 int launch_dw_reduce(const float* dw_part, int cols, const int32_t* inv, long long slots, float* out, int num_sms,

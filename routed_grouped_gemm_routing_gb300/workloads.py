@@ -62,6 +62,10 @@ CONFIGS = {
     "v3": LayerShape("v3", T=8192, H=7168, I=2048, E=256, k=8),
     "wide": LayerShape("wide", T=4096, H=7168, I=3072, E=384, k=6),
     "skew": LayerShape("skew", T=8192, H=7168, I=2048, E=256, k=8, skew_c=0.5),
+    # V3 expert shapes with 16 experts and 512 tokens: the same ~256 routed
+    # rows per expert as the V3 layer in ~3 GB of device memory (kernel
+    # profiling captures must stay small).
+    "v3_slice": LayerShape("v3_slice", T=512, H=7168, I=2048, E=16, k=8),
 }
 
 
