@@ -16,7 +16,7 @@
 //    backward recomputes them (README, "Recompute dispatched x").
 //  * Dense operands (weights, saved activations) arrive by TMA.
 //  * Warp roles: warps 0-3 epilogue (TMEM -> registers -> global), warp 4 TMA
-//    producer, warp 5 gather producer, warp 6 MMA issuer and TMEM owner.  A
+//    producer, warp 5 MMA issuer and TMEM owner, warps 6.. gather producers.  A
 //    4-stage shared-memory ring (full/empty mbarriers) feeds the MMA; two
 //    256-column TMEM accumulators let the epilogue of one tile overlap the
 //    main loop of the next.
@@ -167,11 +167,13 @@ __device__ void role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const Gem
 }
 
 // --------------------------------------------------------- gather producer
-// Copies 16-byte chunks of token rows into the 128-byte-swizzled tile layout:
-// chunk c of tile row r lands at r*128 + ((c ^ (r & 7)) * 16).
+// kGatherWarps warps copy 16-byte chunks of token rows into the
+// 128-byte-swizzled tile layout (chunk c of tile row r lands at
+// r*128 + ((c ^ (r & 7)) * 16)); each warp owns an equal share of the rows of
+// every stage, so several warps' copies are in flight at once.
 template <int F>
 __device__ void role_gather(const GemmArgs& p, int total, uint32_t sA, uint32_t sB, Bars bars, volatile int* abort,
-                            int lane) {
+                            int gw, int lane) {
     using Tr = GemmTraits<F>;
     const int c = lane & 7;
     const int rb = lane >> 3;
@@ -184,10 +186,13 @@ __device__ void role_gather(const GemmArgs& p, int total, uint32_t sA, uint32_t 
         const TileCoord t = decode_tile<F>(tile, p);
         if constexpr (!Tr::kAMN) {
             // K-major A: the tile's 128 routed rows are fixed; K runs along H.
-            int tok[32];
+            constexpr int kRowsPerWarp = kBM / kGatherWarps;
+            constexpr int kPerLane = kRowsPerWarp / 4;
+            const int rw0 = gw * kRowsPerWarp;
+            int tok[kPerLane];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int s = __ldg(p.perm + t.m0 + rb + 4 * jj);
+            for (int jj = 0; jj < kPerLane; ++jj) {
+                const int s = __ldg(p.perm + t.m0 + rw0 + rb + 4 * jj);
                 tok[jj] = s >= 0 ? s / k : -1;
             }
             for (int kb = 0; kb < t.nkb; ++kb) {
@@ -195,8 +200,8 @@ __device__ void role_gather(const GemmArgs& p, int total, uint32_t sA, uint32_t 
                 const uint32_t a = sA + stage * kStageABytes;
                 const int col = kb * kBK + c * 8;
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int r = rb + 4 * jj;
+                for (int jj = 0; jj < kPerLane; ++jj) {
+                    const int r = rw0 + rb + 4 * jj;
                     const int tk = tok[jj];
                     const __nv_bfloat16* g = src + (size_t)(tk < 0 ? 0 : tk) * (size_t)H + col;
                     cp_async_16(a + r * 128 + ((c ^ (r & 7)) << 4), g, tk < 0 ? 0u : 16u);
@@ -211,25 +216,28 @@ __device__ void role_gather(const GemmArgs& p, int total, uint32_t sA, uint32_t 
             // MN-major token operand of a weight gradient: the 64 K rows of a
             // stage are routed rows of expert e; columns run along H.
             constexpr int kRegions = (F == DW1) ? 2 : 4;
+            constexpr int kRowsPerWarp = kBK / kGatherWarps;  // 16
+            constexpr int kPerLane = kRowsPerWarp / 4;        // 4
             const int col0 = (F == DW1) ? t.m0 : t.n0;
+            const int rw0 = gw * kRowsPerWarp;
+            // permutation entries of this warp's rows, one k block ahead
+            int nxt = t.nkb > 0 ? __ldg(p.perm + t.krow0 + rw0 + (lane & (kRowsPerWarp - 1))) : -1;
             for (int kb = 0; kb < t.nkb; ++kb) {
+                const int cur = nxt;
+                if (kb + 1 < t.nkb) nxt = __ldg(p.perm + t.krow0 + (kb + 1) * kBK + rw0 + (lane & (kRowsPerWarp - 1)));
                 if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
                 const uint32_t dst0 = (F == DW1) ? (sA + stage * kStageABytes) : (sB + stage * kStageBBytes);
-                const int row0 = t.krow0 + kb * kBK;
-                const int s0 = __ldg(p.perm + row0 + lane);
-                const int s1 = __ldg(p.perm + row0 + 32 + lane);
-                const int t0 = s0 >= 0 ? s0 / k : -1;
-                const int t1 = s1 >= 0 ? s1 / k : -1;
-                int tq[16];
+                const int tcur = cur >= 0 ? cur / k : -1;
+                int tq[kPerLane];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) tq[q] = __shfl_sync(0xffffffffu, q < 8 ? t0 : t1, (rb + 4 * q) & 31);
+                for (int q = 0; q < kPerLane; ++q) tq[q] = __shfl_sync(0xffffffffu, tcur, rb + 4 * q);
 #pragma unroll
                 for (int g = 0; g < kRegions; ++g) {
                     const int colg = col0 + 64 * g + 8 * c;
                     const bool okc = colg < H;
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int r = rb + 4 * q;
+                    for (int q = 0; q < kPerLane; ++q) {
+                        const int r = rw0 + rb + 4 * q;
                         const bool ok = okc && tq[q] >= 0;
                         const __nv_bfloat16* gp = src + (ok ? (size_t)tq[q] * (size_t)H + colg : (size_t)0);
                         cp_async_16(dst0 + g * 8192 + r * 128 + ((c ^ (r & 7)) << 4), gp, ok ? 16u : 0u);
@@ -478,7 +486,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        constexpr uint32_t kFullCount = 1u + ((Tr::kAGather || Tr::kBGather) ? 32u : 0u);
+        constexpr uint32_t kFullCount = 1u + ((Tr::kAGather || Tr::kBGather) ? 32u * kGatherWarps : 0u);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bars.full(s), kFullCount);
             mbar_init(bars.empty(s), 1);
@@ -491,11 +499,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 6) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_addr(tmem_slot), 2 * kBN);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kWarpTma && lane == 0) {
         if constexpr (!Tr::kAGather) tma_prefetch_map(&mapA);
         if constexpr (!Tr::kBGather) tma_prefetch_map(&mapB);
         tma_prefetch_map(&mapC0);
@@ -507,12 +515,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int total = total_tiles<F>(p);
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         if (lane == 0) role_tma<F>(&mapA, &mapB, p, total, sA, sB, bars, abort);
-    } else if (warp == 5) {
-        if constexpr (Tr::kAGather || Tr::kBGather) role_gather<F>(p, total, sA, sB, bars, abort, lane);
+    } else if (warp >= kWarpGather0) {
+        if constexpr (Tr::kAGather || Tr::kBGather)
+            role_gather<F>(p, total, sA, sB, bars, abort, warp - kWarpGather0, lane);
         cp_async_wait_all();
-    } else if (warp == 6) {
+    } else if (warp == kWarpMma) {
         if (lane == 0) {
             role_mma<F>(p, total, sA, sB, bars, tmem_base, abort);
             if (*abort) {
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, total, bars, tmem_base, sStage + warp * kStageEpiBytes, abort,
                          warp, lane);
     }
-    if (warp == 4 && lane == 0 && *abort) {
+    if (warp == kWarpTma && lane == 0 && *abort) {
         // bulk copies already issued land within microseconds; give them time
         const uint64_t t0 = global_timer_ns();
         while (global_timer_ns() - t0 < 2000000ull) {
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 6) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 2 * kBN);
     }

@@ -17,7 +17,12 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kStageABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kStageBBytes = kBN * kBK * 2;  // 32 KiB
-constexpr int kGemmThreads = 224;            // 4 epilogue warps, TMA warp, gather warp, MMA warp
+constexpr int kGatherWarps = 4;             // warps issuing the cp.async row gathers
+// warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer, 6.. gather producers
+constexpr int kWarpTma = 4;
+constexpr int kWarpMma = 5;
+constexpr int kWarpGather0 = 6;
+constexpr int kGemmThreads = 32 * (kWarpGather0 + kGatherWarps);
 constexpr int kMaxDevices = 64;
 constexpr int kEpiWarps = 4;
 constexpr int kStageEpiBytes = 8192;  // per epilogue warp: TMA-store staging
