@@ -67,8 +67,42 @@ struct TileCoord {
     int krow0;  // first routed row of the expert (weight gradients)
 };
 
+// A tile's coordinates come from the routing tables in global memory.  Each
+// role reads the next tile's entries right after starting the current tile
+// (load_tile_raw), so that latency is hidden behind the current tile's work
+// instead of stalling every role at every tile boundary.
+//
+// Row-grouped GEMMs number their tiles expert by expert, then N tile, then
+// M tile: the 2-3 M tiles of one expert that read the same weight tile get
+// consecutive numbers, run on neighbouring CTAs at the same time, and share
+// that weight tile through L2 (a block of consecutive tiles that straddles
+// two waves of the persistent grid splits at most one such group).  Tile t
+// belongs to expert e = tiles[t / n_tiles], because expert e owns M tiles
+// [offs[e]/128, offs[e+1]/128) and so tile numbers
+// [offs[e]/128 * n_tiles, offs[e+1]/128 * n_tiles).
+struct TileRaw {
+    int a;  // row-grouped: owner expert; weight gradients: counts[e]
+    int b;  // offs[e]
+    int c;  // row-grouped: offs[e + 1]
+};
+
 template <int F>
-__device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
+__device__ __forceinline__ TileRaw load_tile_raw(int tile, const GemmArgs& p) {
+    TileRaw r{0, 0, 0};
+    if constexpr (GemmTraits<F>::kWgrad) {
+        const int e = tile / (p.m_tiles * p.n_tiles);
+        r.a = __ldg(p.counts + e);
+        r.b = __ldg(p.offs + e);
+    } else {
+        r.a = __ldg(p.tiles + tile / p.n_tiles);
+        r.b = __ldg(p.offs + r.a);
+        r.c = __ldg(p.offs + r.a + 1);
+    }
+    return r;
+}
+
+template <int F>
+__device__ __forceinline__ TileCoord finish_tile(int tile, TileRaw r, const GemmArgs& p) {
     TileCoord t;
     if constexpr (GemmTraits<F>::kWgrad) {
         const int per_e = p.m_tiles * p.n_tiles;
@@ -78,13 +112,15 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
         t.nt = rem - mt * p.n_tiles;
         t.m0 = mt * kBM;
         t.n0 = t.nt * kBN;
-        const int cnt = __ldg(p.counts + t.e);
-        t.nkb = (cnt + kBK - 1) / kBK;
-        t.krow0 = __ldg(p.offs + t.e);
+        t.nkb = (r.a + kBK - 1) / kBK;
+        t.krow0 = r.b;
     } else {
-        const int mt = tile / p.n_tiles;
-        t.nt = tile - mt * p.n_tiles;
-        t.e = __ldg(p.tiles + mt);
+        const int ts = r.b / kBM;        // first M tile of expert e
+        const int tc = (r.c - r.b) / kBM;  // M tiles of expert e (>= 1 here)
+        const int l = tile - ts * p.n_tiles;
+        t.nt = l / tc;
+        const int mt = ts + (l - t.nt * tc);
+        t.e = r.a;
         t.m0 = mt * kBM;
         t.n0 = t.nt * (F == L1_FWD ? kBN / 2 : kBN);
         t.nkb = p.K / kBK;
@@ -92,6 +128,28 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
     }
     return t;
 }
+
+// Iterates this CTA's tiles blockIdx.x, blockIdx.x + gridDim.x, ... with the
+// table reads of the next tile in flight.
+template <int F>
+struct TileWalk {
+    const GemmArgs& p;
+    int total;
+    int tile;
+    TileRaw raw;
+    __device__ __forceinline__ TileWalk(const GemmArgs& p_, int total_) : p(p_), total(total_), tile(blockIdx.x) {
+        raw = tile < total ? load_tile_raw<F>(tile, p) : TileRaw{0, 0, 0};
+    }
+    __device__ __forceinline__ bool valid() const { return tile < total; }
+    // Coordinates of the current tile; issues the reads of the next one.
+    __device__ __forceinline__ TileCoord take() {
+        const TileCoord t = finish_tile<F>(tile, raw, p);
+        const int nxt = tile + (int)gridDim.x;
+        if (nxt < total) raw = load_tile_raw<F>(nxt, p);
+        return t;
+    }
+    __device__ __forceinline__ void next() { tile += (int)gridDim.x; }
+};
 
 template <int F>
 __device__ __forceinline__ int total_tiles(const GemmArgs& p) {
@@ -129,8 +187,8 @@ __device__ void role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const Gem
     constexpr uint32_t kTx = (Tr::kAGather ? 0u : (uint32_t)kStageABytes) + (Tr::kBGather ? 0u : (uint32_t)kStageBBytes);
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const TileCoord t = decode_tile<F>(tile, p);
+    for (TileWalk<F> w(p, total); w.valid(); w.next()) {
+        const TileCoord t = w.take();
         for (int kb = 0; kb < t.nkb; ++kb) {
             if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
             const uint32_t fb = bars.full(stage);
@@ -182,8 +240,8 @@ __device__ void role_gather(const GemmArgs& p, int total, uint32_t sA, uint32_t 
     const __nv_bfloat16* src = p.gsrc;
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const TileCoord t = decode_tile<F>(tile, p);
+    for (TileWalk<F> w(p, total); w.valid(); w.next()) {
+        const TileCoord t = w.take();
         if constexpr (!Tr::kAMN) {
             // K-major A: the tile's 128 routed rows are fixed; K runs along H.
             constexpr int kRowsPerWarp = kBM / kGatherWarps;
@@ -262,8 +320,8 @@ __device__ void role_mma(const GemmArgs& p, int total, uint32_t sA, uint32_t sB,
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-        const TileCoord t = decode_tile<F>(tile, p);
+    for (TileWalk<F> w(p, total); w.valid(); w.next(), ++it) {
+        const TileCoord t = w.take();
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
@@ -316,8 +374,8 @@ __device__ void role_epilogue(const GemmArgs& p, OutMaps om, int total, Bars bar
                               uint32_t stage, volatile int* abort, int warp, int lane) {
     int it = 0;
     uint32_t nstore = 0;  // 64-column boxes stored by this warp (picks the staging half)
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-        const TileCoord t = decode_tile<F>(tile, p);
+    for (TileWalk<F> w(p, total); w.valid(); w.next(), ++it) {
+        const TileCoord t = w.take();
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!warp_wait(bars.tfull(acc), acc_phase, abort)) break;
@@ -334,8 +392,17 @@ __device__ void role_epilogue(const GemmArgs& p, OutMaps om, int total, Bars bar
                 const int col = t.n0 + 32 * cc;
                 if (col >= I) break;
                 float g[32], u[32];
-                tmem_ld32(tacc + 32 * cc, g);
-                tmem_ld32(tacc + 128 + 32 * cc, u);
+                {
+                    uint32_t rg[32], ru[32];
+                    tmem_ld32_nowait(tacc + 32 * cc, rg);
+                    tmem_ld32_nowait(tacc + 128 + 32 * cc, ru);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        g[j] = __uint_as_float(rg[j]);
+                        u[j] = __uint_as_float(ru[j]);
+                    }
+                }
                 uint32_t pg[16], pu[16], pa[16];
                 pack32(g, pg);
                 pack32(u, pu);
@@ -428,17 +495,19 @@ __device__ void role_epilogue(const GemmArgs& p, OutMaps om, int total, Bars bar
                 if (col >= N_out) break;
                 uint32_t pk[32];
                 {
-                    float v[32];
+                    uint32_t r0[32], r1[32];
+                    if (have_acc) {
+                        tmem_ld32_nowait(tacc + 64 * c64, r0);
+                        tmem_ld32_nowait(tacc + 64 * c64 + 32, r1);
+                        tmem_ld_wait();
+                    } else {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (have_acc) {
-                            tmem_ld32(tacc + 64 * c64 + 32 * h, v);
-                        } else {
+                        for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                    }
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) pk[16 * h + j] = pack_bf16x2(wv * v[2 * j], wv * v[2 * j + 1]);
+                    for (int j = 0; j < 16; ++j) {
+                        pk[j] = pack_bf16x2(wv * __uint_as_float(r0[2 * j]), wv * __uint_as_float(r0[2 * j + 1]));
+                        pk[16 + j] = pack_bf16x2(wv * __uint_as_float(r1[2 * j]), wv * __uint_as_float(r1[2 * j + 1]));
                     }
                 }
                 const uint32_t buf = stage + (nstore & 1u) * 4096u;

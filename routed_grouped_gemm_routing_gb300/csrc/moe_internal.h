@@ -17,7 +17,7 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kStageABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kStageBBytes = kBN * kBK * 2;  // 32 KiB
-constexpr int kGatherWarps = 4;             // warps issuing the cp.async row gathers
+constexpr int kGatherWarps = 8;             // warps issuing the cp.async row gathers
 // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer, 6.. gather producers
 constexpr int kWarpTma = 4;
 constexpr int kWarpMma = 5;
