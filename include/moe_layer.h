@@ -63,6 +63,7 @@ enum {
     MOE_STATUS_NUM_TILES = 1, /* MOE_STATUS_MPAD / block_m */
     MOE_STATUS_N_INVALID = 2, /* slots whose id was neither -1 nor in [0, E) */
     MOE_STATUS_FLAGS = 3,     /* bit 0: a kernel gave up on a bounded wait */
+    MOE_STATUS_NUM_PAIRS = 4, /* pair_offs[E]: tile pairs the GEMM clusters walk */
     MOE_STATUS_WORDS = 16
 };
 
@@ -77,6 +78,10 @@ enum {
  *    tiles   int32[tiles_cap]  expert owning rows [m*block_m, (m+1)*block_m);
  *                              -1 for m >= Mpad/block_m
  *    status  int32[16]         MOE_STATUS_* words
+ *    pair_offs  int32[E+1]     exclusive prefix sum of ceil(tiles_e / 2), where
+ *                              tiles_e = (offs[e+1]-offs[e]) / block_m: the GEMMs
+ *                              take an expert's M tiles two at a time
+ *    pair_owner int32[tiles_cap] expert of tile pair q; -1 past pair_offs[E]
  *  saved (written by moe_forward, read by moe_backward):
  *    h  bf16[rows_cap, 2I]     L1 output per padded row (gate | up); 0 on padding
  *    a  bf16[rows_cap, I]      SwiGLU output per padded row; 0 on padding
@@ -90,7 +95,7 @@ enum {
  * Mpad for any routing, so no buffer depends on device data. */
 typedef struct moe_layout {
     int64_t rows_cap, tiles_cap;
-    size_t route_bytes, counts, offs, perm, inv, tiles, status;
+    size_t route_bytes, counts, offs, perm, inv, tiles, status, pair_offs, pair_owner;
     size_t saved_bytes, h, a, o;
     size_t bwd_bytes, dh, aw, dxp, dw_part;
     int32_t dw_part_cols;

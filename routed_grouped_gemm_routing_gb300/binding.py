@@ -22,7 +22,7 @@ _LIB = None
 
 HEADER = os.path.join(_build.INCLUDE, "moe_layer.h")
 MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA = 0, -1, -2, -3
-STATUS_MPAD, STATUS_NUM_TILES, STATUS_N_INVALID, STATUS_FLAGS, STATUS_WORDS = 0, 1, 2, 3, 16
+STATUS_MPAD, STATUS_NUM_TILES, STATUS_N_INVALID, STATUS_FLAGS, STATUS_NUM_PAIRS, STATUS_WORDS = 0, 1, 2, 3, 4, 16
 BLOCK_M = 128
 
 
@@ -33,7 +33,7 @@ class MoeShape(ctypes.Structure):
 class MoeLayout(ctypes.Structure):
     _fields_ = [("rows_cap", ctypes.c_int64), ("tiles_cap", ctypes.c_int64)] + [
         (n, ctypes.c_size_t)
-        for n in ("route_bytes", "counts", "offs", "perm", "inv", "tiles", "status",
+        for n in ("route_bytes", "counts", "offs", "perm", "inv", "tiles", "status", "pair_offs", "pair_owner",
                   "saved_bytes", "h", "a", "o", "bwd_bytes", "dh", "aw", "dxp", "dw_part")
     ] + [("dw_part_cols", ctypes.c_int32)]
 
@@ -174,7 +174,8 @@ def route_tables(shape: MoeShape, route_ws) -> dict:
 
     return dict(counts=view(L.counts, shape.E), offs=view(L.offs, shape.E + 1), perm=view(L.perm, L.rows_cap),
                 inv=view(L.inv, shape.T * shape.k), tiles=view(L.tiles, L.tiles_cap),
-                status=view(L.status, STATUS_WORDS))
+                status=view(L.status, STATUS_WORDS), pair_offs=view(L.pair_offs, shape.E + 1),
+                pair_owner=view(L.pair_owner, L.tiles_cap))
 
 
 def saved_tensors(shape: MoeShape, saved) -> dict:

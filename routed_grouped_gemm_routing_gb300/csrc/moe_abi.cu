@@ -213,11 +213,6 @@ int query_device(Ctx* c, const void* data) {
     return MOE_OK;
 }
 
-int grid_for(int sms, long long tiles) {
-    if (tiles <= 0) return 0;
-    return (int)(tiles < sms ? tiles : sms);
-}
-
 GemmArgs base_args(const moe_shape* s, const moe_layout& L, uint8_t* route) {
     GemmArgs a;
     memset(&a, 0, sizeof a);
@@ -232,8 +227,15 @@ GemmArgs base_args(const moe_shape* s, const moe_layout& L, uint8_t* route) {
     a.offs = reinterpret_cast<const int32_t*>(route + L.offs);
     a.counts = reinterpret_cast<const int32_t*>(route + L.counts);
     a.tiles = reinterpret_cast<const int32_t*>(route + L.tiles);
+    a.pair_offs = reinterpret_cast<const int32_t*>(route + L.pair_offs);
+    a.pair_owner = reinterpret_cast<const int32_t*>(route + L.pair_owner);
     a.status = reinterpret_cast<int32_t*>(route + L.status);
     return a;
+}
+
+int grid_for(int sms, long long tiles) {
+    if (tiles <= 0) return 0;
+    return (int)(tiles < sms ? tiles : sms);
 }
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -256,6 +258,8 @@ int compute_layout(const moe_shape* s, moe_layout* L) {
     L->inv = o; o = align_up(o + 4 * (size_t)tk, A);
     L->tiles = o; o = align_up(o + 4 * (size_t)L->tiles_cap, A);
     L->status = o; o = align_up(o + 4 * (size_t)MOE_STATUS_WORDS, A);
+    L->pair_offs = o; o = align_up(o + 4 * (size_t)(s->E + 1), A);
+    L->pair_owner = o; o = align_up(o + 4 * (size_t)L->tiles_cap, A);
     L->route_bytes = o;
     o = 0;
     L->h = o; o = align_up(o + 2 * R * 2 * (size_t)s->I, A);

@@ -141,3 +141,13 @@ def check_tables(run: GpuRun, ref: dict):
     assert st[B.STATUS_NUM_TILES] == ref["num_tiles"]
     assert st[B.STATUS_N_INVALID] == ref["n_invalid"]
     assert st[B.STATUS_FLAGS] == 0, "a kernel reported a bounded-wait timeout"
+    # scheduling tables of the GEMM clusters, derived from the (bit-exact) offsets
+    tiles_e = np.diff(ref["offs"]) // 128
+    pairs_e = (tiles_e + 1) // 2
+    pair_offs = np.concatenate([[0], np.cumsum(pairs_e)]).astype(np.int32)
+    assert np.array_equal(got["pair_offs"], pair_offs)
+    owner = np.full(len(got["pair_owner"]), -1, np.int32)
+    for e in range(len(pairs_e)):
+        owner[pair_offs[e]: pair_offs[e + 1]] = e
+    assert np.array_equal(got["pair_owner"], owner)
+    assert st[B.STATUS_NUM_PAIRS] == pair_offs[-1]

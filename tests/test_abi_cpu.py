@@ -32,11 +32,12 @@ def test_layout(lib, T, H, I, E, k):
     assert L.rows_cap == oracle.rows_cap(T, E, k, 128)
     assert L.tiles_cap == L.rows_cap // 128
     assert L.dw_part_cols == (I + 255) // 256
-    offs = [L.counts, L.offs, L.perm, L.inv, L.tiles, L.status]
+    offs = [L.counts, L.offs, L.perm, L.inv, L.tiles, L.status, L.pair_offs, L.pair_owner]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert L.offs >= L.counts + 4 * E and L.perm >= L.offs + 4 * (E + 1)
     assert L.inv >= L.perm + 4 * L.rows_cap and L.tiles >= L.inv + 4 * T * k
-    assert L.status >= L.tiles + 4 * L.tiles_cap and L.route_bytes >= L.status + 64
+    assert L.status >= L.tiles + 4 * L.tiles_cap and L.pair_offs >= L.status + 64
+    assert L.pair_owner >= L.pair_offs + 4 * (E + 1) and L.route_bytes >= L.pair_owner + 4 * L.tiles_cap
     R = L.rows_cap
     assert L.a >= L.h + 2 * R * 2 * I and L.o >= L.a + 2 * R * I and L.saved_bytes >= L.o + 2 * R * H
     assert L.aw >= L.dh + 2 * R * 2 * I and L.dxp >= L.aw + 2 * R * I
