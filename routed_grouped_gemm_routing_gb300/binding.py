@@ -189,6 +189,17 @@ def saved_tensors(shape: MoeShape, saved) -> dict:
     return dict(h=view(L.h, R, 2 * I), a=view(L.a, R, I), o=view(L.o, R, H))
 
 
+def backward_tensors(shape: MoeShape, bwd) -> dict:
+    """Device views of dh, aw, dxp inside the backward workspace (no copy)."""
+    L = moe_workspace_layout(shape)
+    R, H, I = L.rows_cap, shape.H, shape.I
+
+    def view(off, rows, cols):
+        return bwd[off: off + 2 * rows * cols].view(torch.bfloat16).view(rows, cols)
+
+    return dict(dh=view(L.dh, R, 2 * I), aw=view(L.aw, R, I), dxp=view(L.dxp, R, H))
+
+
 class KernelTrace:
     """Brackets every kernel the library launches from this thread with a
     pair of CUDA events (moe_trace_begin / moe_trace_end), for per-kernel

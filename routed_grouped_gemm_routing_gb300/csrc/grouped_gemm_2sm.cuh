@@ -1,0 +1,771 @@
+// Row-grouped GEMMs of the routed MoE layer on SM pairs (tcgen05 cta_group::2),
+// computed transposed: out^T[features x rows] = W^T . X^T.
+//
+// The pages' kernels tile these GEMMs over the routed rows of each expert
+// (Primus-Turbo "Mega MoE" README, "Pipeline").  Here the MMA's M is 256
+// output features of one expert (128 in each CTA of a 2-CTA cluster, taken
+// from that expert's weights) and its N is a chunk of up to 256 of the
+// expert's routed rows, split 128 + 128 between the two CTAs.  Because N
+// runs in steps of 16, an expert's rows are padded to 32 instead of to a
+// whole 128-row tile, and because each CTA loads only its half of the
+// activations and its own 128 weight columns, an SM needs 32 KiB of
+// operands per 64-deep K block instead of the 48 KiB of a one-SM
+// 128 x 256 tile, so the same tensor-core work needs two thirds of the
+// L2-to-SM bandwidth.
+//
+// Work units: (expert e, feature tile ft, row chunk j).  Expert e's rows are
+// cut into nsub = ceil(count / 256) chunks of equal size (rounded up to 32);
+// the routing prologue's pair tables hold nsub per expert (pair_offs) and the
+// owner of every chunk (pair_owner).  Units are numbered expert by expert,
+// then feature tile, then chunk, so the chunks that stream the same weight
+// tile run at the same time on neighbouring clusters.
+//
+// Roles (per CTA, 14 warps): 0-3 epilogue (TMEM lanes = this CTA's 128
+// features, columns = rows), 4 TMA producer (weights; non-gathered
+// activations), 5 MMA issuer on the even CTA / relay on the odd CTA, 6-13
+// gather producers (x or dY rows picked by the permutation table).
+//   * Producers of both CTAs fill their own stage and arrive on their own
+//     full[s]; the odd CTA's relay thread forwards that to the even CTA's
+//     peer_full[s].
+//   * The even CTA waits for full[s] and peer_full[s], issues the four M=256
+//     MMAs of the stage, and its commit arrives on empty[s] of both CTAs;
+//     after a unit's last K block a commit arrives on tfull[acc] of both.
+//   * Both CTAs' epilogue warps drain their own accumulator rows and arrive
+//     on the even CTA's tempty[acc] (8 arrivals) before it is reused.
+// Every wait is bounded; a timeout raises the CTA's abort flag and the
+// status word, and both CTAs leave through the closing cluster barrier.
+#pragma once
+
+#include "grouped_gemm.cuh"
+
+namespace moe {
+
+constexpr int kT2Stages = 6;              // barrier slots (the L2 dgrad kernel uses 5 stages)
+constexpr int kT2ABytes = 128 * kBK * 2;  // this CTA's 128 features x 64 of K
+constexpr int kT2BBytes = 128 * kBK * 2;  // up to 128 routed rows x 64 of K
+constexpr int kT2InBytes = 3 * 2048;      // L2 dgrad epilogue inputs per warp: h gate, h up, a boxes
+constexpr int kT2NumBars = 3 * kT2Stages + 9 + kEpiWarps;
+static_assert(8 * kT2NumBars + 8 <= 256, "barrier area");
+
+struct T2Bars {
+    uint32_t base;
+    __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * s; }
+    __device__ __forceinline__ uint32_t peer_full(int s) const { return base + 8u * (kT2Stages + s); }
+    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (2 * kT2Stages + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kT2Stages + a); }
+    __device__ __forceinline__ uint32_t tempty(int a) const { return base + 8u * (3 * kT2Stages + 2 + a); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kT2Stages + 4); }
+    // L1 epilogue: up-projection values handed from warp 2 + i to warp i
+    __device__ __forceinline__ uint32_t xfull(int i) const { return base + 8u * (3 * kT2Stages + 5 + i); }
+    __device__ __forceinline__ uint32_t xempty(int i) const { return base + 8u * (3 * kT2Stages + 7 + i); }
+    // L2 dgrad epilogue: the saved h and a boxes of epilogue warp w have landed
+    __device__ __forceinline__ uint32_t ein(int w) const { return base + 8u * (3 * kT2Stages + 9 + w); }
+};
+
+// ------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t cluster_addr_of(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on a barrier that receives arrivals from the other CTA.
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives on the mbarrier at offset `bar` of both CTAs of the pair once
+// every MMA issued so far by this thread is complete.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)0x3)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Column l of a 32-row x 32-column bf16 box in the 64-byte swizzle (row j
+// at byte 64 j, its 16-byte chunk q stored at chunk q ^ ((j / 2) % 4)):
+// v[j] is the value of row j.
+__device__ __forceinline__ void stage_col_sw64(uint32_t box, int l, const float (&v)[32]) {
+    const uint32_t within = (uint32_t)(l & 7) << 1;
+    const int q = l >> 3;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(v[j]);
+        const uint16_t u = *reinterpret_cast<const uint16_t*>(&b);
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(box + j * 64 + ((uint32_t)(q ^ ((j >> 1) & 3)) << 4) + within),
+                     "h"(u)
+                     : "memory");
+    }
+}
+
+// Rows j0..j0+15 of column l of the same box.
+__device__ __forceinline__ void stage_col16_sw64(uint32_t box, int l, int j0, const float (&v)[16]) {
+    const uint32_t within = (uint32_t)(l & 7) << 1;
+    const int q = l >> 3;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+        const int j = j0 + jj;
+        const __nv_bfloat16 b = __float2bfloat16_rn(v[jj]);
+        const uint16_t u = *reinterpret_cast<const uint16_t*>(&b);
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(box + j * 64 + ((uint32_t)(q ^ ((j >> 1) & 3)) << 4) + within),
+                     "h"(u)
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ float ldg_bf16(const __nv_bfloat16* p) {
+    const uint16_t u = __ldg(reinterpret_cast<const unsigned short*>(p));
+    return __uint_as_float((uint32_t)u << 16);
+}
+
+// ------------------------------------------------------------ work units
+template <int F>
+struct T2;
+template <>
+struct T2<L1_FWD> {
+    static constexpr bool kGather = true, kAMN = true;
+    static constexpr int kFeatPerCta = 64;  // 64 gate + 64 up features
+    static constexpr int kStages = 6;
+    static constexpr int kInBytes = 0;
+};
+template <>
+struct T2<L2_FWD> {
+    static constexpr bool kGather = false, kAMN = true;
+    static constexpr int kFeatPerCta = 128;
+    static constexpr int kStages = 6;
+    static constexpr int kInBytes = 0;
+};
+template <>
+struct T2<L2_DGRAD> {
+    static constexpr bool kGather = true, kAMN = false;
+    static constexpr int kFeatPerCta = 128;
+    static constexpr int kStages = 5;
+    static constexpr int kInBytes = kEpiWarps * kT2InBytes;
+};
+template <>
+struct T2<L1_DGRAD> {
+    static constexpr bool kGather = false, kAMN = false;
+    static constexpr int kFeatPerCta = 128;
+    static constexpr int kStages = 6;
+    static constexpr int kInBytes = 0;
+};
+
+template <int F>
+constexpr int t2_smem_bytes() {
+    return 1024 + T2<F>::kStages * (kT2ABytes + kT2BBytes) + kEpiWarps * kStageEpiBytes + T2<F>::kInBytes + 256;
+}
+static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448, "shared memory per CTA");
+
+// Element (row j, column l) of a 32-row x 32-column bf16 box in the 64-byte swizzle.
+__device__ __forceinline__ float lds_sw64(uint32_t box, int j, int l) {
+    uint16_t u;
+    asm volatile("ld.shared.u16 %0, [%1];"
+                 : "=h"(u)
+                 : "r"(box + j * 64 + ((uint32_t)((l >> 3) ^ ((j >> 1) & 3)) << 4) + ((uint32_t)(l & 7) << 1))
+                 : "memory");
+    return __uint_as_float((uint32_t)u << 16);
+}
+// Stores v as element (row j, column l) of the same kind of box.
+__device__ __forceinline__ void sts_sw64(uint32_t box, int j, int l, float v) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    const uint16_t u = *reinterpret_cast<const uint16_t*>(&b);
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(box + j * 64 + ((uint32_t)((l >> 3) ^ ((j >> 1) & 3)) << 4) +
+                                               ((uint32_t)(l & 7) << 1)),
+                 "h"(u)
+                 : "memory");
+}
+
+// One step of a warp-wide transposed reduction of 32 values per lane: after
+// the steps for S = 16, 8, 4, 2, 1, lane j holds the sum over all lanes of
+// their value j.  At step S a lane keeps the half of its S * 2 live values
+// selected by bit S of its lane id and adds the partner's copy of that half.
+template <int S>
+__device__ __forceinline__ void transpose_reduce_step(float (&v)[32], int lane) {
+    const bool upper = (lane & S) != 0;
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+        const float send = upper ? v[i] : v[i + S];
+        const float keep = upper ? v[i + S] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, S);
+    }
+}
+
+struct T2Unit {
+    int e;       // expert
+    int f0;      // first feature of this CTA (L1: of its 64 gate and 64 up features)
+    int fcol;    // this CTA's feature tile (of kFeatPerCta features)
+    int r0;      // first routed row of the unit (index into perm and the row-ordered buffers)
+    int n;       // rows of the unit rounded up to 32: the MMA's N
+    int nvalid;  // routed rows of the unit
+};
+struct T2Raw {
+    int e, po, pn, off, cnt;
+};
+
+template <int F>
+struct T2Walk {
+    const GemmArgs& p;
+    int total, unit, step, rank;
+    T2Raw raw;
+    __device__ __forceinline__ T2Walk(const GemmArgs& p_, int total_, int rank_)
+        : p(p_), total(total_), unit((int)blockIdx.x >> 1), step((int)gridDim.x >> 1), rank(rank_) {
+        if (unit < total) load(unit);
+    }
+    __device__ __forceinline__ void load(int u) {
+        raw.e = __ldg(p.pair_owner + u / p.n_tiles);
+        raw.po = __ldg(p.pair_offs + raw.e);
+        raw.pn = __ldg(p.pair_offs + raw.e + 1);
+        raw.off = __ldg(p.offs + raw.e);
+        raw.cnt = __ldg(p.counts + raw.e);
+    }
+    __device__ __forceinline__ bool valid() const { return unit < total; }
+    __device__ __forceinline__ T2Unit take() {
+        T2Unit t;
+        const int nsub = raw.pn - raw.po;
+        const int l = unit - raw.po * p.n_tiles;
+        const int ft = l / nsub;
+        const int j = l - ft * nsub;
+        const int nb = (((raw.cnt + nsub - 1) / nsub) + 31) & ~31;
+        const int rs = j * nb;
+        t.e = raw.e;
+        t.nvalid = min(nb, raw.cnt - rs);
+        t.n = (t.nvalid + 31) & ~31;
+        t.r0 = raw.off + rs;
+        t.fcol = 2 * ft + rank;
+        t.f0 = t.fcol * T2<F>::kFeatPerCta;
+        const int nxt = unit + step;
+        if (nxt < total) load(nxt);
+        return t;
+    }
+    __device__ __forceinline__ void next() { unit += step; }
+};
+
+__device__ __forceinline__ int t2_total_units(const GemmArgs& p) {
+    int np = *reinterpret_cast<const volatile int32_t*>(p.status + MOE_STATUS_NUM_PAIRS);
+    np = np < 0 ? 0 : (np > p.tiles_cap ? p.tiles_cap : np);
+    return np * p.n_tiles;
+}
+
+// ------------------------------------------------------------ TMA producer
+template <int F>
+__device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, int total, uint32_t sA,
+                            uint32_t sB, T2Bars bars, volatile int* abort, int rank) {
+    const int nkb = p.K / kBK;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (T2Walk<F> w(p, total, rank); w.valid(); w.next()) {
+        const T2Unit t = w.take();
+        const int nh = t.n >> 1;           // this CTA's rows of the unit
+        const int nbox = (nh + 31) >> 5;   // 32-row boxes of a non-gathered B
+        const int rb = t.r0 + nh * rank;
+        const uint32_t tx = (uint32_t)kT2ABytes + (T2<F>::kGather ? 0u : (uint32_t)nbox * 4096u);
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+            const uint32_t fb = bars.full(stage);
+            mbar_arrive_expect_tx(fb, tx);
+            const uint32_t a = sA + stage * kT2ABytes;
+            const uint32_t b = sB + stage * kT2BBytes;
+            const int k0 = kb * kBK;
+            if constexpr (F == L1_FWD) {
+                // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
+                tma_load_4d(a, mA, t.f0, 0, k0, t.e, fb);
+                tma_load_4d(a + 8192, mA, t.f0, 1, k0, t.e, fb);
+            } else if constexpr (F == L2_FWD) {
+                tma_load_3d(a, mA, t.f0, k0, t.e, fb);
+                tma_load_3d(a + 8192, mA, t.f0 + 64, k0, t.e, fb);
+                for (int i = 0; i < nbox; ++i) tma_load_2d(b + i * 4096, mB, k0, rb + 32 * i, fb);
+            } else if constexpr (F == L2_DGRAD) {
+                tma_load_3d(a, mA, k0, t.f0, t.e, fb);
+            } else {  // L1_DGRAD
+                tma_load_3d(a, mA, k0, t.f0, t.e, fb);
+                for (int i = 0; i < nbox; ++i) tma_load_2d(b + i * 4096, mB, k0, rb + 32 * i, fb);
+            }
+            if (++stage == T2<F>::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------- gather producers
+// This CTA's rows of the unit, 16 per warp, 16-byte cp.async chunks into the
+// 128-byte-swizzled K-major layout; rows past the unit's half are left alone
+// (the MMA reads only n / 2 rows).  Padding rows (perm = -1) are zero-filled.
+template <int F>
+__device__ void t2_role_gather(const GemmArgs& p, int total, uint32_t sB, T2Bars bars, volatile int* abort, int gw,
+                               int lane, int rank) {
+    const int c = lane & 7;
+    const int rb = lane >> 3;
+    const int H = p.H;
+    const int k = p.k;
+    const int nkb = p.K / kBK;
+    const __nv_bfloat16* src = p.gsrc;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (T2Walk<F> w(p, total, rank); w.valid(); w.next()) {
+        const T2Unit t = w.take();
+        const int nh = t.n >> 1;
+        const int rbase = t.r0 + nh * rank;
+        int tok[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int r = gw * 16 + rb + 4 * q;
+            int s = -1;
+            if (r < nh) s = __ldg(p.perm + rbase + r);
+            tok[q] = r < nh ? (s >= 0 ? s / k : -1) : -2;  // -2: row not in this unit
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+            const uint32_t b = sB + stage * kT2BBytes;
+            const int col = kb * kBK + c * 8;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int tk = tok[q];
+                if (tk == -2) continue;
+                const int r = gw * 16 + rb + 4 * q;
+                const __nv_bfloat16* g = src + (size_t)(tk < 0 ? 0 : tk) * (size_t)H + col;
+                cp_async_16(b + r * 128 + ((c ^ (r & 7)) << 4), g, tk < 0 ? 0u : 16u);
+            }
+            cp_async_arrive_noinc(bars.full(stage));
+            if (++stage == T2<F>::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// -------------------------------------------- MMA issuer (even CTA) / relay
+template <int F>
+__device__ void t2_role_mma(const GemmArgs& p, int total, uint32_t sA, uint32_t sB, T2Bars bars, uint32_t tmem_base,
+                            volatile int* abort) {
+    const int nkb = p.K / kBK;
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (T2Walk<F> w(p, total, 0); w.valid(); w.next(), ++it) {
+        const T2Unit t = w.take();
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_cl(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
+        const uint32_t idesc = make_idesc_bf16(2 * kBM, t.n, T2<F>::kAMN, false);
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait(bars.full(stage), phase, abort)) return;
+            if (!mbar_wait_cl(bars.peer_full(stage), phase, abort)) return;
+            tc_fence_after();
+            if constexpr (T2<F>::kGather) fence_proxy_async_smem();
+            const uint32_t a = sA + stage * kT2ABytes;
+            const uint32_t b = sB + stage * kT2BBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                const uint64_t ad = T2<F>::kAMN ? make_sdesc_sw128(a + kk * 2048, 8192, 1024)
+                                                : make_sdesc_sw128(a + kk * 32, 16, 1024);
+                const uint64_t bd = make_sdesc_sw128(b + kk * 32, 16, 1024);
+                tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair(bars.empty(stage));
+            if (++stage == T2<F>::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        tc_commit_pair(bars.tfull(acc));
+    }
+}
+
+// The odd CTA's MMA thread: tells the even CTA that this CTA's half of a
+// stage is in shared memory.
+template <int F>
+__device__ void t2_role_relay(const GemmArgs& p, int total, T2Bars bars, volatile int* abort) {
+    const int nkb = p.K / kBK;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (T2Walk<F> w(p, total, 1); w.valid(); w.next()) {
+        (void)w.take();
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait(bars.full(stage), phase, abort)) return;
+            if constexpr (T2<F>::kGather) fence_proxy_async_smem();
+            mbar_arrive_cluster(cluster_addr_of(bars.peer_full(stage), 0));
+            if (++stage == T2<F>::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- epilogue
+// Warp w holds TMEM lanes 32w..32w+31 = 32 features of this CTA and every
+// column (routed row) of the unit.  Each 32-row chunk is written as a
+// 32-row x 32-feature box in the 64-byte swizzle and leaves by TMA store.
+// The L2 dgrad epilogue also reads the saved h and a at its rows and
+// features: a TMA load brings each 32 x 32 box into shared memory (mapH,
+// mapA), the first one while the accumulator is still being computed.
+template <int F>
+__device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMap* mapH, const CUtensorMap* mapAs,
+                                 int total, T2Bars bars, uint32_t tmem_base, uint32_t stage, uint32_t stage_of_warp0,
+                                 uint32_t in_box, volatile int* abort, int warp, int lane, int rank) {
+    const uint32_t tempty_leader[2] = {cluster_addr_of(bars.tempty(0), 0), cluster_addr_of(bars.tempty(1), 0)};
+    int it = 0;
+    uint32_t nstore = 0;
+    uint32_t xchunk = 0;  // L1: chunks handed over between warp i and warp 2 + i
+    uint32_t nin = 0;     // L2 dgrad: input boxes waited for
+    for (T2Walk<F> w(p, total, rank); w.valid(); w.next(), ++it) {
+        const T2Unit t = w.take();
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if constexpr (F == L2_DGRAD) {
+            if (lane == 0 && t.f0 + 32 * warp < p.I) {
+                const uint32_t eb = bars.ein(warp);
+                mbar_arrive_expect_tx(eb, (uint32_t)kT2InBytes);
+                tma_load_2d(in_box, mapH, t.f0 + 32 * warp, t.r0, eb);
+                tma_load_2d(in_box + 2048, mapH, p.I + t.f0 + 32 * warp, t.r0, eb);
+                tma_load_2d(in_box + 4096, mapAs, t.f0 + 32 * warp, t.r0, eb);
+            }
+        }
+        if (!warp_wait(bars.tfull(acc), acc_phase, abort)) break;
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(warp * 32) << 16);
+        bool ok = true;
+#pragma unroll 1
+        for (int c32 = 0; c32 < (t.n >> 5) && ok; ++c32) {
+            const int row0 = t.r0 + 32 * c32;
+            float v[32];
+            tmem_ld32(tacc + 32 * c32, v);
+            if constexpr (F == L1_FWD) {
+                // lanes 0-63: gate features f0..f0+63, lanes 64-127: up features f0..f0+63
+                const int I = p.I;
+                const int pr = warp & 1;
+                const int col = t.f0 + 32 * pr;
+                const uint32_t xch = stage_of_warp0 + (uint32_t)(2 + pr) * kStageEpiBytes + 4096u;
+                if (warp >= 2) {
+                    // up: hand the FP32 values to warp pr, store the h up half
+                    if (!warp_wait(bars.xempty(pr), (xchunk & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(xch + (uint32_t)(j * 32 + lane) * 4u), "f"(v[j])
+                                     : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.xfull(pr));
+                    const uint32_t buf = stage + (nstore & 1u) * 2048u;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    stage_col_sw64(buf, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && col < I) {
+                        tma_store_2d(om.c0, I + col, row0, buf);
+                        bulk_commit();
+                    }
+                } else {
+                    if (!warp_wait(bars.xfull(pr), xchunk & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    float u[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(u[j]) : "r"(xch + (uint32_t)(j * 32 + lane) * 4u)
+                                     : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.xempty(pr));
+                    const uint32_t buf = stage + (nstore & 1u) * 4096u;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    stage_col_sw64(buf, lane, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = v[j] / (1.0f + __expf(-v[j])) * u[j];
+                    stage_col_sw64(buf + 2048, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && col < I) {
+                        tma_store_2d(om.c0, col, row0, buf);
+                        tma_store_2d(om.c1, col, row0, buf + 2048);
+                        bulk_commit();
+                    }
+                }
+                ++xchunk;
+            } else if constexpr (F == L2_DGRAD) {
+                // g = dY . W2^T; da = w g; SwiGLU^T from the saved h; aw = w a;
+                // d(topk weight) partial = sum over this warp's features of g a
+                const int I = p.I;
+                const int col = t.f0 + 32 * warp;
+                const bool colok = col < I;
+                const int sl = __ldg(p.perm + row0 + lane);
+                const float wl = sl >= 0 ? __ldg(p.topk_w + sl) : 0.0f;
+                if (colok) {
+                    if (!warp_wait(bars.ein(warp), nin & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    ++nin;
+                }
+                {
+                    float prod[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) prod[j] = colok ? v[j] * lds_sw64(in_box + 4096, j, lane) : 0.0f;
+                    // lane j ends with the sum over the warp's 32 features of row j
+                    transpose_reduce_step<16>(prod, lane);
+                    transpose_reduce_step<8>(prod, lane);
+                    transpose_reduce_step<4>(prod, lane);
+                    transpose_reduce_step<2>(prod, lane);
+                    transpose_reduce_step<1>(prod, lane);
+                    if (colok) p.outf[(size_t)(row0 + lane) * (size_t)p.dw_cols + (size_t)(col >> 5)] = prod[0];
+                }
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float hg = 0.0f, hu = 0.0f, av = 0.0f;
+                    if (colok) {
+                        hg = lds_sw64(in_box, j, lane);
+                        hu = lds_sw64(in_box + 2048, j, lane);
+                        av = lds_sw64(in_box + 4096, j, lane);
+                    }
+                    const float wv = __shfl_sync(0xffffffffu, wl, j);
+                    const float da = wv * v[j];
+                    const float sg = 1.0f / (1.0f + __expf(-hg));
+                    sts_sw64(stage, j, lane, da * hu * sg * (1.0f + hg * (1.0f - sg)));
+                    sts_sw64(stage + 2048, j, lane, da * hg * sg);
+                    sts_sw64(stage + 4096, j, lane, wv * av);
+                }
+                // the input boxes are consumed: bring in the next chunk's
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && colok) {
+                    if (c32 + 1 < (t.n >> 5)) {
+                        const uint32_t eb = bars.ein(warp);
+                        mbar_arrive_expect_tx(eb, (uint32_t)kT2InBytes);
+                        tma_load_2d(in_box, mapH, col, row0 + 32, eb);
+                        tma_load_2d(in_box + 2048, mapH, I + col, row0 + 32, eb);
+                        tma_load_2d(in_box + 4096, mapAs, col, row0 + 32, eb);
+                    }
+                    tma_store_2d(om.c0, col, row0, stage);
+                    tma_store_2d(om.c0, I + col, row0, stage + 2048);
+                    tma_store_2d(om.c1, col, row0, stage + 4096);
+                    bulk_commit();
+                }
+            } else {
+                // one output: o = w (a . W2) (L2 forward) or dxp = dh . W1^T (L1 dgrad)
+                if constexpr (F == L2_FWD) {
+                    const int sl = __ldg(p.perm + row0 + lane);
+                    const float wl = sl >= 0 ? __ldg(p.topk_w + sl) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= __shfl_sync(0xffffffffu, wl, j);
+                }
+                const uint32_t buf = stage + (nstore & 1u) * 2048u;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                stage_col_sw64(buf, lane, v);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int col = t.f0 + 32 * warp;
+                if (lane == 0 && col < p.H) {
+                    tma_store_2d(om.c0, col, row0, buf);
+                    bulk_commit();
+                }
+            }
+            ++nstore;
+        }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+template <int F>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                         const __grid_constant__ CUtensorMap mapC0, const __grid_constant__ CUtensorMap mapC1,
+                         const __grid_constant__ CUtensorMap mapD, const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + T2<F>::kStages * kT2ABytes;
+    const uint32_t sStage = sB + T2<F>::kStages * kT2BBytes;
+    const uint32_t sIn = sStage + kEpiWarps * kStageEpiBytes;  // L2 dgrad epilogue inputs
+    const uint32_t bar_base = sIn + T2<F>::kInBytes;
+    uint8_t* tail = base_ptr + (bar_base - base);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * kT2NumBars);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const T2Bars bars{bar_base};
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank();
+
+    if (threadIdx.x == 0) {
+        const uint32_t full_count = 1u + (T2<F>::kGather ? 32u * kGatherWarps : 0u);
+        for (int s = 0; s < kT2Stages; ++s) {
+            mbar_init(bars.full(s), full_count);
+            mbar_init(bars.peer_full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bars.tfull(a), 1);
+            mbar_init(bars.tempty(a), 2 * kEpiWarps);
+            mbar_init(bars.xfull(a), 1);
+            mbar_init(bars.xempty(a), 1);
+        }
+        mbar_init(bars.drain(), 1);
+        for (int w = 0; w < kEpiWarps; ++w) mbar_init(bars.ein(w), 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc_pair(smem_addr(tmem_slot), 2 * kBN);
+        tmem_relinquish_pair();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_map(&mapA);
+        if constexpr (!T2<F>::kGather || F == L2_DGRAD) tma_prefetch_map(&mapB);
+        if constexpr (F == L2_DGRAD) tma_prefetch_map(&mapD);
+        tma_prefetch_map(&mapC0);
+        if constexpr (F == L1_FWD || F == L2_DGRAD) tma_prefetch_map(&mapC1);
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = t2_total_units(p);
+
+    if (warp == kWarpTma) {
+        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, total, sA, sB, bars, abort, rank);
+    } else if (warp >= kWarpGather0) {
+        if constexpr (T2<F>::kGather) t2_role_gather<F>(p, total, sB, bars, abort, warp - kWarpGather0, lane, rank);
+        cp_async_wait_all();
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            if (rank == 0) {
+                t2_role_mma<F>(p, total, sA, sB, bars, tmem_base, abort);
+                if (*abort) {
+                    // let every MMA already issued finish before TMEM is released
+                    tc_commit_pair_local(bars.drain());
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
+                    }
+                }
+            } else {
+                t2_role_relay<F>(p, total, bars, abort);
+            }
+        }
+    } else {
+        t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, total, bars, tmem_base,
+                            sStage + warp * kStageEpiBytes, sStage, sIn + warp * kT2InBytes, abort, warp, lane, rank);
+    }
+    if (warp == kWarpTma && lane == 0 && *abort) {
+        // bulk copies already issued land within microseconds; give them time
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 2000000ull) {
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 2 * kBN);
+    }
+    if (threadIdx.x == 0 && *abort) atomicOr(reinterpret_cast<int*>(p.status + MOE_STATUS_FLAGS), 1);
+}
+
+// Launches one 2-CTA cluster per unit up to the number of clusters that fit
+// on the device at once (persistent: each cluster walks units c, c + grid/2..).
+template <int F>
+int launch_gemm_pair(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
+    static int clusters_fit[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = t2_smem_bytes<F>();
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (clusters_fit[dev] == 0) {
+        // set once per device, outside any stream capture (on the first call)
+        e = cudaFuncSetAttribute(moe_gemm_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 t2_smem_bytes<F>());
+        if (e != cudaSuccess) return (int)e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return (int)e;
+        cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, moe_gemm_pair_kernel<F>, &cfg);
+        if (e != cudaSuccess) return (int)e;
+        if (n < 1) return (int)cudaErrorInvalidConfiguration;
+        clusters_fit[dev] = n;
+    }
+    if (max_units <= 0) return 0;
+    const int clusters = max_units < clusters_fit[dev] ? max_units : clusters_fit[dev];
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<F>, m.a, m.b, m.c0, m.c1, m.d, a);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaGetLastError();
+}
+
+}  // namespace moe

@@ -266,7 +266,7 @@ int compute_layout(const moe_shape* s, moe_layout* L) {
     L->a = o; o = align_up(o + 2 * R * (size_t)s->I, A);
     L->o = o; o = align_up(o + 2 * R * (size_t)s->H, A);
     L->saved_bytes = o;
-    L->dw_part_cols = (s->I + kBN - 1) / kBN;
+    L->dw_part_cols = (s->I + 31) / 32;  // one partial per 32 features of the L2 dgrad epilogue
     o = 0;
     L->dh = o; o = align_up(o + 2 * R * 2 * (size_t)s->I, A);
     L->aw = o; o = align_up(o + 2 * R * (size_t)s->I, A);
@@ -323,30 +323,31 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     auto* a = reinterpret_cast<__nv_bfloat16*>(sv + L.a);
     auto* o = reinterpret_cast<__nv_bfloat16*>(sv + L.o);
     cudaStream_t st = (cudaStream_t)stream;
-    // L1 grouped GEMM (gathered x) + SwiGLU -> h, a
+    // L1 grouped GEMM (gathered x) + SwiGLU -> h, a; units of 128 gate and
+    // 128 up features x one row chunk of one expert
     GemmMaps m1;
     memset(&m1, 0, sizeof m1);
-    if ((rc = map_w1_halves(&m1.b, W1, E, H, I))) return rc;
+    if ((rc = map_w1_halves(&m1.a, W1, E, H, I))) return rc;
     if ((rc = map_2d(&m1.c0, h, L.rows_cap, 2 * I, 32, 32, "h (store)"))) return rc;
     if ((rc = map_2d(&m1.c1, a, L.rows_cap, I, 32, 32, "a (store)"))) return rc;
     GemmArgs g1 = base_args(shape, L, route);
     g1.K = H;
-    g1.n_tiles = cdiv(I, kBN / 2);
+    g1.n_tiles = cdiv(I, 2 * 64);
     g1.gsrc = static_cast<const __nv_bfloat16*>(x);
-    int e = launch_gemm(L1_FWD, g1, m1, grid_for(c.sms, L.tiles_cap * g1.n_tiles), st);
+    int e = launch_gemm(L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
     if (e) return cuda_fail(e, "L1 grouped GEMM launch");
 
-    // L2 grouped GEMM + routing-weight epilogue -> o
+    // L2 grouped GEMM + routing-weight epilogue -> o; units of 256 features
     GemmMaps m2;
     memset(&m2, 0, sizeof m2);
-    if ((rc = map_2d(&m2.a, a, L.rows_cap, I, 64, kBM, "a"))) return rc;
-    if ((rc = map_3d(&m2.b, W2, E, I, H, 64, 64, "W2"))) return rc;
-    if ((rc = map_2d(&m2.c0, o, L.rows_cap, H, 64, 32, "o (store)"))) return rc;
+    if ((rc = map_3d(&m2.a, W2, E, I, H, 64, 64, "W2"))) return rc;
+    if ((rc = map_2d(&m2.b, a, L.rows_cap, I, 64, 32, "a (rows)"))) return rc;
+    if ((rc = map_2d(&m2.c0, o, L.rows_cap, H, 32, 32, "o (store)"))) return rc;
     GemmArgs g2 = base_args(shape, L, route);
     g2.K = I;
-    g2.n_tiles = cdiv(H, kBN);
+    g2.n_tiles = cdiv(H, 2 * 128);
     g2.topk_w = topk_w;
-    e = launch_gemm(L2_FWD, g2, m2, grid_for(c.sms, L.tiles_cap * g2.n_tiles), st);
+    e = launch_gemm(L2_FWD, g2, m2, (int)L.tiles_cap * g2.n_tiles, st);
     if (e) return cuda_fail(e, "L2 grouped GEMM launch");
 
     // combine: y[t] = sum_j o[inv[t, j]]
@@ -390,21 +391,24 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     auto* dxp = reinterpret_cast<__nv_bfloat16*>(ws + L.dxp);
     auto* dwp = reinterpret_cast<float*>(ws + L.dw_part);
     const auto* inv = reinterpret_cast<const int32_t*>(route + L.inv);
-    // L2 dgrad (gathered dY) + SwiGLU^T -> dh, aw, dw_part
+    // L2 dgrad (gathered dY) + SwiGLU^T -> dh, aw, dw_part; units of 256
+    // features of I
     GemmMaps m;
     memset(&m, 0, sizeof m);
-    if ((rc = map_3d(&m.b, W2, E, I, H, 64, kBN, "W2 (K-major)"))) return rc;
+    if ((rc = map_3d(&m.a, W2, E, I, H, 64, 128, "W2 (K-major)"))) return rc;
+    if ((rc = map_2d(&m.b, h, L.rows_cap, 2 * I, 32, 32, "h (epilogue input)"))) return rc;
+    if ((rc = map_2d(&m.d, a, L.rows_cap, I, 32, 32, "a (epilogue input)"))) return rc;
     if ((rc = map_2d(&m.c0, dh, L.rows_cap, 2 * I, 32, 32, "dh (store)"))) return rc;
     if ((rc = map_2d(&m.c1, aw, L.rows_cap, I, 32, 32, "aw (store)"))) return rc;
     GemmArgs g = base_args(shape, L, route);
     g.K = H;
-    g.n_tiles = cdiv(I, kBN);
+    g.n_tiles = cdiv(I, 2 * 128);
     g.gsrc = static_cast<const __nv_bfloat16*>(dY);
     g.topk_w = topk_w;
     g.h_in = h;
     g.a_in = a;
     g.outf = dwp;
-    int e = launch_gemm(L2_DGRAD, g, m, grid_for(c.sms, L.tiles_cap * g.n_tiles), st);
+    int e = launch_gemm(L2_DGRAD, g, m, (int)L.tiles_cap * g.n_tiles, st);
     if (e) return cuda_fail(e, "L2 dgrad launch");
 
     // dW2[e] = aw_e^T . dY_e (variable K)
@@ -431,16 +435,16 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     e = launch_gemm(DW1, g4, m4, grid_for(c.sms, (long long)E * g4.m_tiles * g4.n_tiles), st);
     if (e) return cuda_fail(e, "dW1 launch");
 
-    // L1 dgrad: dxp = dh . W1[e]^T
+    // L1 dgrad: dxp = dh . W1[e]^T; units of 256 features of H
     GemmMaps m5;
     memset(&m5, 0, sizeof m5);
-    if ((rc = map_2d(&m5.a, dh, L.rows_cap, 2 * I, 64, kBM, "dh (tiles)"))) return rc;
-    if ((rc = map_3d(&m5.b, W1, E, H, 2 * I, 64, kBN, "W1 (K-major)"))) return rc;
-    if ((rc = map_2d(&m5.c0, dxp, L.rows_cap, H, 64, 32, "dxp (store)"))) return rc;
+    if ((rc = map_3d(&m5.a, W1, E, H, 2 * I, 64, 128, "W1 (K-major)"))) return rc;
+    if ((rc = map_2d(&m5.b, dh, L.rows_cap, 2 * I, 64, 32, "dh (rows)"))) return rc;
+    if ((rc = map_2d(&m5.c0, dxp, L.rows_cap, H, 32, 32, "dxp (store)"))) return rc;
     GemmArgs g5 = base_args(shape, L, route);
     g5.K = 2 * I;
-    g5.n_tiles = cdiv(H, kBN);
-    e = launch_gemm(L1_DGRAD, g5, m5, grid_for(c.sms, L.tiles_cap * g5.n_tiles), st);
+    g5.n_tiles = cdiv(H, 2 * 128);
+    e = launch_gemm(L1_DGRAD, g5, m5, (int)L.tiles_cap * g5.n_tiles, st);
     if (e) return cuda_fail(e, "L1 dgrad launch");
 
     // backward combine and the routing-weight gradient

@@ -10,7 +10,8 @@
 
 namespace moe {
 
-// Grouped-GEMM tile: 128 routed rows x 256 output columns x 64 of K per stage.
+// Weight-gradient tile: 128 x 256 of dW[e], 64 routed rows of K per stage (the
+// row-grouped SM-pair kernels use the same 64-deep K blocks).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
@@ -58,10 +59,11 @@ struct GemmArgs {
     float* outf;                // dw_part (L2_DGRAD epilogue); bf16 outputs leave by TMA store
 };
 
-// Tensor maps of one grouped-GEMM launch: operands A, B (loads) and up to
-// two outputs C0, C1 (TMA stores).  Unused maps are zero.
+// Tensor maps of one grouped-GEMM launch: operands A, B (loads), up to two
+// outputs C0, C1 (TMA stores) and one more epilogue input D.  Unused maps
+// are zero.
 struct GemmMaps {
-    CUtensorMap a, b, c0, c1;
+    CUtensorMap a, b, c0, c1, d;
 };
 
 // Layout of the three workspaces (host only).

@@ -31,7 +31,7 @@ def test_layout(lib, T, H, I, E, k):
     L = B.moe_workspace_layout(B.shape_of(T, H, I, E, k))
     assert L.rows_cap == oracle.rows_cap(T, E, k, 128)
     assert L.tiles_cap == L.rows_cap // 128
-    assert L.dw_part_cols == (I + 255) // 256
+    assert L.dw_part_cols == (I + 31) // 32
     offs = [L.counts, L.offs, L.perm, L.inv, L.tiles, L.status, L.pair_offs, L.pair_owner]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert L.offs >= L.counts + 4 * E and L.perm >= L.offs + 4 * (E + 1)
