@@ -61,6 +61,8 @@ def _lib():
             L.oracle_rows_cap.restype = i64
             L.oracle_route.argtypes = [i32, i32, i32, i32] + [vp] * 7
             L.oracle_route.restype = None
+            L.oracle_router_topk.argtypes = [i32, i32, i32, vp, vp, vp]
+            L.oracle_router_topk.restype = None
             for suf in ("b16", "f64"):
                 getattr(L, f"oracle_forward_{suf}").argtypes = [i32] * 5 + [vp] * 5 + [i32, vp, vp]
                 getattr(L, f"oracle_backward_tokens_{suf}").argtypes = [i32] * 5 + [vp] * 6 + [i32, vp, vp, vp]
@@ -83,6 +85,21 @@ def num_threads() -> int:
 
 def rows_cap(T: int, E: int, k: int, bm: int) -> int:
     return int(_lib().oracle_rows_cap(T, E, k, bm))
+
+
+def router_topk(logits: np.ndarray, k: int):
+    """Top-k gating of router logits [T, E] (FP32): returns topk_idx int32
+    [T, k] (decreasing logit, equal logits in increasing expert id; NaN
+    counts as -inf) and topk_w float32 [T, k] (softmax over the k selected
+    logits, FP64 then rounded)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    idx = np.zeros((max(T, 1), k), np.int32)
+    w = np.zeros((max(T, 1), k), np.float32)
+    _lib().oracle_router_topk(T, E, k, _p(lg), _p(idx), _p(w))
+    return idx[:T], w[:T]
 
 
 def route(topk_idx: np.ndarray, E: int, bm: int = 128) -> dict:

@@ -27,6 +27,57 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* ----------------------------------------------------------------- router */
+
+/*
+ * Top-k gating from router logits (the step in front of the layer: the
+ * Primus-Turbo "Mega MoE" README takes topk_idx / topk_weights from the
+ * router, "Key points"; the ROCm Primus MoE guide's router produces them
+ * from logits).  For each token t, over its E logits:
+ *   key(v) = v, except that a NaN counts as -infinity;
+ *   topk_idx[t, 0..k-1] = the k experts with the largest keys, in
+ *     decreasing key order, equal keys in increasing expert id;
+ *   topk_w[t, j] = exp(key_j - m) / sum_i exp(key_i - m) over the k selected
+ *     keys, m = the largest selected key, computed in FP64 and rounded to
+ *     FP32 (softmax over the selected logits).  When m is infinite the
+ *     weights are the limit: 1/n on the n selected keys equal to m, 0 on the
+ *     others.
+ * Selection is done by k passes over the row, each taking the best key not
+ * yet taken (plain loops, no sort).
+ */
+static double router_key(float v) { return isnan(v) ? -INFINITY : (double)v; }
+
+void oracle_router_topk(int T, int E, int k, const float* logits, int32_t* topk_idx, float* topk_w) {
+    char* taken = (char*)malloc((size_t)(E > 0 ? E : 1));
+    double* key = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+    for (int t = 0; t < T; ++t) {
+        const float* row = logits + (size_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || router_key(row[e]) > router_key(row[best])) best = e;
+            }
+            taken[best] = 1;
+            topk_idx[(size_t)t * k + j] = best;
+            key[j] = router_key(row[best]);
+        }
+        double m = key[0];
+        if (isinf(m)) {
+            int n = 0;
+            for (int j = 0; j < k; ++j) n += key[j] == m;
+            for (int j = 0; j < k; ++j) topk_w[(size_t)t * k + j] = key[j] == m ? (float)(1.0 / n) : 0.0f;
+        } else {
+            double sum = 0;
+            for (int j = 0; j < k; ++j) sum += exp(key[j] - m);
+            for (int j = 0; j < k; ++j) topk_w[(size_t)t * k + j] = (float)(exp(key[j] - m) / sum);
+        }
+    }
+    free(taken);
+    free(key);
+}
+
 /* ---------------------------------------------------------------- routing */
 
 /* Row capacity of the block-M padded layout: the padded row count
