@@ -112,6 +112,22 @@ int moe_workspace_layout(const moe_shape* shape, moe_layout* out);
  * route_bytes.  Bit-exact and deterministic; no host synchronisation. */
 int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* route_ws, void* stream);
 
+/* Router top-k gating fused in front of the routing prologue (the router
+ * that produces topk_idx / topk_weights: Mega MoE README, "Key points"; ROCm
+ * Primus MoE training guide, router).  logits f32[T, E] (device, row-major).
+ * For each token writes topk_idx int32[T, k]: the k largest logits in
+ * decreasing order, equal logits in increasing expert id, a NaN logit
+ * ranked as -infinity; and topk_w f32[T, k]: the softmax over the k selected
+ * logits (when the largest selected logit is infinite, 1/n on the n selected
+ * logits equal to it and 0 elsewhere).  Then builds every route_ws table
+ * from that topk_idx exactly as moe_route_prologue does.  All device
+ * buffers are the caller's and 16-byte aligned; two kernels on `stream`, no
+ * host synchronisation, capturable.  topk_idx and topk_w are overwritten.
+ * Errors: MOE_EINVAL for a bad shape or a NULL pointer, MOE_EUNSUPPORTED for
+ * a misaligned pointer, MOE_ECUDA for a launch error. */
+int moe_router_topk(const moe_shape* shape, const float* logits, int32_t* topk_idx, float* topk_w, void* route_ws,
+                    void* stream);
+
 /* Forward (Mega MoE README, "Pipeline"): x bf16[T,H], W1 bf16[E,H,2I]
  * (columns [0,I) gate, [I,2I) up), W2 bf16[E,I,H], topk_w f32[T,k],
  * route_ws from moe_route_prologue on the same topk_idx (its status words

@@ -63,10 +63,12 @@ def lib():
             vp, P = ctypes.c_void_p, ctypes.POINTER
             L.moe_workspace_layout.argtypes = [P(MoeShape), P(MoeLayout)]
             L.moe_route_prologue.argtypes = [P(MoeShape), vp, vp, vp]
+            L.moe_router_topk.argtypes = [P(MoeShape)] + [vp] * 5
             L.moe_forward.argtypes = [P(MoeShape)] + [vp] * 8
             L.moe_backward.argtypes = [P(MoeShape)] + [vp] * 13
             L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
-            for n in ("moe_workspace_layout", "moe_route_prologue", "moe_forward", "moe_backward", "moe_read_status"):
+            for n in ("moe_workspace_layout", "moe_route_prologue", "moe_router_topk", "moe_forward", "moe_backward",
+                      "moe_read_status"):
                 getattr(L, n).restype = ctypes.c_int
             L.moe_trace_begin.argtypes = [vp, ctypes.c_int]
             L.moe_trace_begin.restype = ctypes.c_int
@@ -115,6 +117,17 @@ def _ptr(t, dtype, numel=None, name="tensor"):
     if numel is not None and t.numel() < numel:
         raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
     return t.data_ptr()
+
+
+def moe_router_topk(shape: MoeShape, logits, topk_idx, topk_w, route_ws, stream=None):
+    """Router top-k gating (logits f32 [T, E] -> topk_idx int32 [T, k], topk_w
+    f32 [T, k]) followed by the routing prologue into route_ws."""
+    L = moe_workspace_layout(shape)
+    _check(lib().moe_router_topk(
+        ctypes.byref(shape), _ptr(logits, torch.float32, shape.T * shape.E, "logits"),
+        _ptr(topk_idx, torch.int32, shape.T * shape.k, "topk_idx"),
+        _ptr(topk_w, torch.float32, shape.T * shape.k, "topk_w"),
+        _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), _stream(stream)))
 
 
 def moe_route_prologue(shape: MoeShape, topk_idx, route_ws, stream=None):

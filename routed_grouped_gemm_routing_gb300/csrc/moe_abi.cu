@@ -303,6 +303,28 @@ int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* ro
     return MOE_OK;
 }
 
+int moe_router_topk(const moe_shape* shape, const float* logits, int32_t* topk_idx, float* topk_w, void* route_ws,
+                    void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!route_ws || (shape->T > 0 && (!logits || !topk_idx || !topk_w))) return fail(MOE_EINVAL, "NULL pointer argument");
+    const void* ptrs[] = {logits, topk_idx, topk_w, route_ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if ((rc = query_device(&c, route_ws))) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    trace_pre(st);
+    int e = launch_router_topk(logits, shape->T, shape->E, shape->k, topk_idx, topk_w, c.sms, st);
+    trace_post(st, "router_topk");
+    if (e) return cuda_fail(e, "router top-k launch");
+    trace_pre(st);
+    e = launch_route_prologue(*shape, c.L, topk_idx, static_cast<uint8_t*>(route_ws), st);
+    trace_post(st, "route_prologue");
+    if (e) return cuda_fail(e, "route prologue launch");
+    return MOE_OK;
+}
+
 int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2, const float* topk_w,
                 void* route_ws, void* saved, void* y, void* stream) {
     Ctx c;

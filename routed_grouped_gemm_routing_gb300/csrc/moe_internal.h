@@ -75,6 +75,8 @@ int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t
 int launch_gemm(int flavour, const GemmArgs& a, const GemmMaps& maps, int grid, cudaStream_t st);
 int launch_combine(const __nv_bfloat16* rows, const int32_t* inv, int T, int k, int H, __nv_bfloat16* out,
                    int num_sms, cudaStream_t st);
+int launch_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w, int num_sms,
+                       cudaStream_t st);
 int launch_dw_reduce(const float* dw_part, int cols, const int32_t* inv, long long slots, float* out, int num_sms,
                      cudaStream_t st);
 
