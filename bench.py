@@ -63,10 +63,16 @@ def load_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
+# the sources that define the grouped-GEMM kernels whose DRAM traffic
+# profiles/traffic.json records; a change to any of them voids the record
+GEMM_SOURCES = ("grouped_gemm.cuh", "grouped_gemm_2sm.cuh", "ptx.cuh", "moe_internal.h", "gemm_fwd.cu",
+                "gemm_dgrad.cu", "gemm_wgrad.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "routed_grouped_gemm_routing_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in GEMM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -386,6 +392,36 @@ def run_ours(args):
                "note": "x, topk_idx, topk_weights, dY copied in from pinned host memory and y, dx, "
                        "d topk_weights copied out every step; dW1/dW2 stay on the device"}
 
+    # the router stage in front of the layer (logits -> top-k ids and weights
+    # -> routing tables), timed on its own: it is not part of the layer step
+    # the metric counts, which takes topk_idx / topk_weights as inputs
+    router = None
+    if not args.no_router:
+        g = torch.Generator(device=dev)
+        g.manual_seed(args.seed * 7919 + 11)
+        logits = torch.randn(T, E, generator=g, device=dev, dtype=torch.float32)
+        r_idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+        r_w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        r_route = torch.empty(max(ws.layout.route_bytes, 16), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            B.moe_router_topk(ws.shape, logits, r_idx, r_w, r_route)
+        torch.cuda.synchronize()
+        rtrace = B.KernelTrace(max_launches=2 * 20)
+        with rtrace:
+            for _ in range(20):
+                B.moe_router_topk(ws.shape, logits, r_idx, r_w, r_route)
+        torch.cuda.synchronize()
+        rper = {}
+        for name, d in rtrace.durations_ms():
+            rper.setdefault(name, []).append(d)
+        rk = {n: statistics.median(v) for n, v in rper.items()}
+        r_bytes = T * E * 4 + T * k * 8  # logits read once, ids and weights written once
+        router = {"ms": sum(rk.values()), "kernels_ms": rk,
+                  "router_topk_gbs": r_bytes / (rk["router_topk"] / 1e3) / 1e9,
+                  "router_topk_frac_of_hbm": r_bytes / (rk["router_topk"] / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+                  "note": "median of 20 runs of moe_router_topk (router kernel + routing prologue) on the "
+                          "workload's logits; not part of the layer step"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -423,6 +459,7 @@ def run_ours(args):
         "roofline": roofline,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "router": router,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -440,6 +477,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-router", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=2)
