@@ -64,9 +64,10 @@ def _lib():
             L.oracle_router_topk.argtypes = [i32, i32, i32, vp, vp, vp]
             L.oracle_router_topk.restype = None
             for suf in ("b16", "f64"):
-                getattr(L, f"oracle_forward_{suf}").argtypes = [i32] * 5 + [vp] * 5 + [i32, vp, vp]
-                getattr(L, f"oracle_backward_tokens_{suf}").argtypes = [i32] * 5 + [vp] * 6 + [i32, vp, vp, vp]
-                getattr(L, f"oracle_backward_experts_{suf}").argtypes = [i32] * 5 + [vp] * 6 + [i32, vp, vp, vp]
+                f64 = ctypes.c_double
+                getattr(L, f"oracle_forward_{suf}").argtypes = [i32] * 5 + [f64] + [vp] * 5 + [i32, vp, vp]
+                getattr(L, f"oracle_backward_tokens_{suf}").argtypes = [i32] * 5 + [f64] + [vp] * 6 + [i32, vp, vp, vp]
+                getattr(L, f"oracle_backward_experts_{suf}").argtypes = [i32] * 5 + [f64] + [vp] * 6 + [i32, vp, vp, vp]
                 for n in ("forward", "backward_tokens", "backward_experts"):
                     getattr(L, f"oracle_{n}_{suf}").restype = None
             L.oracle_num_threads.restype = ctypes.c_int
@@ -146,21 +147,22 @@ def _dims(x, W1, W2, topk_idx):
     return T, H, I, E, k
 
 
-def forward(x, W1, W2, topk_idx, topk_w, tokens=None, precision="b16"):
+def forward(x, W1, W2, topk_idx, topk_w, tokens=None, precision="b16", clamp=0.0):
     """y rows [len(tokens), H] for the listed tokens (all tokens by default).
 
     precision "b16": x, W1, W2 are bfloat16 bit patterns (uint16 arrays),
-    topk_w float32, FP32 arithmetic.  precision "f64": everything float64."""
+    topk_w float32, FP32 arithmetic.  precision "f64": everything float64.
+    clamp > 0: SwiGLU inputs clamped to [-clamp, clamp] (0: no clamp)."""
     (x, W1, W2, idx, w), rdt = _prep(precision, x, W1, W2, topk_idx, topk_w)
     T, H, I, E, k = _dims(x, W1, W2, idx)
     toks = np.ascontiguousarray(np.arange(T) if tokens is None else tokens, dtype=np.int32)
     y = np.zeros((len(toks), H), rdt)
     fn = getattr(_lib(), f"oracle_forward_{precision}")
-    fn(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), len(toks), _p(toks), _p(y))
+    fn(T, H, I, E, k, float(clamp), _p(x), _p(W1), _p(W2), _p(idx), _p(w), len(toks), _p(toks), _p(y))
     return y
 
 
-def backward_tokens(x, W1, W2, topk_idx, topk_w, dY, tokens=None, precision="b16"):
+def backward_tokens(x, W1, W2, topk_idx, topk_w, dY, tokens=None, precision="b16", clamp=0.0):
     """(dx [n, H], dtopk_w [n, k]) for the listed tokens."""
     (x, W1, W2, idx, w, dY), rdt = _prep(precision, x, W1, W2, topk_idx, topk_w, dY)
     T, H, I, E, k = _dims(x, W1, W2, idx)
@@ -168,11 +170,12 @@ def backward_tokens(x, W1, W2, topk_idx, topk_w, dY, tokens=None, precision="b16
     dx = np.zeros((len(toks), H), rdt)
     dw = np.zeros((len(toks), k), rdt)
     fn = getattr(_lib(), f"oracle_backward_tokens_{precision}")
-    fn(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), _p(dY), len(toks), _p(toks), _p(dx), _p(dw))
+    fn(T, H, I, E, k, float(clamp), _p(x), _p(W1), _p(W2), _p(idx), _p(w), _p(dY), len(toks), _p(toks), _p(dx),
+       _p(dw))
     return dx, dw
 
 
-def backward_experts(x, W1, W2, topk_idx, topk_w, dY, experts=None, precision="b16"):
+def backward_experts(x, W1, W2, topk_idx, topk_w, dY, experts=None, precision="b16", clamp=0.0):
     """(dW1 [n, H, 2I], dW2 [n, I, H]) for the listed experts."""
     (x, W1, W2, idx, w, dY), rdt = _prep(precision, x, W1, W2, topk_idx, topk_w, dY)
     T, H, I, E, k = _dims(x, W1, W2, idx)
@@ -180,5 +183,6 @@ def backward_experts(x, W1, W2, topk_idx, topk_w, dY, experts=None, precision="b
     dW1 = np.zeros((len(exps), H, 2 * I), rdt)
     dW2 = np.zeros((len(exps), I, H), rdt)
     fn = getattr(_lib(), f"oracle_backward_experts_{precision}")
-    fn(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), _p(dY), len(exps), _p(exps), _p(dW1), _p(dW2))
+    fn(T, H, I, E, k, float(clamp), _p(x), _p(W1), _p(W2), _p(idx), _p(w), _p(dY), len(exps), _p(exps), _p(dW1),
+       _p(dW2))
     return dW1, dW2

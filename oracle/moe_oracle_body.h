@@ -31,10 +31,21 @@
 
 static REAL FN(sigmoid_)(REAL z) { return (REAL)1 / ((REAL)1 + (REAL)exp(-(double)z)); }
 
+/* Activation clamp (reading of the DeepGEMM Mega-MoE article's
+ * `activation_clamp` argument, given there without a formula): with c > 0
+ * both SwiGLU inputs are clamped to [-c, c] before a = silu(gate) * up, and
+ * the gradient passes where -c <= z <= c and is 0 outside; c <= 0 is no
+ * clamp. */
+static REAL FN(clamp_)(REAL z, double c) {
+    if (c <= 0) return z;
+    return z < (REAL)-c ? (REAL)-c : (z > (REAL)c ? (REAL)c : z);
+}
+static REAL FN(clamp_pass_)(REAL z, double c) { return (c <= 0 || (z >= (REAL)-c && z <= (REAL)c)) ? (REAL)1 : (REAL)0; }
+
 /* Forward of one slot: fills hg, hu, a (length I) and o (length H) for token
  * row xt routed to the expert whose weights start at W1e / W2e. */
 static void FN(slot_forward_)(int H, int I, const IN_T* x, size_t xoff,
-                              const IN_T* W1, size_t w1off, const IN_T* W2, size_t w2off,
+                              const IN_T* W1, size_t w1off, const IN_T* W2, size_t w2off, double clamp,
                               REAL* hg, REAL* hu, REAL* a, REAL* o) {
     for (int i = 0; i < I; ++i) { hg[i] = 0; hu[i] = 0; }
     for (int h = 0; h < H; ++h) {
@@ -45,7 +56,10 @@ static void FN(slot_forward_)(int H, int I, const IN_T* x, size_t xoff,
             hu[i] += xv * LD(W1, row + (size_t)I + (size_t)i);
         }
     }
-    for (int i = 0; i < I; ++i) a[i] = hg[i] * FN(sigmoid_)(hg[i]) * hu[i];
+    for (int i = 0; i < I; ++i) {
+        REAL g = FN(clamp_)(hg[i], clamp), u = FN(clamp_)(hu[i], clamp);
+        a[i] = g * FN(sigmoid_)(g) * u;
+    }
     for (int c = 0; c < H; ++c) o[c] = 0;
     for (int i = 0; i < I; ++i) {
         REAL av = a[i];
@@ -62,7 +76,7 @@ static void FN(slot_forward_)(int H, int I, const IN_T* x, size_t xoff,
  *   dhg[i] = da[i] * hu[i] * s(hg[i]) * (1 + hg[i] (1 - s(hg[i])))   (d silu)
  *   dhu[i] = da[i] * silu(hg[i])                                                */
 static void FN(slot_backward_)(int H, int I, const IN_T* dY, size_t dyoff, REAL wv,
-                               const IN_T* W2, size_t w2off,
+                               const IN_T* W2, size_t w2off, double clamp,
                                const REAL* hg, const REAL* hu,
                                REAL* da, REAL* dhg, REAL* dhu) {
     for (int i = 0; i < I; ++i) {
@@ -72,14 +86,15 @@ static void FN(slot_backward_)(int H, int I, const IN_T* dY, size_t dyoff, REAL 
         da[i] = s;
     }
     for (int i = 0; i < I; ++i) {
-        REAL sg = FN(sigmoid_)(hg[i]);
-        dhg[i] = da[i] * hu[i] * sg * ((REAL)1 + hg[i] * ((REAL)1 - sg));
-        dhu[i] = da[i] * hg[i] * sg;
+        REAL g = FN(clamp_)(hg[i], clamp), u = FN(clamp_)(hu[i], clamp);
+        REAL sg = FN(sigmoid_)(g);
+        dhg[i] = da[i] * u * sg * ((REAL)1 + g * ((REAL)1 - sg)) * FN(clamp_pass_)(hg[i], clamp);
+        dhu[i] = da[i] * g * sg * FN(clamp_pass_)(hu[i], clamp);
     }
 }
 
 /* y rows for the listed tokens: y_out[n, :] is token tok_list[n]. */
-void FN(oracle_forward_)(int T, int H, int I, int E, int k,
+void FN(oracle_forward_)(int T, int H, int I, int E, int k, double clamp,
                          const IN_T* x, const IN_T* W1, const IN_T* W2,
                          const int32_t* topk_idx, const W_T* topk_w,
                          int n_tok, const int32_t* tok_list, REAL* y_out) {
@@ -99,7 +114,7 @@ void FN(oracle_forward_)(int T, int H, int I, int E, int k,
                 int e = topk_idx[(size_t)t * k + j];
                 if (e < 0 || e >= E) continue;
                 FN(slot_forward_)(H, I, x, (size_t)t * H, W1, (size_t)e * H * 2 * I,
-                                  W2, (size_t)e * I * H, hg, hu, a, o);
+                                  W2, (size_t)e * I * H, clamp, hg, hu, a, o);
                 REAL wv = (REAL)topk_w[(size_t)t * k + j];
                 for (int c = 0; c < H; ++c) y[c] += wv * o[c];
             }
@@ -111,7 +126,7 @@ void FN(oracle_forward_)(int T, int H, int I, int E, int k,
 /* dx rows and d(topk_w) rows for the listed tokens.
  *   dx[t,h]      = sum_j sum_i dhg[i] W1[e,h,i] + dhu[i] W1[e,h,I+i]
  *   dtopk_w[t,j] = sum_c dY[t,c] o[c]        (derivative of y w.r.t. w[t,j]) */
-void FN(oracle_backward_tokens_)(int T, int H, int I, int E, int k,
+void FN(oracle_backward_tokens_)(int T, int H, int I, int E, int k, double clamp,
                                  const IN_T* x, const IN_T* W1, const IN_T* W2,
                                  const int32_t* topk_idx, const W_T* topk_w, const IN_T* dY,
                                  int n_tok, const int32_t* tok_list,
@@ -137,12 +152,12 @@ void FN(oracle_backward_tokens_)(int T, int H, int I, int E, int k,
                 *dw = 0;
                 if (e < 0 || e >= E) continue;
                 size_t w1off = (size_t)e * H * 2 * I, w2off = (size_t)e * I * H;
-                FN(slot_forward_)(H, I, x, (size_t)t * H, W1, w1off, W2, w2off, hg, hu, a, o);
+                FN(slot_forward_)(H, I, x, (size_t)t * H, W1, w1off, W2, w2off, clamp, hg, hu, a, o);
                 REAL s = 0;
                 for (int c = 0; c < H; ++c) s += LD(dY, (size_t)t * H + (size_t)c) * o[c];
                 *dw = s;
                 REAL wv = (REAL)topk_w[(size_t)t * k + j];
-                FN(slot_backward_)(H, I, dY, (size_t)t * H, wv, W2, w2off, hg, hu, da, dhg, dhu);
+                FN(slot_backward_)(H, I, dY, (size_t)t * H, wv, W2, w2off, clamp, hg, hu, da, dhg, dhu);
                 for (int h = 0; h < H; ++h) {
                     size_t row = w1off + (size_t)h * (size_t)(2 * I);
                     REAL acc = 0;
@@ -164,7 +179,7 @@ void FN(oracle_backward_tokens_)(int T, int H, int I, int E, int k,
  * An expert that receives no slot gets exactly zero.  The per-slot terms are
  * computed first; each output row is then summed over the slots in order
  * (rows are independent, so they are spread over threads). */
-void FN(oracle_backward_experts_)(int T, int H, int I, int E, int k,
+void FN(oracle_backward_experts_)(int T, int H, int I, int E, int k, double clamp,
                                   const IN_T* x, const IN_T* W1, const IN_T* W2,
                                   const int32_t* topk_idx, const W_T* topk_w, const IN_T* dY,
                                   int n_exp, const int32_t* exp_list,
@@ -193,10 +208,10 @@ void FN(oracle_backward_experts_)(int T, int H, int I, int E, int k,
             for (int q = 0; q < ns; ++q) {
                 int64_t s = slots[q];
                 int t = (int)(s / k);
-                FN(slot_forward_)(H, I, x, (size_t)t * H, W1, w1off, W2, w2off, hg, hu, a, o);
+                FN(slot_forward_)(H, I, x, (size_t)t * H, W1, w1off, W2, w2off, clamp, hg, hu, a, o);
                 REAL wv = (REAL)topk_w[s];
                 REAL* dhq = dh + (size_t)q * 2 * I;
-                FN(slot_backward_)(H, I, dY, (size_t)t * H, wv, W2, w2off, hg, hu, da, dhq, dhq + I);
+                FN(slot_backward_)(H, I, dY, (size_t)t * H, wv, W2, w2off, clamp, hg, hu, da, dhq, dhq + I);
                 for (int i = 0; i < I; ++i) aw[(size_t)q * I + i] = a[i] * wv;
             }
             free(hg); free(hu); free(a); free(o); free(da);
