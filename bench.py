@@ -132,7 +132,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_sample(shape, inputs, n_tok, seed=0):
+def oracle_sample(shape, inputs, n_tok, seed=0, clamp=0.0):
     """Host copies of a bounded sample of the workload for the CPU oracle:
     n_tok tokens (forward, dx, d topk_weights) and the weight gradients of one
     typically loaded expert.  Returns (callable running it, useful FLOPs,
@@ -169,9 +169,9 @@ def oracle_sample(shape, inputs, n_tok, seed=0):
     wa = inputs["topk_w"].cpu().numpy().astype(np.float32)
 
     def run():
-        oracle.forward(xt, W1t, W2t, idx_t, wt)
-        oracle.backward_tokens(xt, W1t, W2t, idx_t, wt, dYt)
-        oracle.backward_experts(xa, W1e, W2e, idx_e, wa, dYa)
+        oracle.forward(xt, W1t, W2t, idx_t, wt, clamp=clamp)
+        oracle.backward_tokens(xt, W1t, W2t, idx_t, wt, dYt, clamp=clamp)
+        oracle.backward_experts(xa, W1e, W2e, idx_e, wa, dYa, clamp=clamp)
 
     slots = int(((idx >= 0) & (idx < E)).sum())
     flops = 6.0 * H * I * slots + 6.0 * H * I * slots + 6.0 * H * I * int(counts[e])
@@ -190,13 +190,16 @@ def cpu_cores():
 METRIC = "MoE layer fwd+bwd TFLOP/s (useful FLOPs) & routed tokens/s; % of GB300 BF16 dense peak"
 
 
-def config_dict(shape, world):
+def config_dict(shape, world, activation_clamp=0.0):
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     label = " (DeepSeek-V3-shaped expert layer)" if shape.name == "v3" else ""
-    return {"workload": f"{shape.name}: T={T} H={H} I={I} E={E} k={k}{label}",
-            "T": T, "H": H, "I": I, "E": E, "k": k, "block_m": 128,
-            "l2": "inputs larger than L2 (weights alone are many times the 129 MB L2)",
-            "parallelism": "replicas" if world > 1 else "single GPU"}
+    out = {"workload": f"{shape.name}: T={T} H={H} I={I} E={E} k={k}{label}",
+           "T": T, "H": H, "I": I, "E": E, "k": k, "block_m": 128,
+           "l2": "inputs larger than L2 (weights alone are many times the 129 MB L2)",
+           "parallelism": "replicas" if world > 1 else "single GPU"}
+    if activation_clamp > 0:
+        out["activation_clamp"] = activation_clamp
+    return out
 
 
 # -------------------------------------------------------------- main arms
@@ -213,7 +216,8 @@ def run_reference(args):
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inputs = make_layer_inputs(shape, seed=args.seed, device=dev)
-    run, flops, desc = oracle_sample(shape, inputs, n_tok=args.ref_tokens, seed=args.seed)
+    run, flops, desc = oracle_sample(shape, inputs, n_tok=args.ref_tokens, seed=args.seed,
+                                     clamp=args.activation_clamp)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -226,7 +230,7 @@ def run_reference(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": config_dict(shape, args.gpus),
+        "config": config_dict(shape, args.gpus, args.activation_clamp),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -260,7 +264,7 @@ def run_ours(args):
     shape = CONFIGS[args.config]
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     inp = make_layer_inputs(shape, seed=args.seed + rank, device=dev)
-    ws = MoEWorkspace(T, H, I, E, k, device=dev)
+    ws = MoEWorkspace(T, H, I, E, k, device=dev, activation_clamp=args.activation_clamp)
     s = ws.shape
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     dx = torch.empty_like(y)
@@ -427,7 +431,8 @@ def run_ours(args):
         import oracle
 
         oracle.build()
-        run, flops, desc = oracle_sample(shape, inp, n_tok=args.cpu_tokens, seed=args.seed)
+        run, flops, desc = oracle_sample(shape, inp, n_tok=args.cpu_tokens, seed=args.seed,
+                                         clamp=args.activation_clamp)
         reps, t0 = 0, time.perf_counter()
         while True:
             run()
@@ -447,7 +452,7 @@ def run_ours(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded Gaussian inputs and weights, Gaussian-logit top-k routing)",
-        "config": config_dict(shape, world),
+        "config": config_dict(shape, world, args.activation_clamp),
         "routed_tokens_per_s": tok_s,
         "pct_bf16_peak_burst": 100.0 * value / world / float(peaks["bf16_tflops"]),
         "pct_bf16_peak_sustained": 100.0 * value / world / float(peaks["bf16_tflops_sustained"]),
@@ -478,6 +483,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-router", action="store_true")
+    ap.add_argument("--activation-clamp", type=float, default=0.0,
+                    help="SwiGLU input clamp c > 0 (0: none, the default workload)")
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=2)

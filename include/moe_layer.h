@@ -45,9 +45,16 @@ extern "C" {
 
 /* Layer shape.  T tokens, hidden H, intermediate I, E experts, top-k k,
  * block_m = row alignment of each expert's group (DeepGEMM Mega-MoE article,
- * "Block-M Alignment for Irregular Token Counts"; only 128 is supported). */
+ * "Block-M Alignment for Irregular Token Counts"; only 128 is supported).
+ * activation_clamp: the SwiGLU activation clamp (the `activation_clamp`
+ * argument of the DeepGEMM Mega-MoE article's fused op, given there without
+ * a formula; read here as: with c > 0 both SwiGLU inputs, gate and up, are
+ * clamped to [-c, c] before silu(gate) * up, and their gradients pass where
+ * -c <= input <= c and are 0 outside).  0 (or any c <= 0) = no clamp; NaN
+ * or infinity is MOE_EINVAL. */
 typedef struct moe_shape {
     int32_t T, H, I, E, k, block_m;
+    float activation_clamp;
 } moe_shape;
 
 enum {
@@ -86,6 +93,11 @@ enum {
  *    h  bf16[rows_cap, 2I]     L1 output per padded row (gate | up); 0 on padding
  *    a  bf16[rows_cap, I]      SwiGLU output per padded row; 0 on padding
  *    o  bf16[rows_cap, H]      weighted L2 output per padded row
+ *    cmask u32[rows_cap, 2I/32] with an activation clamp: bit l of word
+ *                              (r, g) = 1 when input feature 32 g + l of
+ *                              SwiGLU (gate features first, then up) was
+ *                              inside [-c, c] in the forward (the FP32
+ *                              decision the backward reuses)
  *  bwd_ws (scratch of moe_backward):
  *    dh      bf16[rows_cap, 2I]          gradient at h; 0 on padding
  *    aw      bf16[rows_cap, I]           w * a per padded row; 0 on padding
@@ -96,7 +108,7 @@ enum {
 typedef struct moe_layout {
     int64_t rows_cap, tiles_cap;
     size_t route_bytes, counts, offs, perm, inv, tiles, status, pair_offs, pair_owner;
-    size_t saved_bytes, h, a, o;
+    size_t saved_bytes, h, a, o, cmask;
     size_t bwd_bytes, dh, aw, dxp, dw_part;
     int32_t dw_part_cols;
 } moe_layout;

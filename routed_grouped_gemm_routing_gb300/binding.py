@@ -27,14 +27,15 @@ BLOCK_M = 128
 
 
 class MoeShape(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "block_m")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "block_m")] + [
+        ("activation_clamp", ctypes.c_float)]
 
 
 class MoeLayout(ctypes.Structure):
     _fields_ = [("rows_cap", ctypes.c_int64), ("tiles_cap", ctypes.c_int64)] + [
         (n, ctypes.c_size_t)
         for n in ("route_bytes", "counts", "offs", "perm", "inv", "tiles", "status", "pair_offs", "pair_owner",
-                  "saved_bytes", "h", "a", "o", "bwd_bytes", "dh", "aw", "dxp", "dw_part")
+                  "saved_bytes", "h", "a", "o", "cmask", "bwd_bytes", "dh", "aw", "dxp", "dw_part")
     ] + [("dw_part_cols", ctypes.c_int32)]
 
 
@@ -89,8 +90,8 @@ def _check(rc: int):
         raise MoeError(rc, lib().moe_last_error().decode())
 
 
-def shape_of(T: int, H: int, I: int, E: int, k: int, block_m: int = BLOCK_M) -> MoeShape:
-    return MoeShape(T, H, I, E, k, block_m)
+def shape_of(T: int, H: int, I: int, E: int, k: int, block_m: int = BLOCK_M, activation_clamp: float = 0.0) -> MoeShape:
+    return MoeShape(T, H, I, E, k, block_m, activation_clamp)
 
 
 def moe_workspace_layout(shape: MoeShape) -> MoeLayout:

@@ -159,6 +159,13 @@ __device__ __forceinline__ void stage_col16_sw64(uint32_t box, int l, int j0, co
     }
 }
 
+// SwiGLU activation clamp (c = INFINITY: none): the input clamped to
+// [-c, c], and whether its gradient passes (-c <= z <= c).
+__device__ __forceinline__ float clamp_in(float z, float c) { return c < INFINITY ? fminf(fmaxf(z, -c), c) : z; }
+__device__ __forceinline__ float clamp_pass(float z, float c) {
+    return (c == INFINITY || (z >= -c && z <= c)) ? 1.0f : 0.0f;
+}
+
 __device__ __forceinline__ float ldg_bf16(const __nv_bfloat16* p) {
     const uint16_t u = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __uint_as_float((uint32_t)u << 16);
@@ -233,6 +240,41 @@ __device__ __forceinline__ void transpose_reduce_step(float (&v)[32], int lane) 
         const float send = upper ? v[i] : v[i + S];
         const float keep = upper ? v[i + S] : v[i];
         v[i] = keep + __shfl_xor_sync(0xffffffffu, send, S);
+    }
+}
+
+// SwiGLU^T of one 32-row chunk of the L2 dgrad epilogue, element (row j,
+// feature lane): from g = v[j], the saved h (gate, up) and a boxes in
+// shared memory and the routing weight w (lane j of wl), stage
+//   da = w g,  dgate = da * up * s(gate) * (1 + gate (1 - s(gate))),
+//   dup = da * silu(gate),  aw = w a
+// into the three output boxes.  kClamp: gate and up clamped to [-c, c] and
+// the gradients masked by the forward's decisions (bit lane of row j's
+// gmask / umask word, lane j holding row j's words).
+template <bool kClamp>
+__device__ __forceinline__ void swiglu_t_chunk(uint32_t stage, uint32_t in_box, bool colok, int lane, float wl,
+                                               const float (&v)[32], float c, uint32_t gmask, uint32_t umask) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float hg = 0.0f, hu = 0.0f, av = 0.0f;
+        if (colok) {
+            hg = lds_sw64(in_box, j, lane);
+            hu = lds_sw64(in_box + 2048, j, lane);
+            av = lds_sw64(in_box + 4096, j, lane);
+        }
+        const float wv = __shfl_sync(0xffffffffu, wl, j);
+        const float da = wv * v[j];
+        float gc = hg, uc = hu, pg = 1.0f, pu = 1.0f;
+        if constexpr (kClamp) {
+            gc = fminf(fmaxf(hg, -c), c);
+            uc = fminf(fmaxf(hu, -c), c);
+            pg = (float)((__shfl_sync(0xffffffffu, gmask, j) >> lane) & 1u);
+            pu = (float)((__shfl_sync(0xffffffffu, umask, j) >> lane) & 1u);
+        }
+        const float sg = 1.0f / (1.0f + __expf(-gc));
+        sts_sw64(stage, j, lane, da * uc * sg * (1.0f + gc * (1.0f - sg)) * pg);
+        sts_sw64(stage + 2048, j, lane, da * gc * sg * pu);
+        sts_sw64(stage + 4096, j, lane, wv * av);
     }
 }
 
@@ -525,8 +567,33 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();
                     stage_col_sw64(buf, lane, v);
+                    if (p.clamp == INFINITY) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = v[j] / (1.0f + __expf(-v[j])) * u[j];
+                        for (int j = 0; j < 32; ++j) v[j] = v[j] / (1.0f + __expf(-v[j])) * u[j];
+                    } else {
+                        if (col < I) {
+                        // record the FP32 clamp decisions for the backward:
+                        // one 32-feature word per row for gate, one for up
+                        uint32_t gw = 0, uw = 0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const uint32_t bg = __ballot_sync(0xffffffffu, clamp_pass(v[j], p.clamp) != 0.0f);
+                            const uint32_t bu = __ballot_sync(0xffffffffu, clamp_pass(u[j], p.clamp) != 0.0f);
+                            if (lane == j) {
+                                gw = bg;
+                                uw = bu;
+                            }
+                        }
+                        const size_t words = (size_t)(2 * I / 32);
+                        p.cmask[(size_t)(row0 + lane) * words + (size_t)(col / 32)] = gw;
+                        p.cmask[(size_t)(row0 + lane) * words + (size_t)((I + col) / 32)] = uw;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float g = clamp_in(v[j], p.clamp);
+                            v[j] = g / (1.0f + __expf(-g)) * clamp_in(u[j], p.clamp);
+                        }
+                    }
                     stage_col_sw64(buf + 2048, lane, v);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -566,21 +633,18 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                 }
                 if (lane == 0) bulk_wait_read<0>();
                 __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float hg = 0.0f, hu = 0.0f, av = 0.0f;
-                    if (colok) {
-                        hg = lds_sw64(in_box, j, lane);
-                        hu = lds_sw64(in_box + 2048, j, lane);
-                        av = lds_sw64(in_box + 4096, j, lane);
-                    }
-                    const float wv = __shfl_sync(0xffffffffu, wl, j);
-                    const float da = wv * v[j];
-                    const float sg = 1.0f / (1.0f + __expf(-hg));
-                    sts_sw64(stage, j, lane, da * hu * sg * (1.0f + hg * (1.0f - sg)));
-                    sts_sw64(stage + 2048, j, lane, da * hg * sg);
-                    sts_sw64(stage + 4096, j, lane, wv * av);
+                // the forward's clamp decisions of this warp's features: lane
+                // l loads the words of row row0 + l, row j's are shuffled out
+                uint32_t gmask = 0xffffffffu, umask = 0xffffffffu;
+                if (p.clamp < INFINITY && colok) {
+                    const size_t words = (size_t)(2 * I / 32);
+                    gmask = __ldg(p.cmask + (size_t)(row0 + lane) * words + (size_t)(col / 32));
+                    umask = __ldg(p.cmask + (size_t)(row0 + lane) * words + (size_t)((I + col) / 32));
                 }
+                if (p.clamp < INFINITY)
+                    swiglu_t_chunk<true>(stage, in_box, colok, lane, wl, v, p.clamp, gmask, umask);
+                else
+                    swiglu_t_chunk<false>(stage, in_box, colok, lane, wl, v, p.clamp, gmask, umask);
                 // the input boxes are consumed: bring in the next chunk's
                 fence_proxy_async_smem();
                 __syncwarp();

@@ -2,6 +2,7 @@
 // workspace layout, TMA descriptors and the launch sequence of the layer.
 // No allocation, no synchronisation (except moe_read_status), no host read
 // of device data.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -91,6 +92,7 @@ int check_shape(const moe_shape* s) {
     if (s->k < 1 || s->k > s->E) return fail(MOE_EINVAL, "k must be in [1, E]");
     if (s->H % 64 || s->I % 64) return fail(MOE_EUNSUPPORTED, "H and I must be multiples of 64");
     if (s->block_m != kBM) return fail(MOE_EUNSUPPORTED, "block_m must be 128");
+    if (!isfinite(s->activation_clamp)) return fail(MOE_EINVAL, "activation_clamp must be finite");
     if ((long long)s->T * s->k >= (1ll << 31)) return fail(MOE_EINVAL, "T*k must be < 2^31");
     const long long tk = (long long)s->T * s->k;
     const long long cap = tk + (long long)(tk < s->E ? tk : s->E) * (s->block_m - 1);
@@ -222,6 +224,7 @@ GemmArgs base_args(const moe_shape* s, const moe_layout& L, uint8_t* route) {
     a.E = s->E;
     a.k = s->k;
     a.tiles_cap = (int)L.tiles_cap;
+    a.clamp = s->activation_clamp > 0.0f ? s->activation_clamp : INFINITY;
     a.dw_cols = L.dw_part_cols;
     a.perm = reinterpret_cast<const int32_t*>(route + L.perm);
     a.offs = reinterpret_cast<const int32_t*>(route + L.offs);
@@ -265,6 +268,7 @@ int compute_layout(const moe_shape* s, moe_layout* L) {
     L->h = o; o = align_up(o + 2 * R * 2 * (size_t)s->I, A);
     L->a = o; o = align_up(o + 2 * R * (size_t)s->I, A);
     L->o = o; o = align_up(o + 2 * R * (size_t)s->H, A);
+    L->cmask = o; o = align_up(o + 4 * R * (size_t)(2 * s->I / 32), A);
     L->saved_bytes = o;
     L->dw_part_cols = (s->I + 31) / 32;  // one partial per 32 features of the L2 dgrad epilogue
     o = 0;
@@ -344,6 +348,7 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     auto* h = reinterpret_cast<__nv_bfloat16*>(sv + L.h);
     auto* a = reinterpret_cast<__nv_bfloat16*>(sv + L.a);
     auto* o = reinterpret_cast<__nv_bfloat16*>(sv + L.o);
+    auto* cmask = reinterpret_cast<uint32_t*>(sv + L.cmask);
     cudaStream_t st = (cudaStream_t)stream;
     // L1 grouped GEMM (gathered x) + SwiGLU -> h, a; units of 128 gate and
     // 128 up features x one row chunk of one expert
@@ -356,6 +361,7 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     g1.K = H;
     g1.n_tiles = cdiv(I, 2 * 64);
     g1.gsrc = static_cast<const __nv_bfloat16*>(x);
+    g1.cmask = cmask;
     int e = launch_gemm(L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
     if (e) return cuda_fail(e, "L1 grouped GEMM launch");
 
@@ -429,6 +435,7 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     g.topk_w = topk_w;
     g.h_in = h;
     g.a_in = a;
+    g.cmask = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(sv + L.cmask));
     g.outf = dwp;
     int e = launch_gemm(L2_DGRAD, g, m, (int)L.tiles_cap * g.n_tiles, st);
     if (e) return cuda_fail(e, "L2 dgrad launch");

@@ -45,6 +45,8 @@ struct GemmArgs {
     int m_tiles;    // output row tiles per expert (weight-gradient flavours)
     int tiles_cap;  // bound on routed-row tiles (row-grouped flavours)
     int dw_cols;    // columns of dw_part
+    float clamp;    // SwiGLU input clamp (INFINITY = none)
+    uint32_t* cmask;  // clamp decisions [rows_cap][2I/32] (written by L1, read by L2 dgrad)
     const int32_t* perm;
     const int32_t* offs;
     const int32_t* counts;

@@ -16,8 +16,8 @@ from . import binding as B
 class MoEWorkspace:
     """Caller-owned device buffers of one layer shape (reused across steps)."""
 
-    def __init__(self, T: int, H: int, I: int, E: int, k: int, device=None):
-        self.shape = B.shape_of(T, H, I, E, k)
+    def __init__(self, T: int, H: int, I: int, E: int, k: int, device=None, activation_clamp: float = 0.0):
+        self.shape = B.shape_of(T, H, I, E, k, activation_clamp=activation_clamp)
         self.layout = B.moe_workspace_layout(self.shape)
         dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         L = self.layout
@@ -43,10 +43,12 @@ def _dims(x, W1, W2, topk_idx):
 
 class MoEFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, x, W1, W2, topk_idx, topk_weights, ws=None):
+    def forward(ctx, x, W1, W2, topk_idx, topk_weights, ws=None, activation_clamp=0.0):
         T, H, I, E, k = _dims(x, W1, W2, topk_idx)
         if ws is None or (ws.shape.T, ws.shape.H, ws.shape.I, ws.shape.E, ws.shape.k) != (T, H, I, E, k):
-            ws = MoEWorkspace(T, H, I, E, k, device=x.device)
+            ws = MoEWorkspace(T, H, I, E, k, device=x.device, activation_clamp=activation_clamp)
+        elif ws.shape.activation_clamp != activation_clamp:
+            ws.shape.activation_clamp = activation_clamp
         idx = topk_idx if topk_idx.dtype == torch.int32 else topk_idx.to(torch.int32)
         idx = idx.contiguous()
         w = topk_weights.to(torch.float32).contiguous()
@@ -71,16 +73,18 @@ class MoEFunction(torch.autograd.Function):
         dw = torch.empty(s.T, s.k, dtype=torch.float32, device=dev)
         B.moe_backward(s, dy.to(torch.bfloat16).contiguous(), x, W1.contiguous(), W2.contiguous(), w, ws.route,
                        ws.saved, ws.bwd, dx, dW1, dW2, dw)
-        return dx, dW1, dW2, None, dw.to(ctx.w_dtype), None
+        return dx, dW1, dW2, None, dw.to(ctx.w_dtype), None, None
 
 
-def moe_layer(x, W1, W2, topk_idx, topk_weights, workspace: MoEWorkspace | None = None):
+def moe_layer(x, W1, W2, topk_idx, topk_weights, workspace: MoEWorkspace | None = None,
+              activation_clamp: float = 0.0):
     """y = sum_j topk_weights[:, j] * SwiGLU-MLP_{topk_idx[:, j]}(x), bf16.
 
     x bf16 [T,H]; W1 bf16 [E,H,2I] (gate | up); W2 bf16 [E,I,H];
     topk_idx int32/int64 [T,k] (-1 = dropped slot); topk_weights float [T,k].
-    Differentiable in x, W1, W2 and topk_weights."""
-    return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace)
+    Differentiable in x, W1, W2 and topk_weights.  activation_clamp > 0
+    clamps both SwiGLU inputs to [-c, c] (gradients pass inside only)."""
+    return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace, float(activation_clamp))
 
 
 def train_step_from_host(x_h, topk_idx_h, topk_w_h, dY_h, W1, W2, ws: MoEWorkspace, outs: dict):

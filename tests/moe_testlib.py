@@ -49,14 +49,14 @@ def oracle_route(inp, E):
     return oracle.route(inp["topk_idx"].cpu().numpy(), E, 128)
 
 
-def oracle_all(inp, E):
+def oracle_all(inp, E, clamp=0.0):
     """Oracle over the whole (small) problem."""
     x, W1, W2, dY = (bf16_bits(inp[n]) for n in ("x", "W1", "W2", "dY"))
     idx = inp["topk_idx"].cpu().numpy().astype(np.int32)
     w = inp["topk_w"].cpu().numpy().astype(np.float32)
-    y = oracle.forward(x, W1, W2, idx, w)
-    dx, dw = oracle.backward_tokens(x, W1, W2, idx, w, dY)
-    dW1, dW2 = oracle.backward_experts(x, W1, W2, idx, w, dY)
+    y = oracle.forward(x, W1, W2, idx, w, clamp=clamp)
+    dx, dw = oracle.backward_tokens(x, W1, W2, idx, w, dY, clamp=clamp)
+    dW1, dW2 = oracle.backward_experts(x, W1, W2, idx, w, dY, clamp=clamp)
     return dict(y=y, dx=dx, dtopk_w=dw, dW1=dW1, dW2=dW2)
 
 
@@ -99,8 +99,8 @@ def oracle_experts(inp, E, exps):
 class GpuRun:
     """Buffers of one layer shape plus one prologue + forward + backward."""
 
-    def __init__(self, T, H, I, E, k, device="cuda"):
-        self.shape = B.shape_of(T, H, I, E, k)
+    def __init__(self, T, H, I, E, k, device="cuda", activation_clamp=0.0):
+        self.shape = B.shape_of(T, H, I, E, k, activation_clamp=activation_clamp)
         self.L = B.moe_workspace_layout(self.shape)
         L = self.L
         self.route = torch.empty(max(L.route_bytes, 16), dtype=torch.uint8, device=device)

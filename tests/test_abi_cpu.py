@@ -39,7 +39,8 @@ def test_layout(lib, T, H, I, E, k):
     assert L.status >= L.tiles + 4 * L.tiles_cap and L.pair_offs >= L.status + 64
     assert L.pair_owner >= L.pair_offs + 4 * (E + 1) and L.route_bytes >= L.pair_owner + 4 * L.tiles_cap
     R = L.rows_cap
-    assert L.a >= L.h + 2 * R * 2 * I and L.o >= L.a + 2 * R * I and L.saved_bytes >= L.o + 2 * R * H
+    assert L.a >= L.h + 2 * R * 2 * I and L.o >= L.a + 2 * R * I and L.cmask >= L.o + 2 * R * H
+    assert L.saved_bytes >= L.cmask + 4 * R * (2 * I // 32)
     assert L.aw >= L.dh + 2 * R * 2 * I and L.dxp >= L.aw + 2 * R * I
     assert L.dw_part >= L.dxp + 2 * R * H and L.bwd_bytes >= L.dw_part + 4 * R * L.dw_part_cols
 
@@ -50,7 +51,9 @@ def test_layout(lib, T, H, I, E, k):
                                       ((64, 128, 64, 2000, 2, 128), B.MOE_EINVAL),
                                       ((-1, 128, 64, 8, 2, 128), B.MOE_EINVAL),
                                       ((64, 128, 64, 8, 2, 64), B.MOE_EUNSUPPORTED),
-                                      ((64, 0, 64, 8, 2, 128), B.MOE_EINVAL)])
+                                      ((64, 0, 64, 8, 2, 128), B.MOE_EINVAL),
+                                      ((64, 128, 64, 8, 2, 128, float("nan")), B.MOE_EINVAL),
+                                      ((64, 128, 64, 8, 2, 128, float("inf")), B.MOE_EINVAL)])
 def test_bad_shapes_rejected_on_host(lib, bad, code):
     s = B.MoeShape(*bad)
     out = B.MoeLayout()
