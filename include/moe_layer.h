@@ -89,6 +89,11 @@ enum {
  *                              tiles_e = (offs[e+1]-offs[e]) / block_m: the GEMMs
  *                              take an expert's M tiles two at a time
  *    pair_owner int32[tiles_cap] expert of tile pair q; -1 past pair_offs[E]
+ *    blk_counts int32[route_blocks*(E+1) (at least 1)] prologue scratch: the
+ *                              slots are cut into route_blocks blocks of whole
+ *                              1024-slot rounds; per block and expert the
+ *                              number of that expert's slots in earlier
+ *                              blocks, then one count of invalid ids per block
  *  saved (written by moe_forward, read by moe_backward):
  *    h  bf16[rows_cap, 2I]     L1 output per padded row (gate | up); 0 on padding
  *    a  bf16[rows_cap, I]      SwiGLU output per padded row; 0 on padding
@@ -107,10 +112,11 @@ enum {
  * Mpad for any routing, so no buffer depends on device data. */
 typedef struct moe_layout {
     int64_t rows_cap, tiles_cap;
-    size_t route_bytes, counts, offs, perm, inv, tiles, status, pair_offs, pair_owner;
+    size_t route_bytes, counts, offs, perm, inv, tiles, status, pair_offs, pair_owner, blk_counts;
     size_t saved_bytes, h, a, o, cmask;
     size_t bwd_bytes, dh, aw, dxp, dw_part;
     int32_t dw_part_cols;
+    int32_t route_blocks;
 } moe_layout;
 
 /* Sizes and offsets of the three workspaces for `shape`.  Host only; touches
@@ -121,7 +127,8 @@ int moe_workspace_layout(const moe_shape* shape, moe_layout* out);
  * dispatch prologue that builds routing tables; DeepGEMM Mega-MoE article,
  * "Block-M Alignment").  Reads topk_idx int32[T, k] (device), writes every
  * route_ws table and status word listed above.  route_ws must hold
- * route_bytes.  Bit-exact and deterministic; no host synchronisation. */
+ * route_bytes.  Bit-exact and deterministic; no host synchronisation; up to
+ * three kernels on `stream` (block counts, scan, placement). */
 int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* route_ws, void* stream);
 
 /* Router top-k gating fused in front of the routing prologue (the router
@@ -133,7 +140,7 @@ int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* ro
  * logits (when the largest selected logit is infinite, 1/n on the n selected
  * logits equal to it and 0 elsewhere).  Then builds every route_ws table
  * from that topk_idx exactly as moe_route_prologue does.  All device
- * buffers are the caller's and 16-byte aligned; two kernels on `stream`, no
+ * buffers are the caller's and 16-byte aligned; kernels on `stream` only, no
  * host synchronisation, capturable.  topk_idx and topk_w are overwritten.
  * Errors: MOE_EINVAL for a bad shape or a NULL pointer, MOE_EUNSUPPORTED for
  * a misaligned pointer, MOE_ECUDA for a launch error. */

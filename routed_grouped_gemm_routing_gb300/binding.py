@@ -35,8 +35,8 @@ class MoeLayout(ctypes.Structure):
     _fields_ = [("rows_cap", ctypes.c_int64), ("tiles_cap", ctypes.c_int64)] + [
         (n, ctypes.c_size_t)
         for n in ("route_bytes", "counts", "offs", "perm", "inv", "tiles", "status", "pair_offs", "pair_owner",
-                  "saved_bytes", "h", "a", "o", "cmask", "bwd_bytes", "dh", "aw", "dxp", "dw_part")
-    ] + [("dw_part_cols", ctypes.c_int32)]
+                  "blk_counts", "saved_bytes", "h", "a", "o", "cmask", "bwd_bytes", "dh", "aw", "dxp", "dw_part")
+    ] + [("dw_part_cols", ctypes.c_int32), ("route_blocks", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):

@@ -33,8 +33,6 @@ int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaS
 
 namespace {
 const char* const kGemmNames[] = {"gemm_l1_fwd", "gemm_l2_fwd", "gemm_l2_dgrad", "gemm_l1_dgrad", "gemm_dw1", "gemm_dw2"};
-void trace_pre(cudaStream_t st);
-void trace_post(cudaStream_t st, const char* name);
 }  // namespace
 
 int launch_gemm(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
@@ -59,6 +57,8 @@ struct Trace {
 };
 thread_local Trace g_trace;
 
+}  // namespace
+
 void trace_pre(cudaStream_t st) {
     Trace& t = g_trace;
     if (t.events && 2 * t.n + 1 < t.capacity) cudaEventRecord((cudaEvent_t)t.events[2 * t.n], st);
@@ -70,6 +70,8 @@ void trace_post(cudaStream_t st, const char* name) {
     if (t.n < kTraceNames) t.names[t.n] = name;
     ++t.n;
 }
+
+namespace {
 
 int fail(int code, const std::string& msg) {
     g_err = msg;
@@ -263,6 +265,11 @@ int compute_layout(const moe_shape* s, moe_layout* L) {
     L->status = o; o = align_up(o + 4 * (size_t)MOE_STATUS_WORDS, A);
     L->pair_offs = o; o = align_up(o + 4 * (size_t)(s->E + 1), A);
     L->pair_owner = o; o = align_up(o + 4 * (size_t)L->tiles_cap, A);
+    int nblk = 0;
+    long long per_blk = 0;
+    route_block_split(tk, &nblk, &per_blk);
+    L->route_blocks = nblk;
+    L->blk_counts = o; o = align_up(o + 4 * ((size_t)nblk * (size_t)(s->E + 1) + 1), A);
     L->route_bytes = o;
     o = 0;
     L->h = o; o = align_up(o + 2 * R * 2 * (size_t)s->I, A);
@@ -300,9 +307,7 @@ int moe_route_prologue(const moe_shape* shape, const int32_t* topk_idx, void* ro
     if (!route_ws || (shape->T > 0 && !topk_idx)) return fail(MOE_EINVAL, "NULL pointer argument");
     if (!aligned16(route_ws) || !aligned16(topk_idx)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
     if ((rc = query_device(&c, route_ws))) return rc;
-    trace_pre((cudaStream_t)stream);
     int e = launch_route_prologue(*shape, c.L, topk_idx, static_cast<uint8_t*>(route_ws), (cudaStream_t)stream);
-    trace_post((cudaStream_t)stream, "route_prologue");
     if (e) return cuda_fail(e, "route prologue launch");
     return MOE_OK;
 }
@@ -322,9 +327,7 @@ int moe_router_topk(const moe_shape* shape, const float* logits, int32_t* topk_i
     int e = launch_router_topk(logits, shape->T, shape->E, shape->k, topk_idx, topk_w, c.sms, st);
     trace_post(st, "router_topk");
     if (e) return cuda_fail(e, "router top-k launch");
-    trace_pre(st);
     e = launch_route_prologue(*shape, c.L, topk_idx, static_cast<uint8_t*>(route_ws), st);
-    trace_post(st, "route_prologue");
     if (e) return cuda_fail(e, "route prologue launch");
     return MOE_OK;
 }

@@ -71,6 +71,16 @@ struct GemmMaps {
 // Layout of the three workspaces (host only).
 int compute_layout(const moe_shape* s, moe_layout* L);
 
+// The routing prologue cuts the T*k slots into at most kMaxRouteBlocks blocks
+// of whole 1024-slot rounds: nblk blocks of per_blk slots (the last one
+// shorter); nblk = 0 when there are no slots.
+constexpr int kMaxRouteBlocks = 1024;
+void route_block_split(long long tk, int* nblk, long long* per_blk);
+
+// Kernel tracing hook (moe_trace_begin): events around every launch.
+void trace_pre(cudaStream_t st);
+void trace_post(cudaStream_t st, const char* name);
+
 // Kernel launchers (return a cudaError_t as int).
 int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t* topk_idx, uint8_t* route,
                           cudaStream_t st);

@@ -4,29 +4,36 @@
 // "No-Sync, CUDA Graph compatible"; DeepGEMM Mega-MoE article, "Block-M
 // Alignment for Irregular Token Counts").
 //
-// One CTA of 1024 threads:
-//   1. per-expert histogram (shared-memory integer atomics: order-free, exact)
-//      and a count of ids that are neither -1 nor in [0, E);
-//   2. block-M padded sizes, exclusive prefix sum over experts with a
-//      warp-shuffle scan -> offs, Mpad, tile-owner table;
-//   3. stable placement: slots are visited in chunks of 1024 in increasing
-//      slot order; inside a chunk a slot's row is
-//        offs[e] + (slots of e in earlier chunks) + (slots of e in earlier
-//        warps of this chunk) + (lower lanes of its warp with the same e),
-//      the last term from __match_any_sync, so every expert's rows hold its
-//      slots in increasing slot order, bit-exactly reproducible.
-// Two scheduling tables for the grouped GEMMs ride along: the M tiles of an
-// expert are taken two at a time by a 2-CTA cluster, so pair_offs is the
-// exclusive prefix sum of ceil(tiles_e / 2) and pair_owner[q] the expert of
-// tile pair q (-1 past the last pair).
+// Three kernels on the caller's stream, so that the work spreads over the
+// whole GPU instead of one SM:
+//   1. route_hist (one CTA per slot block, blocks of whole 1024-slot rounds
+//      in increasing slot order): per-expert counts of the block, and for
+//      every valid slot its rank among the block's earlier slots of the same
+//      expert (warp ranks from __match_any_sync, then earlier warps of the
+//      round, then earlier rounds), kept in inv[] until step 3; ids that are
+//      neither -1 nor in [0, E) are counted per block.  Also sets every
+//      perm entry to -1 (padding).
+//   2. route_scan (one CTA): per expert, the exclusive prefix over blocks of
+//      the block counts (in place) and the total count; block-M padded sizes
+//      and their exclusive prefix sum (warp-shuffle scan) -> offs, Mpad, the
+//      tile-owner table, the status words, and the two scheduling tables of
+//      the SM-pair GEMMs: pair_offs = exclusive prefix sum of
+//      ceil(tiles_e / 2), pair_owner[q] = expert of tile pair q (-1 past the
+//      last pair).
+//   3. route_place (grid over slots): row = offs[e] + (slots of e in earlier
+//      blocks) + (rank inside the block); perm[row] = s, inv[s] = row, and
+//      inv[s] = -1 for a dropped slot.
+// An expert's rows therefore hold its slots in increasing slot order: the
+// tables are bit-exact and reproducible, and need no atomics on global
+// memory (the block counts are plain per-block integer sums).
 #include "moe_internal.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int kPrologueThreads = 1024;
-constexpr int kWarps = kPrologueThreads / 32;
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
@@ -37,44 +44,96 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
     return v;
 }
 
-__global__ void __launch_bounds__(kPrologueThreads, 1)
-    route_prologue_kernel(int T, int E, int k, int bm, const int32_t* __restrict__ idx, int32_t* __restrict__ counts,
-                          int32_t* __restrict__ offs, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                          int32_t* __restrict__ tiles, int32_t* __restrict__ status,
-                          int32_t* __restrict__ pair_offs, int32_t* __restrict__ pair_owner, long long rows_cap,
-                          long long tiles_cap) {
+// 1. block counts and in-block ranks
+__global__ void __launch_bounds__(kThreads, 1)
+    route_hist_kernel(long long tk, int E, long long per_blk, const int32_t* __restrict__ idx,
+                      int32_t* __restrict__ inv, int32_t* __restrict__ bcnt, int32_t* __restrict__ bbad,
+                      int32_t* __restrict__ perm, long long rows_cap) {
     extern __shared__ int sm[];
-    int* cnt = sm;                // [E]
-    int* base = sm + E;           // [E]
-    int* wcnt = sm + 2 * E;       // [kWarps][E]
+    int* run = sm;       // [E] slots of expert e in this block's earlier rounds
+    int* wcnt = sm + E;  // [kWarps][E] slots of e per warp in the current round
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += kThreads) run[e] = 0;
+    for (int q = tid; q < kWarps * E; q += kThreads) wcnt[q] = 0;
+    if (tid == 0) s_bad = 0;
+    for (long long r = (long long)blockIdx.x * kThreads + tid; r < rows_cap; r += (long long)gridDim.x * kThreads)
+        perm[r] = -1;
+    __syncthreads();
+
+    const long long s0 = (long long)blockIdx.x * per_blk;
+    const long long s1 = s0 + per_blk < tk ? s0 + per_blk : tk;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int bad = 0;
+    for (long long c0 = s0; c0 < s1; c0 += kThreads) {
+        const long long s = c0 + tid;
+        const int e = s < s1 ? __ldg(idx + s) : -1;
+        const bool valid = e >= 0 && e < E;
+        if (s < s1 && !valid && e != -1) ++bad;
+        const int key = valid ? e : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int rank = __popc(peers & lt_mask);
+        if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
+        __syncthreads();
+        if (valid) {
+            int pre = run[e];
+            for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
+            inv[s] = pre + rank;
+        }
+        __syncthreads();
+        for (int q = tid; q < E; q += kThreads) {
+            int tot = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                tot += wcnt[w * E + q];
+                wcnt[w * E + q] = 0;
+            }
+            run[q] += tot;
+        }
+        __syncthreads();
+    }
+    for (int d = 16; d > 0; d >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, d);
+    if (lane == 0 && bad) atomicAdd(&s_bad, bad);
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) bcnt[(size_t)blockIdx.x * E + e] = run[e];
+    if (tid == 0) bbad[blockIdx.x] = s_bad;
+}
+
+// 2. totals, padded offsets, tile and pair tables, status words (one CTA)
+__global__ void __launch_bounds__(kThreads, 1)
+    route_scan_kernel(int E, int nblk, int bm, int32_t* __restrict__ bcnt, const int32_t* __restrict__ bbad,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offs, int32_t* __restrict__ tiles,
+                      int32_t* __restrict__ status, int32_t* __restrict__ pair_offs,
+                      int32_t* __restrict__ pair_owner, long long tiles_cap) {
+    extern __shared__ int sm[];
+    int* cnt = sm;       // [E]
+    int* base = sm + E;  // [E]
     __shared__ int warp_tot[kWarps];
     __shared__ int warp_tot2[kWarps];
     __shared__ int s_invalid;
     __shared__ int s_mpad;
     __shared__ int s_pairs;
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long tk = (long long)T * k;
 
-    for (int e = tid; e < E; e += kPrologueThreads) cnt[e] = 0;
-    for (int q = tid; q < kWarps * E; q += kPrologueThreads) wcnt[q] = 0;
+    // per expert: exclusive prefix over blocks (in place) and the total
+    for (int e = tid; e < E; e += kThreads) {
+        int acc = 0;
+        for (int b = 0; b < nblk; ++b) {
+            const int v = bcnt[(size_t)b * E + e];
+            bcnt[(size_t)b * E + e] = acc;
+            acc += v;
+        }
+        cnt[e] = acc;
+    }
+    int bad = 0;
+    for (int b = tid; b < nblk; b += kThreads) bad += bbad[b];
+    for (int d = 16; d > 0; d >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, d);
     if (tid == 0) s_invalid = 0;
     __syncthreads();
-
-    // 1. histogram
-    int bad = 0;
-    for (long long s = tid; s < tk; s += kPrologueThreads) {
-        const int e = __ldg(idx + s);
-        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-        else if (e != -1) ++bad;
-    }
-    for (int d = 16; d > 0; d >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, d);
     if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
-    __syncthreads();
 
-    // 2. padded exclusive scan over experts; each thread owns a contiguous run
+    // padded exclusive scan over experts; each thread owns a contiguous run
     // (and the same scan of the per-expert tile-pair counts)
-    const int per = (E + kPrologueThreads - 1) / kPrologueThreads;
+    const int per = (E + kThreads - 1) / kThreads;
     const int e0 = tid * per;
     int run = 0, run2 = 0;
     for (int q = 0; q < per; ++q) {
@@ -114,7 +173,7 @@ __global__ void __launch_bounds__(kPrologueThreads, 1)
             acc2 += (t + 1) / 2;
         }
     }
-    if (tid == kPrologueThreads - 1) {
+    if (tid == kThreads - 1) {
         s_mpad = warp_tot[kWarps - 1];
         s_pairs = warp_tot2[kWarps - 1];
         offs[E] = s_mpad;
@@ -126,75 +185,98 @@ __global__ void __launch_bounds__(kPrologueThreads, 1)
         status[MOE_STATUS_NUM_PAIRS] = s_pairs;
         for (int q = MOE_STATUS_NUM_PAIRS + 1; q < MOE_STATUS_WORDS; ++q) status[q] = 0;
     }
-    for (long long r = tid; r < rows_cap; r += kPrologueThreads) perm[r] = -1;
     __syncthreads();
 
     // tile owners (and no owner past the last tile pair)
     const int mpad = s_mpad;
-    for (long long m = (long long)mpad / bm + tid; m < tiles_cap; m += kPrologueThreads) tiles[m] = -1;
-    for (long long q = (long long)s_pairs + tid; q < tiles_cap; q += kPrologueThreads) pair_owner[q] = -1;
-    for (int e = tid; e < E; e += kPrologueThreads) {
+    for (long long m = (long long)mpad / bm + tid; m < tiles_cap; m += kThreads) tiles[m] = -1;
+    for (long long q = (long long)s_pairs + tid; q < tiles_cap; q += kThreads) pair_owner[q] = -1;
+    for (int e = tid; e < E; e += kThreads) {
         const int m_end = (base[e] + ((cnt[e] + bm - 1) / bm) * bm) / bm;
         for (int m = base[e] / bm; m < m_end; ++m) tiles[m] = e;
     }
+}
 
-    // 3. stable placement, 1024 slots per round
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (long long c0 = 0; c0 < tk; c0 += kPrologueThreads) {
-        const long long s = c0 + tid;
-        const int e = s < tk ? __ldg(idx + s) : -1;
-        const bool valid = e >= 0 && e < E;
-        const int key = valid ? e : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        const int rank = __popc(peers & lt_mask);
-        if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
-        __syncthreads();
-        if (valid) {
-            int pre = 0;
-            for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
-            const int row = base[e] + pre + rank;
+// 3. placement
+__global__ void __launch_bounds__(256)
+    route_place_kernel(long long tk, int E, long long per_blk, const int32_t* __restrict__ idx,
+                       const int32_t* __restrict__ offs, const int32_t* __restrict__ bcnt,
+                       int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    for (long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x; s < tk;
+         s += (long long)gridDim.x * blockDim.x) {
+        const int e = __ldg(idx + s);
+        if (e >= 0 && e < E) {
+            const int row = __ldg(offs + e) + bcnt[(size_t)(s / per_blk) * E + e] + inv[s];
             perm[row] = (int32_t)s;
             inv[s] = row;
-        } else if (s < tk) {
+        } else {
             inv[s] = -1;
         }
-        __syncthreads();
-        for (int q = tid; q < E; q += kPrologueThreads) {
-            int tot = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                tot += wcnt[w * E + q];
-                wcnt[w * E + q] = 0;
-            }
-            base[q] += tot;
-        }
-        __syncthreads();
     }
 }
 
-}  // namespace
-
-int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t* topk_idx, uint8_t* route,
-                          cudaStream_t st) {
-    const size_t smem = sizeof(int) * (size_t)(2 + kWarps) * (size_t)s.E;
-    // opt in once per device to the largest size any E <= 1024 needs
-    static bool done[kMaxDevices] = {};
+int set_smem_once(const void* fn, int bytes, bool* done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
     if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(route_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(int) * (2 + kWarps) * 1024));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return (int)e;
         done[dev] = true;
     }
-    route_prologue_kernel<<<1, kPrologueThreads, smem, st>>>(
-        s.T, s.E, s.k, s.block_m, topk_idx, reinterpret_cast<int32_t*>(route + L.counts),
-        reinterpret_cast<int32_t*>(route + L.offs), reinterpret_cast<int32_t*>(route + L.perm),
-        reinterpret_cast<int32_t*>(route + L.inv), reinterpret_cast<int32_t*>(route + L.tiles),
+    return 0;
+}
+
+}  // namespace
+
+void route_block_split(long long tk, int* nblk, long long* per_blk) {
+    const long long rounds = (tk + kThreads - 1) / kThreads;
+    long long rpb = (rounds + kMaxRouteBlocks - 1) / kMaxRouteBlocks;
+    if (rpb < 1) rpb = 1;
+    *per_blk = rpb * kThreads;
+    *nblk = (int)((tk + *per_blk - 1) / *per_blk);
+}
+
+int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t* topk_idx, uint8_t* route,
+                          cudaStream_t st) {
+    // opt in once per device to the largest size any E <= 1024 needs
+    static bool done_hist[kMaxDevices] = {};
+    int e = set_smem_once((const void*)route_hist_kernel, (int)(sizeof(int) * (1 + kWarps) * 1024), done_hist);
+    if (e) return e;
+    const long long tk = (long long)s.T * s.k;
+    int nblk = 0;
+    long long per_blk = 0;
+    route_block_split(tk, &nblk, &per_blk);
+    auto* counts = reinterpret_cast<int32_t*>(route + L.counts);
+    auto* offs = reinterpret_cast<int32_t*>(route + L.offs);
+    auto* perm = reinterpret_cast<int32_t*>(route + L.perm);
+    auto* inv = reinterpret_cast<int32_t*>(route + L.inv);
+    auto* bcnt = reinterpret_cast<int32_t*>(route + L.blk_counts);
+    int32_t* bbad = bcnt + (size_t)nblk * s.E;
+    if (nblk > 0) {
+        trace_pre(st);
+        route_hist_kernel<<<nblk, kThreads, sizeof(int) * (size_t)(1 + kWarps) * s.E, st>>>(
+            tk, s.E, per_blk, topk_idx, inv, bcnt, bbad, perm, (long long)L.rows_cap);
+        trace_post(st, "route_hist");
+        if ((e = (int)cudaGetLastError())) return e;
+    }
+    trace_pre(st);
+    route_scan_kernel<<<1, kThreads, sizeof(int) * 2 * (size_t)s.E, st>>>(
+        s.E, nblk, s.block_m, bcnt, bbad, counts, offs, reinterpret_cast<int32_t*>(route + L.tiles),
         reinterpret_cast<int32_t*>(route + L.status), reinterpret_cast<int32_t*>(route + L.pair_offs),
-        reinterpret_cast<int32_t*>(route + L.pair_owner), (long long)L.rows_cap, (long long)L.tiles_cap);
-    return (int)cudaGetLastError();
+        reinterpret_cast<int32_t*>(route + L.pair_owner), (long long)L.tiles_cap);
+    trace_post(st, "route_scan");
+    if ((e = (int)cudaGetLastError())) return e;
+    if (tk > 0) {
+        long long blocks = (tk + 255) / 256;
+        if (blocks > 16384) blocks = 16384;
+        trace_pre(st);
+        route_place_kernel<<<(unsigned)blocks, 256, 0, st>>>(tk, s.E, per_blk, topk_idx, offs, bcnt, perm, inv);
+        trace_post(st, "route_place");
+        if ((e = (int)cudaGetLastError())) return e;
+    }
+    return 0;
 }
 
 }  // namespace moe

@@ -26,7 +26,8 @@ def test_exports_every_declared_function(lib):
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(64, 128, 64, 8, 2), (4096, 2048, 1408, 64, 6), (8192, 7168, 2048, 256, 8),
-                                       (4096, 7168, 3072, 384, 6), (1, 64, 64, 1024, 3), (0, 64, 64, 4, 2)])
+                                       (4096, 7168, 3072, 384, 6), (1, 64, 64, 1024, 3), (0, 64, 64, 4, 2),
+                                       (300000, 64, 64, 16, 8)])
 def test_layout(lib, T, H, I, E, k):
     L = B.moe_workspace_layout(B.shape_of(T, H, I, E, k))
     assert L.rows_cap == oracle.rows_cap(T, E, k, 128)
@@ -37,7 +38,14 @@ def test_layout(lib, T, H, I, E, k):
     assert L.offs >= L.counts + 4 * E and L.perm >= L.offs + 4 * (E + 1)
     assert L.inv >= L.perm + 4 * L.rows_cap and L.tiles >= L.inv + 4 * T * k
     assert L.status >= L.tiles + 4 * L.tiles_cap and L.pair_offs >= L.status + 64
-    assert L.pair_owner >= L.pair_offs + 4 * (E + 1) and L.route_bytes >= L.pair_owner + 4 * L.tiles_cap
+    assert L.pair_owner >= L.pair_offs + 4 * (E + 1) and L.blk_counts >= L.pair_owner + 4 * L.tiles_cap
+    assert L.blk_counts % 256 == 0
+    # slot blocks of whole 1024-slot rounds, at most 1024 of them
+    tk = T * k
+    rounds = -(-tk // 1024)
+    per = max(1, -(-rounds // 1024)) * 1024
+    assert L.route_blocks == -(-tk // per) and L.route_blocks <= 1024
+    assert L.route_bytes >= L.blk_counts + 4 * (L.route_blocks * (E + 1) + 1)
     R = L.rows_cap
     assert L.a >= L.h + 2 * R * 2 * I and L.o >= L.a + 2 * R * I and L.cmask >= L.o + 2 * R * H
     assert L.saved_bytes >= L.cmask + 4 * R * (2 * I // 32)
