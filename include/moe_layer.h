@@ -71,6 +71,10 @@ enum {
     MOE_STATUS_N_INVALID = 2, /* slots whose id was neither -1 nor in [0, E) */
     MOE_STATUS_FLAGS = 3,     /* bit 0: a kernel gave up on a bounded wait */
     MOE_STATUS_NUM_PAIRS = 4, /* pair_offs[E]: tile pairs the GEMM clusters walk */
+    MOE_STATUS_SCHED = 8,     /* words 8..15: work counters of the row-grouped GEMMs,
+                                 zeroed by the prologue and back at zero after every
+                                 GEMM launch; so calls that use one route_ws must
+                                 not run concurrently */
     MOE_STATUS_WORDS = 16
 };
 

@@ -17,13 +17,15 @@
 // cut into nsub = ceil(count / 256) chunks of equal size (rounded up to 32);
 // the routing prologue's pair tables hold nsub per expert (pair_offs) and the
 // owner of every chunk (pair_owner).  Units are numbered expert by expert,
-// then feature tile, then chunk, so the chunks that stream the same weight
-// tile run at the same time on neighbouring clusters.
+// then feature tile, then chunk, and handed to the clusters at run time
+// (unit feed below), so the chunks that stream the same weight tile run at
+// the same time on different clusters and share it in L2.
 //
-// Roles (per CTA, 14 warps): 0-3 epilogue (TMEM lanes = this CTA's 128
+// Roles (per CTA, 15 warps): 0-3 epilogue (TMEM lanes = this CTA's 128
 // features, columns = rows), 4 TMA producer (weights; non-gathered
 // activations), 5 MMA issuer on the even CTA / relay on the odd CTA, 6-13
-// gather producers (x or dY rows picked by the permutation table).
+// gather producers (x or dY rows picked by the permutation table), 14 unit
+// scheduler (even CTA).
 //   * Producers of both CTAs fill their own stage and arrive on their own
 //     full[s]; the odd CTA's relay thread forwards that to the even CTA's
 //     peer_full[s].
@@ -44,8 +46,13 @@ constexpr int kT2Stages = 6;              // barrier slots (the L2 dgrad kernel 
 constexpr int kT2ABytes = 128 * kBK * 2;  // this CTA's 128 features x 64 of K
 constexpr int kT2BBytes = 128 * kBK * 2;  // up to 128 routed rows x 64 of K
 constexpr int kT2InBytes = 3 * 2048;      // L2 dgrad epilogue inputs per warp: h gate, h up, a boxes
-constexpr int kT2NumBars = 3 * kT2Stages + 9 + kEpiWarps;
-static_assert(8 * kT2NumBars + 8 <= 256, "barrier area");
+constexpr int kUR = 4;                    // slots of the unit ring
+constexpr int kT2NumBars = 3 * kT2Stages + 9 + kEpiWarps + 2 * kUR + 1;
+constexpr int kT2TailBytes = 512;         // barriers, TMEM address, abort flag, unit ring
+constexpr int kT2RingOff = (8 * kT2NumBars + 8 + 15) & ~15;
+static_assert(kT2RingOff + 16 * kUR <= kT2TailBytes, "barrier area");
+constexpr int kWarpSched = kWarpGather0 + kGatherWarps;  // unit scheduler (even CTA, lane 0)
+constexpr int kT2Threads = kGemmThreads + 32;
 
 struct T2Bars {
     uint32_t base;
@@ -60,6 +67,13 @@ struct T2Bars {
     __device__ __forceinline__ uint32_t xempty(int i) const { return base + 8u * (3 * kT2Stages + 7 + i); }
     // L2 dgrad epilogue: the saved h and a boxes of epilogue warp w have landed
     __device__ __forceinline__ uint32_t ein(int w) const { return base + 8u * (3 * kT2Stages + 9 + w); }
+    // unit ring: slot i published (both CTAs) / read by every consumer of
+    // both CTAs (even CTA's barrier); the even CTA's TMA producer took a unit
+    __device__ __forceinline__ uint32_t ufull(int i) const { return base + 8u * (3 * kT2Stages + 9 + kEpiWarps + i); }
+    __device__ __forceinline__ uint32_t uempty(int i) const {
+        return base + 8u * (3 * kT2Stages + 9 + kEpiWarps + kUR + i);
+    }
+    __device__ __forceinline__ uint32_t ustart() const { return base + 8u * (3 * kT2Stages + 9 + kEpiWarps + 2 * kUR); }
 };
 
 // ------------------------------------------------------- cluster helpers
@@ -70,6 +84,22 @@ __device__ __forceinline__ uint32_t cluster_addr_of(uint32_t local, uint32_t ran
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Arrival that makes this thread's earlier shared::cluster stores visible to
+// whoever observes the phase with acquire.cluster.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int4 v) {
+    asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ int4 ld_shared_v4s(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -205,7 +235,8 @@ struct T2<L1_DGRAD> {
 
 template <int F>
 constexpr int t2_smem_bytes() {
-    return 1024 + T2<F>::kStages * (kT2ABytes + kT2BBytes) + kEpiWarps * kStageEpiBytes + T2<F>::kInBytes + 256;
+    return 1024 + T2<F>::kStages * (kT2ABytes + kT2BBytes) + kEpiWarps * kStageEpiBytes + T2<F>::kInBytes +
+           kT2TailBytes;
 }
 static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448, "shared memory per CTA");
 
@@ -286,46 +317,72 @@ struct T2Unit {
     int n;       // rows of the unit rounded up to 32: the MMA's N
     int nvalid;  // routed rows of the unit
 };
-struct T2Raw {
-    int e, po, pn, off, cnt;
-};
+// ------------------------------------------------------------ unit feed
+// Units are handed out at run time, so that the clusters that stream the
+// same weight tile (the row chunks of one expert and feature tile, numbered
+// next to each other) start them at nearly the same moment and share the
+// tile in L2; a static stride lets the clusters drift apart over a launch.
+// Cluster c starts with unit c; the even CTA's scheduler thread claims each
+// further unit from a global counter (ncl + atomicAdd) as soon as the even
+// CTA's TMA producer has started the cluster's previous unit, decodes it from
+// the routing tables and publishes it in a kUR-slot ring in the shared
+// memory of both CTAs (ufull[i]); every consumer of both CTAs reads the slot
+// and arrives on the even CTA's uempty[i].  An expert of -1 ends the walk.
+// Slot: {expert, feature tile, first row, n << 16 | routed rows}.
+__device__ __forceinline__ int4 t2_decode(const GemmArgs& p, int u) {
+    const int e = __ldg(p.pair_owner + u / p.n_tiles);
+    const int po = __ldg(p.pair_offs + e);
+    const int nsub = __ldg(p.pair_offs + e + 1) - po;
+    const int off = __ldg(p.offs + e);
+    const int cnt = __ldg(p.counts + e);
+    const int l = u - po * p.n_tiles;
+    const int ft = l / nsub;
+    const int j = l - ft * nsub;
+    const int nb = (((cnt + nsub - 1) / nsub) + 31) & ~31;
+    const int rs = j * nb;
+    const int nvalid = min(nb, cnt - rs);
+    const int n = (nvalid + 31) & ~31;
+    return make_int4(e, ft, off + rs, (n << 16) | nvalid);
+}
 
 template <int F>
-struct T2Walk {
-    const GemmArgs& p;
-    int total, unit, step, rank;
-    T2Raw raw;
-    __device__ __forceinline__ T2Walk(const GemmArgs& p_, int total_, int rank_)
-        : p(p_), total(total_), unit((int)blockIdx.x >> 1), step((int)gridDim.x >> 1), rank(rank_) {
-        if (unit < total) load(unit);
-    }
-    __device__ __forceinline__ void load(int u) {
-        raw.e = __ldg(p.pair_owner + u / p.n_tiles);
-        raw.po = __ldg(p.pair_offs + raw.e);
-        raw.pn = __ldg(p.pair_offs + raw.e + 1);
-        raw.off = __ldg(p.offs + raw.e);
-        raw.cnt = __ldg(p.counts + raw.e);
-    }
-    __device__ __forceinline__ bool valid() const { return unit < total; }
-    __device__ __forceinline__ T2Unit take() {
-        T2Unit t;
-        const int nsub = raw.pn - raw.po;
-        const int l = unit - raw.po * p.n_tiles;
-        const int ft = l / nsub;
-        const int j = l - ft * nsub;
-        const int nb = (((raw.cnt + nsub - 1) / nsub) + 31) & ~31;
-        const int rs = j * nb;
-        t.e = raw.e;
-        t.nvalid = min(nb, raw.cnt - rs);
-        t.n = (t.nvalid + 31) & ~31;
-        t.r0 = raw.off + rs;
-        t.fcol = 2 * ft + rank;
+struct T2Feed {
+    uint32_t ring;  // this CTA's ring slots
+    T2Bars bars;
+    int rank;
+    int n;  // units taken so far
+    __device__ __forceinline__ T2Feed(uint32_t ring_, T2Bars bars_, int rank_)
+        : ring(ring_), bars(bars_), rank(rank_), n(0) {}
+    // Takes the next unit into t; false at the end of the walk or on abort.
+    // kWarp: every lane of the warp calls (warp-collective wait), otherwise
+    // one thread.  start: the even CTA's TMA producer, whose take lets the
+    // scheduler claim the cluster's next unit.
+    template <bool kWarp>
+    __device__ __forceinline__ bool next(T2Unit& t, volatile int* abort, int lane, bool start = false) {
+        const int i = n % kUR;
+        const uint32_t ph = (uint32_t)(n / kUR) & 1u;
+        bool ok = rank == 0 ? mbar_wait(bars.ufull(i), ph, abort) : mbar_wait_cl(bars.ufull(i), ph, abort);
+        if constexpr (kWarp) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        const int4 v = ld_shared_v4s(ring + 16u * (uint32_t)i);
+        if constexpr (kWarp) __syncwarp();
+        if (!kWarp || lane == 0) {
+            if (rank == 0)
+                mbar_arrive(bars.uempty(i));
+            else
+                mbar_arrive_release_cluster(cluster_addr_of(bars.uempty(i), 0));
+            if (start) mbar_arrive(bars.ustart());
+        }
+        ++n;
+        if (v.x < 0) return false;
+        t.e = v.x;
+        t.fcol = 2 * v.y + rank;
         t.f0 = t.fcol * T2<F>::kFeatPerCta;
-        const int nxt = unit + step;
-        if (nxt < total) load(nxt);
-        return t;
+        t.r0 = v.z;
+        t.n = v.w >> 16;
+        t.nvalid = v.w & 0xffff;
+        return true;
     }
-    __device__ __forceinline__ void next() { unit += step; }
 };
 
 __device__ __forceinline__ int t2_total_units(const GemmArgs& p) {
@@ -334,15 +391,48 @@ __device__ __forceinline__ int t2_total_units(const GemmArgs& p) {
     return np * p.n_tiles;
 }
 
+// The even CTA's unit scheduler (one thread).  The work counter and the
+// count of clusters done are status words of route_ws (zeroed by the routing
+// prologue); the last cluster to finish puts both back to zero for the next
+// launch on the same tables.
+template <int F>
+__device__ void t2_role_sched(const GemmArgs& p, uint32_t ring, T2Bars bars, volatile int* abort) {
+    const int total = t2_total_units(p);
+    const int ncl = (int)gridDim.x >> 1;
+    int* ctr = reinterpret_cast<int*>(p.status + MOE_STATUS_SCHED + 2 * F);
+    int* fin = ctr + 1;
+    const uint32_t ring1 = cluster_addr_of(ring, 1);
+    int u = (int)blockIdx.x >> 1;
+    for (int n = 0;; ++n) {
+        if (n > 0) {
+            if (!mbar_wait(bars.ustart(), (uint32_t)(n - 1) & 1u, abort)) break;
+            u = ncl + atomicAdd(ctr, 1);
+        }
+        const int4 v = u < total ? t2_decode(p, u) : make_int4(-1, 0, 0, 0);
+        const int i = n % kUR;
+        if (!mbar_wait_cl(bars.uempty(i), ((uint32_t)(n / kUR) & 1u) ^ 1u, abort)) break;
+        st_shared_v4(ring + 16u * (uint32_t)i, (uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w);
+        st_cluster_v4(ring1 + 16u * (uint32_t)i, v);
+        mbar_arrive(bars.ufull(i));
+        mbar_arrive_release_cluster(cluster_addr_of(bars.ufull(i), 1));
+        if (v.x < 0) break;
+    }
+    __threadfence();
+    if (atomicAdd(fin, 1) == ncl - 1) {
+        atomicExch(ctr, 0);
+        atomicExch(fin, 0);
+    }
+}
+
 // ------------------------------------------------------------ TMA producer
 template <int F>
-__device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, int total, uint32_t sA,
-                            uint32_t sB, T2Bars bars, volatile int* abort, int rank) {
+__device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, uint32_t ring,
+                            uint32_t sA, uint32_t sB, T2Bars bars, volatile int* abort, int rank) {
     const int nkb = p.K / kBK;
     int stage = 0;
     uint32_t phase = 0;
-    for (T2Walk<F> w(p, total, rank); w.valid(); w.next()) {
-        const T2Unit t = w.take();
+    T2Feed<F> feed(ring, bars, rank);
+    for (T2Unit t; feed.template next<false>(t, abort, 0, rank == 0);) {
         const int nh = t.n >> 1;           // this CTA's rows of the unit
         const int nbox = (nh + 31) >> 5;   // 32-row boxes of a non-gathered B
         const int rb = t.r0 + nh * rank;
@@ -381,8 +471,8 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
 // 128-byte-swizzled K-major layout; rows past the unit's half are left alone
 // (the MMA reads only n / 2 rows).  Padding rows (perm = -1) are zero-filled.
 template <int F>
-__device__ void t2_role_gather(const GemmArgs& p, int total, uint32_t sB, T2Bars bars, volatile int* abort, int gw,
-                               int lane, int rank) {
+__device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, T2Bars bars, volatile int* abort,
+                               int gw, int lane, int rank) {
     const int c = lane & 7;
     const int rb = lane >> 3;
     const int H = p.H;
@@ -391,8 +481,8 @@ __device__ void t2_role_gather(const GemmArgs& p, int total, uint32_t sB, T2Bars
     const __nv_bfloat16* src = p.gsrc;
     int stage = 0;
     uint32_t phase = 0;
-    for (T2Walk<F> w(p, total, rank); w.valid(); w.next()) {
-        const T2Unit t = w.take();
+    T2Feed<F> feed(ring, bars, rank);
+    for (T2Unit t; feed.template next<true>(t, abort, lane);) {
         const int nh = t.n >> 1;
         const int rbase = t.r0 + nh * rank;
         int tok[4];
@@ -426,14 +516,14 @@ __device__ void t2_role_gather(const GemmArgs& p, int total, uint32_t sB, T2Bars
 
 // -------------------------------------------- MMA issuer (even CTA) / relay
 template <int F>
-__device__ void t2_role_mma(const GemmArgs& p, int total, uint32_t sA, uint32_t sB, T2Bars bars, uint32_t tmem_base,
-                            volatile int* abort) {
+__device__ void t2_role_mma(const GemmArgs& p, uint32_t ring, uint32_t sA, uint32_t sB, T2Bars bars,
+                            uint32_t tmem_base, volatile int* abort) {
     const int nkb = p.K / kBK;
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
-    for (T2Walk<F> w(p, total, 0); w.valid(); w.next(), ++it) {
-        const T2Unit t = w.take();
+    T2Feed<F> feed(ring, bars, 0);
+    for (T2Unit t; feed.template next<false>(t, abort, 0); ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_cl(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
@@ -467,12 +557,12 @@ __device__ void t2_role_mma(const GemmArgs& p, int total, uint32_t sA, uint32_t 
 // The odd CTA's MMA thread: tells the even CTA that this CTA's half of a
 // stage is in shared memory.
 template <int F>
-__device__ void t2_role_relay(const GemmArgs& p, int total, T2Bars bars, volatile int* abort) {
+__device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, volatile int* abort) {
     const int nkb = p.K / kBK;
     int stage = 0;
     uint32_t phase = 0;
-    for (T2Walk<F> w(p, total, 1); w.valid(); w.next()) {
-        (void)w.take();
+    T2Feed<F> feed(ring, bars, 1);
+    for (T2Unit t; feed.template next<false>(t, abort, 0);) {
         for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(bars.full(stage), phase, abort)) return;
             if constexpr (T2<F>::kGather) fence_proxy_async_smem();
@@ -494,15 +584,15 @@ __device__ void t2_role_relay(const GemmArgs& p, int total, T2Bars bars, volatil
 // mapA), the first one while the accumulator is still being computed.
 template <int F>
 __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMap* mapH, const CUtensorMap* mapAs,
-                                 int total, T2Bars bars, uint32_t tmem_base, uint32_t stage, uint32_t stage_of_warp0,
+                                 uint32_t ring, T2Bars bars, uint32_t tmem_base, uint32_t stage, uint32_t stage_of_warp0,
                                  uint32_t in_box, volatile int* abort, int warp, int lane, int rank) {
     const uint32_t tempty_leader[2] = {cluster_addr_of(bars.tempty(0), 0), cluster_addr_of(bars.tempty(1), 0)};
     int it = 0;
     uint32_t nstore = 0;
     uint32_t xchunk = 0;  // L1: chunks handed over between warp i and warp 2 + i
     uint32_t nin = 0;     // L2 dgrad: input boxes waited for
-    for (T2Walk<F> w(p, total, rank); w.valid(); w.next(), ++it) {
-        const T2Unit t = w.take();
+    T2Feed<F> feed(ring, bars, rank);
+    for (T2Unit t; feed.template next<true>(t, abort, lane); ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if constexpr (F == L2_DGRAD) {
@@ -693,7 +783,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
 }
 
 template <int F>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kT2Threads, 1)
     moe_gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                          const __grid_constant__ CUtensorMap mapC0, const __grid_constant__ CUtensorMap mapC1,
                          const __grid_constant__ CUtensorMap mapD, const GemmArgs p) {
@@ -706,6 +796,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t sStage = sB + T2<F>::kStages * kT2BBytes;
     const uint32_t sIn = sStage + kEpiWarps * kStageEpiBytes;  // L2 dgrad epilogue inputs
     const uint32_t bar_base = sIn + T2<F>::kInBytes;
+    const uint32_t ring = bar_base + kT2RingOff;
     uint8_t* tail = base_ptr + (bar_base - base);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * kT2NumBars);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -729,6 +820,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(bars.drain(), 1);
         for (int w = 0; w < kEpiWarps; ++w) mbar_init(bars.ein(w), 1);
+        // consumers of a published unit: TMA, MMA or relay, epilogue warps
+        // and (gathering flavours) gather warps, in both CTAs
+        const uint32_t consumers = 2u * (2u + kEpiWarps + (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u));
+        for (int i = 0; i < kUR; ++i) {
+            mbar_init(bars.ufull(i), 1);
+            mbar_init(bars.uempty(i), consumers);
+        }
+        mbar_init(bars.ustart(), 1);
         *abort = 0;
         fence_mbar_init();
     }
@@ -747,17 +846,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = t2_total_units(p);
 
     if (warp == kWarpTma) {
-        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, total, sA, sB, bars, abort, rank);
+        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, bars, abort, rank);
+    } else if (warp == kWarpSched) {
+        if (lane == 0 && rank == 0) t2_role_sched<F>(p, ring, bars, abort);
     } else if (warp >= kWarpGather0) {
-        if constexpr (T2<F>::kGather) t2_role_gather<F>(p, total, sB, bars, abort, warp - kWarpGather0, lane, rank);
+        if constexpr (T2<F>::kGather) t2_role_gather<F>(p, ring, sB, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             if (rank == 0) {
-                t2_role_mma<F>(p, total, sA, sB, bars, tmem_base, abort);
+                t2_role_mma<F>(p, ring, sA, sB, bars, tmem_base, abort);
                 if (*abort) {
                     // let every MMA already issued finish before TMEM is released
                     tc_commit_pair_local(bars.drain());
@@ -766,11 +866,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             } else {
-                t2_role_relay<F>(p, total, bars, abort);
+                t2_role_relay<F>(p, ring, bars, abort);
             }
         }
     } else {
-        t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, total, bars, tmem_base,
+        t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, ring, bars, tmem_base,
                             sStage + warp * kStageEpiBytes, sStage, sIn + warp * kT2InBytes, abort, warp, lane, rank);
     }
     if (warp == kWarpTma && lane == 0 && *abort) {
@@ -790,7 +890,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // Launches one 2-CTA cluster per unit up to the number of clusters that fit
-// on the device at once (persistent: each cluster walks units c, c + grid/2..).
+// on the device at once (persistent: each cluster takes units from the unit
+// feed until none is left).
 template <int F>
 int launch_gemm_pair(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
     static int clusters_fit[kMaxDevices] = {};
@@ -804,7 +905,7 @@ int launch_gemm_pair(const GemmArgs& a, const GemmMaps& m, int max_units, cudaSt
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.blockDim = dim3(kT2Threads, 1, 1);
     cfg.dynamicSmemBytes = t2_smem_bytes<F>();
     cfg.stream = st;
     cfg.attrs = attr;
