@@ -1,14 +1,17 @@
-// Instantiations of the grouped GEMM engine: DW1 and DW2.
-#include "grouped_gemm.cuh"
+// Instantiations of the weight-gradient GEMMs (SM-pair kernels with the
+// gathered operand resident in shared memory): DW1 and DW2.
+#include "wgrad_pair.cuh"
 
 namespace moe {
 
-int launch_gemm_dw1(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
-    return launch_gemm_flavour<DW1>(a, m, grid, st);
+// m.b = dh (box 64 x 64), m.c0 = dW1 [E][H][2I] (box 64 x 32)
+int launch_gemm_dw1(const GemmArgs& a, const GemmMaps& m, int, cudaStream_t st) {
+    return launch_wgrad_pair<DW1>(a, m.b, m.c0, st);
 }
 
-int launch_gemm_dw2(const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
-    return launch_gemm_flavour<DW2>(a, m, grid, st);
+// m.a = aw (box 64 x 64), m.c0 = dW2 [E][I][H] (box 64 x 32)
+int launch_gemm_dw2(const GemmArgs& a, const GemmMaps& m, int, cudaStream_t st) {
+    return launch_wgrad_pair<DW2>(a, m.a, m.c0, st);
 }
 
 }  // namespace moe

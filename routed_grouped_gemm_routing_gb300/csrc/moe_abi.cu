@@ -238,11 +238,6 @@ GemmArgs base_args(const moe_shape* s, const moe_layout& L, uint8_t* route) {
     return a;
 }
 
-int grid_for(int sms, long long tiles) {
-    if (tiles <= 0) return 0;
-    return (int)(tiles < sms ? tiles : sms);
-}
-
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 }  // namespace
@@ -448,11 +443,13 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     memset(&m3, 0, sizeof m3);
     if ((rc = map_2d(&m3.a, aw, L.rows_cap, I, 64, 64, "aw"))) return rc;
     if ((rc = map_3d(&m3.c0, dW2, E, I, H, 64, 32, "dW2 (store)"))) return rc;
+    // units: (expert, 256 features of H); each streams the expert's aw in
+    // tiles of 256 features of I
     GemmArgs g3 = base_args(shape, L, route);
-    g3.m_tiles = cdiv(I, kBM);
-    g3.n_tiles = cdiv(H, kBN);
+    g3.m_tiles = cdiv(H, 256);
+    g3.n_tiles = cdiv(I, 256);
     g3.gsrc = static_cast<const __nv_bfloat16*>(dY);
-    e = launch_gemm(DW2, g3, m3, grid_for(c.sms, (long long)E * g3.m_tiles * g3.n_tiles), st);
+    e = launch_gemm(DW2, g3, m3, E * g3.m_tiles, st);
     if (e) return cuda_fail(e, "dW2 launch");
 
     // dW1[e] = x_e^T . dh_e (variable K, x re-gathered)
@@ -460,11 +457,13 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     memset(&m4, 0, sizeof m4);
     if ((rc = map_2d(&m4.b, dh, L.rows_cap, 2 * I, 64, 64, "dh (rows)"))) return rc;
     if ((rc = map_3d(&m4.c0, dW1, E, H, 2 * I, 64, 32, "dW1 (store)"))) return rc;
+    // units: (expert, 256 features of H); each streams the expert's dh in
+    // tiles of 256 features of 2I
     GemmArgs g4 = base_args(shape, L, route);
-    g4.m_tiles = cdiv(H, kBM);
-    g4.n_tiles = cdiv(2 * I, kBN);
+    g4.m_tiles = cdiv(H, 256);
+    g4.n_tiles = cdiv(2 * I, 256);
     g4.gsrc = static_cast<const __nv_bfloat16*>(x);
-    e = launch_gemm(DW1, g4, m4, grid_for(c.sms, (long long)E * g4.m_tiles * g4.n_tiles), st);
+    e = launch_gemm(DW1, g4, m4, E * g4.m_tiles, st);
     if (e) return cuda_fail(e, "dW1 launch");
 
     // L1 dgrad: dxp = dh . W1[e]^T; units of 256 features of H

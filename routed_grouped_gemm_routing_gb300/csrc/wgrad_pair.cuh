@@ -1,0 +1,502 @@
+// Weight gradients of the routed MoE layer on SM pairs (tcgen05 cta_group::2)
+// with the gathered token operand kept in shared memory:
+//   dW1[e] = gather(x)_e^T . dh_e        dW2[e] = aw_e^T . gather(dY)_e
+// (Primus-Turbo "Mega MoE" README, "Pipeline": the backward's variable-K
+// weight-gradient GEMMs, K = the expert's routed rows; the dispatched x is
+// recomputed by gathering it again, section "Recompute dispatched x in
+// backward").
+//
+// A work unit is (expert e, stationary tile s): 256 features of H, 128 in
+// each CTA of a 2-CTA cluster.  Each CTA gathers its 128 features of the
+// token operand (x for dW1, dY for dW2) for all of the expert's routed rows
+// ONCE into a shared-memory slab (up to kWSlabKb 64-row K blocks), and then
+// streams the other operand (dh for dW1, aw for dW2) by TMA, 128 of its
+// features per CTA at a time, through a kWStages ring.  For every streamed
+// tile t the pair issues M=256 x N=256 MMAs over the expert's rows:
+//   dW1: A = slab (M = H features), B = dh (N = 2I features)
+//   dW2: A = aw   (M = I features), B = slab (N = H features)
+// so each CTA's TMEM holds 128 output rows x 256 output columns of dW[e]
+// and leaves through the same TMA-store epilogue as the one-SM tiles.
+// The token operand is gathered once per unit instead of once per output
+// tile (16x fewer gathered bytes for dW1, 8x for dW2), and each SM streams
+// 16 KiB per K block instead of 48 KiB.
+//
+// Experts with more rows than the slab holds run K in chunks of kWSlabKb
+// blocks, the slab gathered again for every (tile, chunk).  An expert
+// without routed rows gets zeros.
+//
+// Roles (per CTA, 14 warps): 0-3 epilogue, 4 TMA producer (streamed
+// operand), 5 MMA issuer on the even CTA / relay on the odd CTA (forwards
+// "this CTA's half has landed" for slab blocks and stages), 6-13 gather
+// producers (slab).  Every wait is bounded, as in the other GEMM kernels.
+#pragma once
+
+#include "grouped_gemm_2sm.cuh"
+
+namespace moe {
+
+constexpr int kWSlabKb = 5;                  // slab capacity in 64-row K blocks (320 routed rows)
+constexpr int kWStages = 6;                  // streamed-operand ring
+constexpr int kWBlockBytes = 128 * kBK * 2;  // 16 KiB: 128 features x 64 rows, MN-major, 128B swizzle
+constexpr int kWNumBars = 3 * kWSlabKb + 3 * kWStages + 5;
+constexpr int kWTailBytes = 512;
+static_assert(8 * kWNumBars + 8 <= kWTailBytes, "barrier area");
+constexpr int kWSmemBytes = 1024 + (kWSlabKb + kWStages) * kWBlockBytes + kEpiWarps * kStageEpiBytes + kWTailBytes;
+static_assert(kWSmemBytes <= 232448, "shared memory per CTA");
+
+struct WBars {
+    uint32_t base;
+    __device__ __forceinline__ uint32_t slab_full(int i) const { return base + 8u * i; }
+    __device__ __forceinline__ uint32_t peer_slab_full(int i) const { return base + 8u * (kWSlabKb + i); }
+    __device__ __forceinline__ uint32_t slab_empty(int i) const { return base + 8u * (2 * kWSlabKb + i); }
+    __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * (3 * kWSlabKb + s); }
+    __device__ __forceinline__ uint32_t peer_full(int s) const { return base + 8u * (3 * kWSlabKb + kWStages + s); }
+    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (3 * kWSlabKb + 2 * kWStages + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kWSlabKb + 3 * kWStages + a); }
+    __device__ __forceinline__ uint32_t tempty(int a) const {
+        return base + 8u * (3 * kWSlabKb + 3 * kWStages + 2 + a);
+    }
+    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kWSlabKb + 3 * kWStages + 4); }
+};
+
+// Shape of one unit.  S = stationary tiles per expert (over H), T = streamed
+// tiles (over 2I for dW1, over I for dW2).
+struct WUnit {
+    int e, s;
+    int off;  // first routed row of the expert
+    int cnt;  // routed rows of the expert
+    int nkb;  // 64-row K blocks
+    int nch;  // K chunks of at most kWSlabKb blocks
+};
+
+// Static walk over units cluster, cluster + clusters, ...; the expert's
+// count and offset for the next unit are read while the current one runs.
+struct WWalk {
+    const GemmArgs& p;
+    int total, unit, step;
+    int cnt, off;
+    __device__ __forceinline__ WWalk(const GemmArgs& p_)
+        : p(p_), total(p_.E * p_.m_tiles), unit((int)blockIdx.x >> 1), step((int)gridDim.x >> 1) {
+        if (unit < total) load(unit);
+    }
+    __device__ __forceinline__ void load(int u) {
+        const int e = u / p.m_tiles;
+        cnt = __ldg(p.counts + e);
+        off = __ldg(p.offs + e);
+    }
+    __device__ __forceinline__ bool valid() const { return unit < total; }
+    __device__ __forceinline__ WUnit take() {
+        WUnit w;
+        w.e = unit / p.m_tiles;
+        w.s = unit - w.e * p.m_tiles;
+        w.cnt = cnt;
+        w.off = off;
+        w.nkb = (cnt + kBK - 1) / kBK;
+        w.nch = (w.nkb + kWSlabKb - 1) / kWSlabKb;
+        const int nxt = unit + step;
+        if (nxt < total) load(nxt);
+        return w;
+    }
+    __device__ __forceinline__ void next() { unit += step; }
+};
+
+// K blocks [kb0, kb1) of chunk c.
+__device__ __forceinline__ int w_kb0(int c) { return c * kWSlabKb; }
+__device__ __forceinline__ int w_kb1(const WUnit& u, int c) { return min(u.nkb, (c + 1) * kWSlabKb); }
+
+// ------------------------------------------------------------ TMA producer
+// Streamed operand: 128 features (this CTA's half of the tile's 256) x 64 rows
+// per K block, two 64 x 64 boxes.
+template <int F>
+__device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS, WBars bars, volatile int* abort,
+                           int rank) {
+    int stage = 0;
+    uint32_t phase = 0;
+    const int T = p.n_tiles;
+    for (WWalk w(p); w.valid(); w.next()) {
+        const WUnit u = w.take();
+        for (int t = 0; t < T; ++t) {
+            const int f0 = t * 256 + 128 * rank;
+            for (int kb = 0; kb < u.nkb; ++kb) {
+                if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                const uint32_t fb = bars.full(stage);
+                mbar_arrive_expect_tx(fb, (uint32_t)kWBlockBytes);
+                const uint32_t dst = sS + stage * kWBlockBytes;
+                tma_load_2d(dst, mS, f0, u.off + kb * kBK, fb);
+                tma_load_2d(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb);
+                if (++stage == kWStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------- gather producer
+// The slab: this CTA's 128 features of the token operand over the rows of K
+// blocks [kb0, kb1), block kb in slot kb - kb0; 16-byte cp.async chunks into
+// the 128-byte-swizzled MN-major layout (row r of a 64-feature region at
+// r*128, chunk c at (c ^ (r & 7)) * 16); padding rows (perm = -1) and
+// features past H are zero-filled.
+__device__ __forceinline__ void w_gather_round(const GemmArgs& p, const WUnit& u, int kb0, int kb1, uint32_t sL,
+                                               WBars bars, uint32_t& sphase, volatile int* abort, int gw, int lane,
+                                               int rank, bool& ok) {
+    constexpr int kRowsPerWarp = kBK / kGatherWarps;  // 8
+    const int c = lane & 7;
+    const int rb = lane >> 3;
+    const int H = p.H, k = p.k;
+    const int rw0 = gw * kRowsPerWarp;
+    const int col0 = u.s * 256 + 128 * rank;
+    // permutation entries of this warp's rows in every block of the round
+    int ent[kWSlabKb];
+#pragma unroll
+    for (int i = 0; i < kWSlabKb; ++i)
+        ent[i] = (kb0 + i < kb1) ? __ldg(p.perm + u.off + (kb0 + i) * kBK + rw0 + (lane & (kRowsPerWarp - 1))) : -1;
+#pragma unroll
+    for (int i = 0; i < kWSlabKb; ++i) {
+        if (kb0 + i >= kb1) break;
+        if (!warp_wait(bars.slab_empty(i), ((sphase >> i) & 1u) ^ 1u, abort)) {
+            ok = false;
+            return;
+        }
+        const int tcur = ent[i] >= 0 ? ent[i] / k : -1;
+        const int tq0 = __shfl_sync(0xffffffffu, tcur, rb);
+        const int tq1 = __shfl_sync(0xffffffffu, tcur, rb + 4);
+        const uint32_t dst0 = sL + i * kWBlockBytes;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int colg = col0 + 64 * g + 8 * c;
+            const bool okc = colg < H;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int tq = q ? tq1 : tq0;
+                const int r = rw0 + rb + 4 * q;
+                const bool v = okc && tq >= 0;
+                const __nv_bfloat16* gp = p.gsrc + (v ? (size_t)tq * (size_t)H + colg : (size_t)0);
+                cp_async_16(dst0 + g * 8192 + r * 128 + ((c ^ (r & 7)) << 4), gp, v ? 16u : 0u);
+            }
+        }
+        cp_async_arrive_noinc(bars.slab_full(i));
+        sphase ^= 1u << i;
+    }
+}
+
+__device__ void w_role_gather(const GemmArgs& p, uint32_t sL, WBars bars, volatile int* abort, int gw, int lane,
+                              int rank) {
+    uint32_t sphase = 0;
+    bool ok = true;
+    const int T = p.n_tiles;
+    for (WWalk w(p); w.valid() && ok; w.next()) {
+        const WUnit u = w.take();
+        if (u.nch == 1) {
+            w_gather_round(p, u, 0, u.nkb, sL, bars, sphase, abort, gw, lane, rank, ok);
+        } else {
+            for (int t = 0; t < T && ok; ++t)
+                for (int c = 0; c < u.nch && ok; ++c)
+                    w_gather_round(p, u, w_kb0(c), w_kb1(u, c), sL, bars, sphase, abort, gw, lane, rank, ok);
+        }
+    }
+}
+
+// -------------------------------------------------------------- MMA issuer
+template <int F>
+__device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars bars, uint32_t tmem_base,
+                           volatile int* abort) {
+    constexpr uint32_t idesc = make_idesc_bf16(2 * kBM, 256, true, true);
+    int stage = 0;
+    uint32_t phase = 0, sphase = 0;
+    int it = 0;
+    const int T = p.n_tiles;
+    for (WWalk w(p); w.valid(); w.next()) {
+        const WUnit u = w.take();
+        for (int t = 0; t < T; ++t, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait_cl(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(acc * 256);
+            for (int c = 0; c < u.nch; ++c) {
+                const int kb0 = w_kb0(c), kb1 = w_kb1(u, c);
+                // the slab blocks of this round are waited for on their first
+                // use and released after their last one
+                const bool first = u.nch > 1 || t == 0;
+                const bool last = u.nch > 1 || t == T - 1;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    const int i = kb - kb0;
+                    if (first) {
+                        if (!mbar_wait(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
+                        if (!mbar_wait_cl(bars.peer_slab_full(i), (sphase >> i) & 1u, abort)) return;
+                    }
+                    if (!mbar_wait(bars.full(stage), phase, abort)) return;
+                    if (!mbar_wait_cl(bars.peer_full(stage), phase, abort)) return;
+                    tc_fence_after();
+                    fence_proxy_async_smem();  // the slab was written by cp.async
+                    const uint32_t sl = sL + i * kWBlockBytes;
+                    const uint32_t st = sS + stage * kWBlockBytes;
+                    const uint32_t a = (F == DW1) ? sl : st;
+                    const uint32_t b = (F == DW1) ? st : sl;
+                    // stop at the 16-row step that holds the expert's last row
+                    const int ksteps = min(kBK / 16, (u.cnt - kb * kBK + 15) / 16);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        if (kk >= ksteps) break;
+                        const uint64_t ad = make_sdesc_sw128(a + kk * 2048, 8192, 1024);
+                        const uint64_t bd = make_sdesc_sw128(b + kk * 2048, 8192, 1024);
+                        tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair(bars.empty(stage));
+                    if (last) {
+                        tc_commit_pair(bars.slab_empty(i));
+                        sphase ^= 1u << i;
+                    }
+                    if (++stage == kWStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            tc_commit_pair(bars.tfull(acc));
+        }
+    }
+}
+
+// The odd CTA's MMA thread: tells the even CTA that this CTA's half of a
+// slab block or of a stage is in shared memory, in the order the MMA uses them.
+__device__ void w_role_relay(const GemmArgs& p, WBars bars, volatile int* abort) {
+    int stage = 0;
+    uint32_t phase = 0, sphase = 0;
+    const int T = p.n_tiles;
+    for (WWalk w(p); w.valid(); w.next()) {
+        const WUnit u = w.take();
+        for (int t = 0; t < T; ++t) {
+            for (int c = 0; c < u.nch; ++c) {
+                const int kb0 = w_kb0(c), kb1 = w_kb1(u, c);
+                const bool first = u.nch > 1 || t == 0;
+                const bool last = u.nch > 1 || t == T - 1;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    const int i = kb - kb0;
+                    if (first) {
+                        if (!mbar_wait(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
+                        fence_proxy_async_smem();
+                        mbar_arrive_cluster(cluster_addr_of(bars.peer_slab_full(i), 0));
+                    }
+                    if (last) sphase ^= 1u << i;
+                    if (!mbar_wait(bars.full(stage), phase, abort)) return;
+                    mbar_arrive_cluster(cluster_addr_of(bars.peer_full(stage), 0));
+                    if (++stage == kWStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- epilogue
+// Warp w drains TMEM lanes 32w..32w+31 (32 output rows) x 256 columns as four
+// 32 x 64 boxes in the 128-byte swizzle, each leaving by TMA store.
+template <int F>
+__device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars bars, uint32_t tmem_base,
+                                uint32_t stage, volatile int* abort, int warp, int lane, int rank) {
+    const uint32_t tempty_leader[2] = {cluster_addr_of(bars.tempty(0), 0), cluster_addr_of(bars.tempty(1), 0)};
+    const int T = p.n_tiles;
+    // dW1 is [E][H][2I], dW2 is [E][I][H]
+    const int rows_out = (F == DW1) ? p.H : p.I;
+    const int cols_out = (F == DW1) ? 2 * p.I : p.H;
+    int it = 0;
+    uint32_t nstore = 0;
+    for (WWalk w(p); w.valid(); w.next()) {
+        const WUnit u = w.take();
+        for (int t = 0; t < T; ++t, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            if (!warp_wait(bars.tfull(acc), acc_phase, abort)) {
+                if (lane == 0) bulk_wait_all();
+                return;
+            }
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(warp * 32) << 16);
+            const int row0 = ((F == DW1) ? u.s : t) * 256 + 128 * rank + 32 * warp;
+            const int colb = ((F == DW1) ? t : u.s) * 256;
+            const bool have_acc = u.nkb > 0;
+#pragma unroll 1
+            for (int c64 = 0; c64 < 4; ++c64) {
+                const int col = colb + 64 * c64;
+                if (row0 >= rows_out || col >= cols_out) break;
+                uint32_t pk[32];
+                {
+                    uint32_t r0[32], r1[32];
+                    if (have_acc) {
+                        tmem_ld32_nowait(tacc + 64 * c64, r0);
+                        tmem_ld32_nowait(tacc + 64 * c64 + 32, r1);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        pk[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+                        pk[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+                    }
+                }
+                const uint32_t buf = stage + (nstore & 1u) * 4096u;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                stage_row_sw128(buf, lane, pk);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(mC, col, row0, u.e, buf);
+                    bulk_commit();
+                }
+                ++nstore;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+        }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+// mapS: the streamed operand (dh for dW1, aw for dW2), box 64 x 64;
+// mapC: the weight gradient [E][rows][cols], box 64 x 32.
+template <int F>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_wgrad_pair_kernel(const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapC,
+                          const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t sL = base;                               // slab: kWSlabKb blocks
+    const uint32_t sS = sL + kWSlabKb * kWBlockBytes;       // streamed ring: kWStages blocks
+    const uint32_t sE = sS + kWStages * kWBlockBytes;       // epilogue staging
+    const uint32_t bar_base = sE + kEpiWarps * kStageEpiBytes;
+    uint8_t* tail = base_ptr + (bar_base - base);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * kWNumBars);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const WBars bars{bar_base};
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank();
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWSlabKb; ++i) {
+            mbar_init(bars.slab_full(i), 32u * kGatherWarps);
+            mbar_init(bars.peer_slab_full(i), 1);
+            mbar_init(bars.slab_empty(i), 1);
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.peer_full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bars.tfull(a), 1);
+            mbar_init(bars.tempty(a), 2 * kEpiWarps);
+        }
+        mbar_init(bars.drain(), 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc_pair(smem_addr(tmem_slot), 512);
+        tmem_relinquish_pair();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        tma_prefetch_map(&mapS);
+        tma_prefetch_map(&mapC);
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == kWarpTma) {
+        if (lane == 0) w_role_tma<F>(&mapS, p, sS, bars, abort, rank);
+    } else if (warp >= kWarpGather0) {
+        w_role_gather(p, sL, bars, abort, warp - kWarpGather0, lane, rank);
+        cp_async_wait_all();
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            if (rank == 0) {
+                w_role_mma<F>(p, sL, sS, bars, tmem_base, abort);
+                if (*abort) {
+                    tc_commit_pair_local(bars.drain());
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
+                    }
+                }
+            } else {
+                w_role_relay(p, bars, abort);
+            }
+        }
+    } else {
+        w_role_epilogue<F>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
+    }
+    if (warp == kWarpTma && lane == 0 && *abort) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 2000000ull) {
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
+    }
+    if (threadIdx.x == 0 && *abort) atomicOr(reinterpret_cast<int*>(p.status + MOE_STATUS_FLAGS), 1);
+}
+
+// One 2-CTA cluster per unit up to the clusters that fit at once
+// (persistent, static unit stride).  a.m_tiles = stationary tiles per expert
+// (ceil(H / 256)), a.n_tiles = streamed tiles (ceil(2I / 256) for dW1,
+// ceil(I / 256) for dW2).
+template <int F>
+int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensorMap& mapC, cudaStream_t st) {
+    static int clusters_fit[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return (int)e;
+    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (clusters_fit[dev] == 0) {
+        // set once per device, outside any stream capture (on the first call)
+        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
+        if (e != cudaSuccess) return (int)e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return (int)e;
+        cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, moe_wgrad_pair_kernel<F>, &cfg);
+        if (e != cudaSuccess) return (int)e;
+        if (n < 1) return (int)cudaErrorInvalidConfiguration;
+        clusters_fit[dev] = n;
+    }
+    const long long units = (long long)a.E * a.m_tiles;
+    if (units <= 0) return 0;
+    const int clusters = units < clusters_fit[dev] ? (int)units : clusters_fit[dev];
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, moe_wgrad_pair_kernel<F>, mapS, mapC, a);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaGetLastError();
+}
+
+}  // namespace moe
