@@ -27,8 +27,12 @@
 //
 // Roles (per CTA, 14 warps): 0-3 epilogue, 4 TMA producer (streamed
 // operand), 5 MMA issuer on the even CTA / relay on the odd CTA (forwards
-// "this CTA's half has landed" for slab blocks and stages), 6-13 gather
-// producers (slab).  Every wait is bounded, as in the other GEMM kernels.
+// "this CTA's half of a slab block has landed"), 6-13 gather producers
+// (slab).  Both CTAs' TMA loads of a stage complete one barrier in the even
+// CTA, so the MMA thread waits once per stage: issuing a tcgen05.mma costs
+// the thread about two thirds of the MMA's own pipe time, so every extra
+// wait in its loop would leave the tensor pipe idle.  Every wait is
+// bounded, as in the other GEMM kernels.
 #pragma once
 
 #include "grouped_gemm_2sm.cuh"
@@ -38,7 +42,7 @@ namespace moe {
 constexpr int kWSlabKb = 5;                  // slab capacity in 64-row K blocks (320 routed rows)
 constexpr int kWStages = 6;                  // streamed-operand ring
 constexpr int kWBlockBytes = 128 * kBK * 2;  // 16 KiB: 128 features x 64 rows, MN-major, 128B swizzle
-constexpr int kWNumBars = 3 * kWSlabKb + 3 * kWStages + 5;
+constexpr int kWNumBars = 3 * kWSlabKb + 2 * kWStages + 5;
 constexpr int kWTailBytes = 512;
 static_assert(8 * kWNumBars + 8 <= kWTailBytes, "barrier area");
 constexpr int kWSmemBytes = 1024 + (kWSlabKb + kWStages) * kWBlockBytes + kEpiWarps * kStageEpiBytes + kWTailBytes;
@@ -49,14 +53,14 @@ struct WBars {
     __device__ __forceinline__ uint32_t slab_full(int i) const { return base + 8u * i; }
     __device__ __forceinline__ uint32_t peer_slab_full(int i) const { return base + 8u * (kWSlabKb + i); }
     __device__ __forceinline__ uint32_t slab_empty(int i) const { return base + 8u * (2 * kWSlabKb + i); }
+    // full: the even CTA's barrier counts both CTAs' bytes of a stage
     __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * (3 * kWSlabKb + s); }
-    __device__ __forceinline__ uint32_t peer_full(int s) const { return base + 8u * (3 * kWSlabKb + kWStages + s); }
-    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (3 * kWSlabKb + 2 * kWStages + s); }
-    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kWSlabKb + 3 * kWStages + a); }
+    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (3 * kWSlabKb + kWStages + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kWSlabKb + 2 * kWStages + a); }
     __device__ __forceinline__ uint32_t tempty(int a) const {
-        return base + 8u * (3 * kWSlabKb + 3 * kWStages + 2 + a);
+        return base + 8u * (3 * kWSlabKb + 2 * kWStages + 2 + a);
     }
-    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kWSlabKb + 3 * kWStages + 4); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kWSlabKb + 2 * kWStages + 4); }
 };
 
 // Shape of one unit.  S = stationary tiles per expert (over H), T = streamed
@@ -106,7 +110,8 @@ __device__ __forceinline__ int w_kb1(const WUnit& u, int c) { return min(u.nkb, 
 
 // ------------------------------------------------------------ TMA producer
 // Streamed operand: 128 features (this CTA's half of the tile's 256) x 64 rows
-// per K block, two 64 x 64 boxes.
+// per K block, two 64 x 64 boxes, completing the even CTA's full barrier
+// (which the even CTA's producer arms with both CTAs' bytes).
 template <int F>
 __device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS, WBars bars, volatile int* abort,
                            int rank) {
@@ -119,11 +124,11 @@ __device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS
             const int f0 = t * 256 + 128 * rank;
             for (int kb = 0; kb < u.nkb; ++kb) {
                 if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
-                const uint32_t fb = bars.full(stage);
-                mbar_arrive_expect_tx(fb, (uint32_t)kWBlockBytes);
+                if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * kWBlockBytes);
+                const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
                 const uint32_t dst = sS + stage * kWBlockBytes;
-                tma_load_2d(dst, mS, f0, u.off + kb * kBK, fb);
-                tma_load_2d(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb);
+                tma_load_2d_pair(dst, mS, f0, u.off + kb * kBK, fb);
+                tma_load_2d_pair(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb);
                 if (++stage == kWStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -228,22 +233,21 @@ __device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars ba
                         if (!mbar_wait(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
                         if (!mbar_wait_cl(bars.peer_slab_full(i), (sphase >> i) & 1u, abort)) return;
                     }
-                    if (!mbar_wait(bars.full(stage), phase, abort)) return;
-                    if (!mbar_wait_cl(bars.peer_full(stage), phase, abort)) return;
+                    if (!mbar_wait_cl(bars.full(stage), phase, abort)) return;
                     tc_fence_after();
-                    fence_proxy_async_smem();  // the slab was written by cp.async
+                    if (first) fence_proxy_async_smem();  // a slab block freshly written by cp.async
                     const uint32_t sl = sL + i * kWBlockBytes;
                     const uint32_t st = sS + stage * kWBlockBytes;
-                    const uint32_t a = (F == DW1) ? sl : st;
-                    const uint32_t b = (F == DW1) ? st : sl;
+                    // descriptors of the block's first 16 rows; the next 16 rows
+                    // start 2048 bytes (128 descriptor units) further on
+                    const uint64_t ad = make_sdesc_sw128((F == DW1) ? sl : st, 8192, 1024);
+                    const uint64_t bd = make_sdesc_sw128((F == DW1) ? st : sl, 8192, 1024);
                     // stop at the 16-row step that holds the expert's last row
                     const int ksteps = min(kBK / 16, (u.cnt - kb * kBK + 15) / 16);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         if (kk >= ksteps) break;
-                        const uint64_t ad = make_sdesc_sw128(a + kk * 2048, 8192, 1024);
-                        const uint64_t bd = make_sdesc_sw128(b + kk * 2048, 8192, 1024);
-                        tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_bf16_pair(d, ad + 128u * kk, bd + 128u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair(bars.empty(stage));
                     if (last) {
@@ -262,10 +266,9 @@ __device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars ba
 }
 
 // The odd CTA's MMA thread: tells the even CTA that this CTA's half of a
-// slab block or of a stage is in shared memory, in the order the MMA uses them.
+// slab block is in shared memory, in the order the MMA uses the blocks.
 __device__ void w_role_relay(const GemmArgs& p, WBars bars, volatile int* abort) {
-    int stage = 0;
-    uint32_t phase = 0, sphase = 0;
+    uint32_t sphase = 0;
     const int T = p.n_tiles;
     for (WWalk w(p); w.valid(); w.next()) {
         const WUnit u = w.take();
@@ -282,12 +285,6 @@ __device__ void w_role_relay(const GemmArgs& p, WBars bars, volatile int* abort)
                         mbar_arrive_cluster(cluster_addr_of(bars.peer_slab_full(i), 0));
                     }
                     if (last) sphase ^= 1u << i;
-                    if (!mbar_wait(bars.full(stage), phase, abort)) return;
-                    mbar_arrive_cluster(cluster_addr_of(bars.peer_full(stage), 0));
-                    if (++stage == kWStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
             }
         }
@@ -393,7 +390,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(bars.full(s), 1);
-            mbar_init(bars.peer_full(s), 1);
             mbar_init(bars.empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
