@@ -26,10 +26,13 @@
 // activations), 5 MMA issuer on the even CTA / relay on the odd CTA, 6-13
 // gather producers (x or dY rows picked by the permutation table), 14 unit
 // scheduler (even CTA).
-//   * Producers of both CTAs fill their own stage and arrive on their own
-//     full[s]; the odd CTA's relay thread forwards that to the even CTA's
-//     peer_full[s].
-//   * The even CTA waits for full[s] and peer_full[s], issues the four M=256
+//   * Producers of both CTAs fill their own stage.  Where a flavour gathers
+//     rows (cp.async, L1 fwd and L2 dgrad) each CTA's producers arrive on its
+//     own full[s] and the odd CTA's relay thread forwards that to the even
+//     CTA's peer_full[s]; where every operand comes by TMA (L2 fwd, L1 dgrad)
+//     both CTAs' loads complete the even CTA's full[s] directly
+//     (.cta_group::2), so the MMA thread waits once per stage.
+//   * The even CTA waits for its barrier(s), issues the four M=256
 //     MMAs of the stage, and its commit arrives on empty[s] of both CTAs;
 //     after a unit's last K block a commit arrives on tfull[acc] of both.
 //   * Both CTAs' epilogue warps drain their own accumulator rows and arrive
@@ -90,16 +93,24 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 __device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-// TMA load into this CTA's shared memory whose completion is counted on the
+// TMA loads into this CTA's shared memory whose completion is counted on the
 // mbarrier at `bar_cluster` (a shared::cluster address that may lie in the
-// peer CTA of the pair: .cta_group::2), so that both CTAs' halves of an
-// operand complete one barrier of the MMA-issuing CTA.
+// peer CTA of the pair: .cta_group::2), so that both CTAs' halves of a stage
+// complete one barrier of the MMA-issuing CTA.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, int c0, int c1,
                                                  uint32_t bar_cluster) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
         : "memory");
 }
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int4 v) {
@@ -451,24 +462,31 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
         const uint32_t tx = (uint32_t)kT2ABytes + (T2<F>::kGather ? 0u : (uint32_t)nbox * 4096u);
         for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
-            const uint32_t fb = bars.full(stage);
-            mbar_arrive_expect_tx(fb, tx);
             const uint32_t a = sA + stage * kT2ABytes;
             const uint32_t b = sB + stage * kT2BBytes;
             const int k0 = kb * kBK;
-            if constexpr (F == L1_FWD) {
-                // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
-                tma_load_4d(a, mA, t.f0, 0, k0, t.e, fb);
-                tma_load_4d(a + 8192, mA, t.f0, 1, k0, t.e, fb);
-            } else if constexpr (F == L2_FWD) {
-                tma_load_3d(a, mA, t.f0, k0, t.e, fb);
-                tma_load_3d(a + 8192, mA, t.f0 + 64, k0, t.e, fb);
-                for (int i = 0; i < nbox; ++i) tma_load_2d(b + i * 4096, mB, k0, rb + 32 * i, fb);
-            } else if constexpr (F == L2_DGRAD) {
-                tma_load_3d(a, mA, k0, t.f0, t.e, fb);
-            } else {  // L1_DGRAD
-                tma_load_3d(a, mA, k0, t.f0, t.e, fb);
-                for (int i = 0; i < nbox; ++i) tma_load_2d(b + i * 4096, mB, k0, rb + 32 * i, fb);
+            if constexpr (F == L1_FWD || F == L2_DGRAD) {
+                const uint32_t fb = bars.full(stage);
+                mbar_arrive_expect_tx(fb, tx);
+                if constexpr (F == L1_FWD) {
+                    // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
+                    tma_load_4d(a, mA, t.f0, 0, k0, t.e, fb);
+                    tma_load_4d(a + 8192, mA, t.f0, 1, k0, t.e, fb);
+                } else {
+                    tma_load_3d(a, mA, k0, t.f0, t.e, fb);
+                }
+            } else {
+                // every operand by TMA: both CTAs' halves complete the even
+                // CTA's full barrier, armed there with both halves' bytes
+                if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * tx);
+                const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
+                if constexpr (F == L2_FWD) {
+                    tma_load_3d_pair(a, mA, t.f0, k0, t.e, fb);
+                    tma_load_3d_pair(a + 8192, mA, t.f0 + 64, k0, t.e, fb);
+                } else {  // L1_DGRAD
+                    tma_load_3d_pair(a, mA, k0, t.f0, t.e, fb);
+                }
+                for (int i = 0; i < nbox; ++i) tma_load_2d_pair(b + i * 4096, mB, k0, rb + 32 * i, fb);
             }
             if (++stage == T2<F>::kStages) {
                 stage = 0;
@@ -543,8 +561,12 @@ __device__ void t2_role_mma(const GemmArgs& p, uint32_t ring, uint32_t sA, uint3
         const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
         const uint32_t idesc = make_idesc_bf16(2 * kBM, t.n, T2<F>::kAMN, false);
         for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait(bars.full(stage), phase, abort)) return;
-            if (!mbar_wait_cl(bars.peer_full(stage), phase, abort)) return;
+            if constexpr (T2<F>::kGather) {
+                if (!mbar_wait(bars.full(stage), phase, abort)) return;
+                if (!mbar_wait_cl(bars.peer_full(stage), phase, abort)) return;
+            } else {
+                if (!mbar_wait_cl(bars.full(stage), phase, abort)) return;
+            }
             tc_fence_after();
             if constexpr (T2<F>::kGather) fence_proxy_async_smem();
             const uint32_t a = sA + stage * kT2ABytes;
@@ -575,6 +597,9 @@ __device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
     uint32_t phase = 0;
     T2Feed<F> feed(ring, bars, 1);
     for (T2Unit t; feed.template next<false>(t, abort, 0);) {
+        // flavours fed by TMA alone complete the even CTA's barrier directly;
+        // the relay still takes every unit from the feed
+        if constexpr (!T2<F>::kGather) continue;
         for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(bars.full(stage), phase, abort)) return;
             if constexpr (T2<F>::kGather) fence_proxy_async_smem();
