@@ -26,13 +26,15 @@
 // activations), 5 MMA issuer on the even CTA / relay on the odd CTA, 6-13
 // gather producers (x or dY rows picked by the permutation table), 14 unit
 // scheduler (even CTA).
-//   * Producers of both CTAs fill their own stage.  Where a flavour gathers
-//     rows (cp.async, L1 fwd and L2 dgrad) each CTA's producers arrive on its
-//     own full[s] and the odd CTA's relay thread forwards that to the even
-//     CTA's peer_full[s]; where every operand comes by TMA (L2 fwd, L1 dgrad)
-//     both CTAs' loads complete the even CTA's full[s] directly
-//     (.cta_group::2), so the MMA thread waits once per stage.
-//   * The even CTA waits for its barrier(s), issues the four M=256
+//   * Producers of both CTAs fill their own stage.  Both CTAs' TMA loads
+//     complete the even CTA's full[s] directly (.cta_group::2), armed there
+//     with both halves' bytes.  Where a flavour gathers rows (cp.async, L1
+//     fwd and L2 dgrad), each CTA's gather threads arrive on its own full[s]
+//     and the odd CTA's relay thread forwards its half to the even CTA's
+//     full[s], so the MMA thread waits on one barrier per stage (issuing a
+//     tcgen05.mma costs the thread a good part of the MMA's pipe time, and
+//     every extra wait in its loop shows up as idle tensor-pipe time).
+//   * The even CTA waits for full[s], issues the four M=256
 //     MMAs of the stage, and its commit arrives on empty[s] of both CTAs;
 //     after a unit's last K block a commit arrives on tfull[acc] of both.
 //   * Both CTAs' epilogue warps drain their own accumulator rows and arrive
@@ -50,7 +52,7 @@ constexpr int kT2ABytes = 128 * kBK * 2;  // this CTA's 128 features x 64 of K
 constexpr int kT2BBytes = 128 * kBK * 2;  // up to 128 routed rows x 64 of K
 constexpr int kT2InBytes = 3 * 2048;      // L2 dgrad epilogue inputs per warp: h gate, h up, a boxes
 constexpr int kUR = 4;                    // slots of the unit ring
-constexpr int kT2NumBars = 3 * kT2Stages + 9 + kEpiWarps + 2 * kUR + 1;
+constexpr int kT2NumBars = 2 * kT2Stages + 9 + kEpiWarps + 2 * kUR + 1;
 constexpr int kT2TailBytes = 512;         // barriers, TMEM address, abort flag, unit ring
 constexpr int kT2RingOff = (8 * kT2NumBars + 8 + 15) & ~15;
 static_assert(kT2RingOff + 16 * kUR <= kT2TailBytes, "barrier area");
@@ -60,23 +62,22 @@ constexpr int kT2Threads = kGemmThreads + 32;
 struct T2Bars {
     uint32_t base;
     __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * s; }
-    __device__ __forceinline__ uint32_t peer_full(int s) const { return base + 8u * (kT2Stages + s); }
-    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (2 * kT2Stages + s); }
-    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kT2Stages + a); }
-    __device__ __forceinline__ uint32_t tempty(int a) const { return base + 8u * (3 * kT2Stages + 2 + a); }
-    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kT2Stages + 4); }
+    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (kT2Stages + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (2 * kT2Stages + a); }
+    __device__ __forceinline__ uint32_t tempty(int a) const { return base + 8u * (2 * kT2Stages + 2 + a); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (2 * kT2Stages + 4); }
     // L1 epilogue: up-projection values handed from warp 2 + i to warp i
-    __device__ __forceinline__ uint32_t xfull(int i) const { return base + 8u * (3 * kT2Stages + 5 + i); }
-    __device__ __forceinline__ uint32_t xempty(int i) const { return base + 8u * (3 * kT2Stages + 7 + i); }
+    __device__ __forceinline__ uint32_t xfull(int i) const { return base + 8u * (2 * kT2Stages + 5 + i); }
+    __device__ __forceinline__ uint32_t xempty(int i) const { return base + 8u * (2 * kT2Stages + 7 + i); }
     // L2 dgrad epilogue: the saved h and a boxes of epilogue warp w have landed
-    __device__ __forceinline__ uint32_t ein(int w) const { return base + 8u * (3 * kT2Stages + 9 + w); }
+    __device__ __forceinline__ uint32_t ein(int w) const { return base + 8u * (2 * kT2Stages + 9 + w); }
     // unit ring: slot i published (both CTAs) / read by every consumer of
     // both CTAs (even CTA's barrier); the even CTA's TMA producer took a unit
-    __device__ __forceinline__ uint32_t ufull(int i) const { return base + 8u * (3 * kT2Stages + 9 + kEpiWarps + i); }
+    __device__ __forceinline__ uint32_t ufull(int i) const { return base + 8u * (2 * kT2Stages + 9 + kEpiWarps + i); }
     __device__ __forceinline__ uint32_t uempty(int i) const {
-        return base + 8u * (3 * kT2Stages + 9 + kEpiWarps + kUR + i);
+        return base + 8u * (2 * kT2Stages + 9 + kEpiWarps + kUR + i);
     }
-    __device__ __forceinline__ uint32_t ustart() const { return base + 8u * (3 * kT2Stages + 9 + kEpiWarps + 2 * kUR); }
+    __device__ __forceinline__ uint32_t ustart() const { return base + 8u * (2 * kT2Stages + 9 + kEpiWarps + 2 * kUR); }
 };
 
 // ------------------------------------------------------- cluster helpers
@@ -111,6 +112,14 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2, int c3,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster)
         : "memory");
 }
 __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, int4 v) {
@@ -465,21 +474,17 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
             const uint32_t a = sA + stage * kT2ABytes;
             const uint32_t b = sB + stage * kT2BBytes;
             const int k0 = kb * kBK;
-            if constexpr (F == L1_FWD || F == L2_DGRAD) {
-                const uint32_t fb = bars.full(stage);
-                mbar_arrive_expect_tx(fb, tx);
-                if constexpr (F == L1_FWD) {
-                    // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
-                    tma_load_4d(a, mA, t.f0, 0, k0, t.e, fb);
-                    tma_load_4d(a + 8192, mA, t.f0, 1, k0, t.e, fb);
-                } else {
-                    tma_load_3d(a, mA, k0, t.f0, t.e, fb);
-                }
+            // both CTAs' TMA loads complete the even CTA's full barrier, armed
+            // there with both halves' bytes
+            if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * tx);
+            const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
+            if constexpr (F == L1_FWD) {
+                // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
+                tma_load_4d_pair(a, mA, t.f0, 0, k0, t.e, fb);
+                tma_load_4d_pair(a + 8192, mA, t.f0, 1, k0, t.e, fb);
+            } else if constexpr (F == L2_DGRAD) {
+                tma_load_3d_pair(a, mA, k0, t.f0, t.e, fb);
             } else {
-                // every operand by TMA: both CTAs' halves complete the even
-                // CTA's full barrier, armed there with both halves' bytes
-                if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * tx);
-                const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
                 if constexpr (F == L2_FWD) {
                     tma_load_3d_pair(a, mA, t.f0, k0, t.e, fb);
                     tma_load_3d_pair(a + 8192, mA, t.f0 + 64, k0, t.e, fb);
@@ -561,12 +566,7 @@ __device__ void t2_role_mma(const GemmArgs& p, uint32_t ring, uint32_t sA, uint3
         const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
         const uint32_t idesc = make_idesc_bf16(2 * kBM, t.n, T2<F>::kAMN, false);
         for (int kb = 0; kb < nkb; ++kb) {
-            if constexpr (T2<F>::kGather) {
-                if (!mbar_wait(bars.full(stage), phase, abort)) return;
-                if (!mbar_wait_cl(bars.peer_full(stage), phase, abort)) return;
-            } else {
-                if (!mbar_wait_cl(bars.full(stage), phase, abort)) return;
-            }
+            if (!mbar_wait_cl(bars.full(stage), phase, abort)) return;
             tc_fence_after();
             if constexpr (T2<F>::kGather) fence_proxy_async_smem();
             const uint32_t a = sA + stage * kT2ABytes;
@@ -601,9 +601,12 @@ __device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
         // the relay still takes every unit from the feed
         if constexpr (!T2<F>::kGather) continue;
         for (int kb = 0; kb < nkb; ++kb) {
+            // this CTA's gathered rows of the stage have landed (its local
+            // full barrier counts only the gather threads): make them visible
+            // to the tensor core and arrive on the even CTA's full barrier
             if (!mbar_wait(bars.full(stage), phase, abort)) return;
-            if constexpr (T2<F>::kGather) fence_proxy_async_smem();
-            mbar_arrive_cluster(cluster_addr_of(bars.peer_full(stage), 0));
+            fence_proxy_async_smem();
+            mbar_arrive_cluster(cluster_addr_of(bars.full(stage), 0));
             if (++stage == T2<F>::kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -843,10 +846,11 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     const int rank = (int)cluster_ctarank();
 
     if (threadIdx.x == 0) {
-        const uint32_t full_count = 1u + (T2<F>::kGather ? 32u * kGatherWarps : 0u);
+        // even CTA: its producer's arrive (both CTAs' TMA bytes), its gather
+        // threads and the odd CTA's relay; odd CTA: its gather threads only
+        const uint32_t full_count = !T2<F>::kGather ? 1u : (rank == 0 ? 2u + 32u * kGatherWarps : 32u * kGatherWarps);
         for (int s = 0; s < kT2Stages; ++s) {
             mbar_init(bars.full(s), full_count);
-            mbar_init(bars.peer_full(s), 1);
             mbar_init(bars.empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
