@@ -65,8 +65,8 @@ def load_peaks():
 
 # the sources that define the grouped-GEMM kernels whose DRAM traffic
 # profiles/traffic.json records; a change to any of them voids the record
-GEMM_SOURCES = ("grouped_gemm.cuh", "grouped_gemm_2sm.cuh", "ptx.cuh", "moe_internal.h", "gemm_fwd.cu",
-                "gemm_dgrad.cu", "gemm_wgrad.cu")
+GEMM_SOURCES = ("gemm_common.cuh", "grouped_gemm_2sm.cuh", "wgrad_pair.cuh", "ptx.cuh", "moe_internal.h",
+                "gemm_fwd.cu", "gemm_dgrad.cu", "gemm_wgrad.cu")
 
 
 def kernel_source_hash() -> str:

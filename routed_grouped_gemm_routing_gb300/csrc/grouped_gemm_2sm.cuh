@@ -43,7 +43,7 @@
 // status word, and both CTAs leave through the closing cluster barrier.
 #pragma once
 
-#include "grouped_gemm.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 
