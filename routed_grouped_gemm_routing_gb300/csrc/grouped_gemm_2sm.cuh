@@ -393,8 +393,13 @@ struct T2Feed {
     __device__ __forceinline__ bool next(T2Unit& t, volatile int* abort, int lane, bool start = false) {
         const int i = n % kUR;
         const uint32_t ph = (uint32_t)(n / kUR) & 1u;
-        bool ok = rank == 0 ? mbar_wait(bars.ufull(i), ph, abort) : mbar_wait_cl(bars.ufull(i), ph, abort);
-        if constexpr (kWarp) ok = __all_sync(0xffffffffu, ok);
+        bool ok;
+        if constexpr (kWarp) {
+            ok = rank == 0 ? warp_wait_uniform<false>(bars.ufull(i), ph, abort)
+                           : warp_wait_uniform<true>(bars.ufull(i), ph, abort);
+        } else {
+            ok = rank == 0 ? mbar_wait(bars.ufull(i), ph, abort) : mbar_wait_cl(bars.ufull(i), ph, abort);
+        }
         if (!ok) return false;
         const int4 v = ld_shared_v4s(ring + 16u * (uint32_t)i);
         if constexpr (kWarp) __syncwarp();
@@ -550,41 +555,47 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, T2
 }
 
 // -------------------------------------------- MMA issuer (even CTA) / relay
+// The whole MMA warp runs this loop: it waits warp-uniformly and one elected
+// lane issues the MMAs and their commits (see warp_wait_uniform).
 template <int F>
 __device__ void t2_role_mma(const GemmArgs& p, uint32_t ring, uint32_t sA, uint32_t sB, T2Bars bars,
-                            uint32_t tmem_base, volatile int* abort) {
+                            uint32_t tmem_base, volatile int* abort, int lane) {
     const int nkb = p.K / kBK;
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
     T2Feed<F> feed(ring, bars, 0);
-    for (T2Unit t; feed.template next<false>(t, abort, 0); ++it) {
+    for (T2Unit t; feed.template next<true>(t, abort, lane); ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait_cl(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+        if (!warp_wait_uniform<true>(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
         const uint32_t idesc = make_idesc_bf16(2 * kBM, t.n, T2<F>::kAMN, false);
         for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait_cl(bars.full(stage), phase, abort)) return;
+            if (!warp_wait_uniform<true>(bars.full(stage), phase, abort)) return;
             tc_fence_after();
-            if constexpr (T2<F>::kGather) fence_proxy_async_smem();
             const uint32_t a = sA + stage * kT2ABytes;
             const uint32_t b = sB + stage * kT2BBytes;
+            if (elect_one()) {
+                if constexpr (T2<F>::kGather) fence_proxy_async_smem();
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint64_t ad = T2<F>::kAMN ? make_sdesc_sw128(a + kk * 2048, 8192, 1024)
-                                                : make_sdesc_sw128(a + kk * 32, 16, 1024);
-                const uint64_t bd = make_sdesc_sw128(b + kk * 32, 16, 1024);
-                tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    const uint64_t ad = T2<F>::kAMN ? make_sdesc_sw128(a + kk * 2048, 8192, 1024)
+                                                    : make_sdesc_sw128(a + kk * 32, 16, 1024);
+                    const uint64_t bd = make_sdesc_sw128(b + kk * 32, 16, 1024);
+                    tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+                tc_commit_pair(bars.empty(stage));
             }
-            tc_commit_pair(bars.empty(stage));
+            __syncwarp();
             if (++stage == T2<F>::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        tc_commit_pair(bars.tfull(acc));
+        if (elect_one()) tc_commit_pair(bars.tfull(acc));
+        __syncwarp();
     }
 }
 
@@ -896,19 +907,20 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         if constexpr (T2<F>::kGather) t2_role_gather<F>(p, ring, sB, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            if (rank == 0) {
-                t2_role_mma<F>(p, ring, sA, sB, bars, tmem_base, abort);
-                if (*abort) {
-                    // let every MMA already issued finish before TMEM is released
-                    tc_commit_pair_local(bars.drain());
-                    const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
-                    }
+        if (rank == 0) {
+            t2_role_mma<F>(p, ring, sA, sB, bars, tmem_base, abort, lane);
+            const bool aborted = __any_sync(0xffffffffu, *abort != 0);
+            if (elect_one() && aborted) {
+                // let every MMA already issued (by this same elected lane)
+                // finish before TMEM is released
+                tc_commit_pair_local(bars.drain());
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
                 }
-            } else {
-                t2_role_relay<F>(p, ring, bars, abort);
             }
+            __syncwarp();
+        } else if (lane == 0) {
+            t2_role_relay<F>(p, ring, bars, abort);
         }
     } else {
         t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, ring, bars, tmem_base,

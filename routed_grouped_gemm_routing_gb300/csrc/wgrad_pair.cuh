@@ -205,6 +205,8 @@ __device__ void w_role_gather(const GemmArgs& p, uint32_t sL, WBars bars, volati
 }
 
 // -------------------------------------------------------------- MMA issuer
+// The whole MMA warp runs this loop: it waits warp-uniformly and one elected
+// lane issues the MMAs and their commits (see warp_wait_uniform).
 template <int F>
 __device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars bars, uint32_t tmem_base,
                            volatile int* abort) {
@@ -218,7 +220,7 @@ __device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars ba
         for (int t = 0; t < T; ++t, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait_cl(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+            if (!warp_wait_uniform<true>(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * 256);
             for (int c = 0; c < u.nch; ++c) {
@@ -230,12 +232,11 @@ __device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars ba
                 for (int kb = kb0; kb < kb1; ++kb) {
                     const int i = kb - kb0;
                     if (first) {
-                        if (!mbar_wait(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
-                        if (!mbar_wait_cl(bars.peer_slab_full(i), (sphase >> i) & 1u, abort)) return;
+                        if (!warp_wait_uniform<false>(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
+                        if (!warp_wait_uniform<true>(bars.peer_slab_full(i), (sphase >> i) & 1u, abort)) return;
                     }
-                    if (!mbar_wait_cl(bars.full(stage), phase, abort)) return;
+                    if (!warp_wait_uniform<true>(bars.full(stage), phase, abort)) return;
                     tc_fence_after();
-                    if (first) fence_proxy_async_smem();  // a slab block freshly written by cp.async
                     const uint32_t sl = sL + i * kWBlockBytes;
                     const uint32_t st = sS + stage * kWBlockBytes;
                     // descriptors of the block's first 16 rows; the next 16 rows
@@ -244,23 +245,26 @@ __device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars ba
                     const uint64_t bd = make_sdesc_sw128((F == DW1) ? st : sl, 8192, 1024);
                     // stop at the 16-row step that holds the expert's last row
                     const int ksteps = min(kBK / 16, (u.cnt - kb * kBK + 15) / 16);
+                    if (elect_one()) {
+                        if (first) fence_proxy_async_smem();  // a slab block freshly written by cp.async
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        if (kk >= ksteps) break;
-                        tc_mma_bf16_pair(d, ad + 128u * kk, bd + 128u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            if (kk >= ksteps) break;
+                            tc_mma_bf16_pair(d, ad + 128u * kk, bd + 128u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        tc_commit_pair(bars.empty(stage));
+                        if (last) tc_commit_pair(bars.slab_empty(i));
                     }
-                    tc_commit_pair(bars.empty(stage));
-                    if (last) {
-                        tc_commit_pair(bars.slab_empty(i));
-                        sphase ^= 1u << i;
-                    }
+                    __syncwarp();
+                    if (last) sphase ^= 1u << i;
                     if (++stage == kWStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            tc_commit_pair(bars.tfull(acc));
+            if (elect_one()) tc_commit_pair(bars.tfull(acc));
+            __syncwarp();
         }
     }
 }
@@ -419,18 +423,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         w_role_gather(p, sL, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            if (rank == 0) {
-                w_role_mma<F>(p, sL, sS, bars, tmem_base, abort);
-                if (*abort) {
-                    tc_commit_pair_local(bars.drain());
-                    const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
-                    }
+        if (rank == 0) {
+            w_role_mma<F>(p, sL, sS, bars, tmem_base, abort);
+            const bool aborted = __any_sync(0xffffffffu, *abort != 0);
+            if (elect_one() && aborted) {
+                // let every MMA already issued (by this same elected lane)
+                // finish before TMEM is released
+                tc_commit_pair_local(bars.drain());
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bars.drain(), 0) && global_timer_ns() - t0 < 100000000ull) {
                 }
-            } else {
-                w_role_relay(p, bars, abort);
             }
+            __syncwarp();
+        } else if (lane == 0) {
+            w_role_relay(p, bars, abort);
         }
     } else {
         w_role_epilogue<F>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
