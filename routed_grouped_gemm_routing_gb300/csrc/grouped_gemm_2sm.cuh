@@ -23,8 +23,10 @@
 //
 // Roles (per CTA, 15 warps): 0-3 epilogue (TMEM lanes = this CTA's 128
 // features, columns = rows), 4 TMA producer (weights; non-gathered
-// activations), 5 MMA issuer on the even CTA / relay on the odd CTA, 6-13
-// gather producers (x or dY rows picked by the permutation table), 14 unit
+// activations), 5 MMA warp on the even CTA (warp-uniform waits, one elected
+// lane issues) / relay on the odd CTA, 6-13 gather producers (x or dY rows
+// picked by the permutation table; in the flavours fed by TMA alone, warps
+// 6-8 are three more TMA producers, K blocks dealt round-robin), 14 unit
 // scheduler (even CTA).
 //   * Producers of both CTAs fill their own stage.  Both CTAs' TMA loads
 //     complete the even CTA's full[s] directly (.cta_group::2), armed there
@@ -241,6 +243,7 @@ struct T2<L1_FWD> {
     static constexpr bool kGather = true, kAMN = true;
     static constexpr int kFeatPerCta = 64;  // 64 gate + 64 up features
     static constexpr int kStages = 6;
+    static constexpr int kProducers = 1;  // TMA producer threads (one TMA issue stream each)
     static constexpr int kInBytes = 0;
 };
 template <>
@@ -248,6 +251,7 @@ struct T2<L2_FWD> {
     static constexpr bool kGather = false, kAMN = true;
     static constexpr int kFeatPerCta = 128;
     static constexpr int kStages = 6;
+    static constexpr int kProducers = 4;  // TMA producer threads (one TMA issue stream each)
     static constexpr int kInBytes = 0;
 };
 template <>
@@ -255,6 +259,7 @@ struct T2<L2_DGRAD> {
     static constexpr bool kGather = true, kAMN = false;
     static constexpr int kFeatPerCta = 128;
     static constexpr int kStages = 5;
+    static constexpr int kProducers = 1;  // TMA producer threads (one TMA issue stream each)
     static constexpr int kInBytes = kEpiWarps * kT2InBytes;
 };
 template <>
@@ -262,6 +267,7 @@ struct T2<L1_DGRAD> {
     static constexpr bool kGather = false, kAMN = false;
     static constexpr int kFeatPerCta = 128;
     static constexpr int kStages = 6;
+    static constexpr int kProducers = 4;  // TMA producer threads (one TMA issue stream each)
     static constexpr int kInBytes = 0;
 };
 
@@ -271,6 +277,9 @@ constexpr int t2_smem_bytes() {
            kT2TailBytes;
 }
 static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448, "shared memory per CTA");
+static_assert(T2<L1_FWD>::kProducers == 1 && T2<L2_DGRAD>::kProducers == 1 && T2<L2_FWD>::kProducers <= 1 + kGatherWarps &&
+                  T2<L1_DGRAD>::kProducers <= 1 + kGatherWarps,
+              "producer warps");
 
 // Element (row j, column l) of a 32-row x 32-column bf16 box in the 64-byte swizzle.
 __device__ __forceinline__ float lds_sw64(uint32_t box, int j, int l) {
@@ -462,19 +471,33 @@ __device__ void t2_role_sched(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
 }
 
 // ------------------------------------------------------------ TMA producer
+// The K blocks are dealt round-robin to kProducers threads in different warps
+// (block g to thread g % kProducers): one thread's bulk tensor copies are
+// processed one after the other, at about 30 bytes per cycle for these boxes
+// on this GPU, whatever the number in flight, while copies from separate
+// threads proceed side by side.
 template <int F>
 __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, uint32_t ring,
-                            uint32_t sA, uint32_t sB, T2Bars bars, volatile int* abort, int rank) {
+                            uint32_t sA, uint32_t sB, T2Bars bars, volatile int* abort, int rank, int pid) {
+    constexpr int NP = T2<F>::kProducers;
     const int nkb = p.K / kBK;
     int stage = 0;
     uint32_t phase = 0;
+    uint32_t g = 0;
     T2Feed<F> feed(ring, bars, rank);
-    for (T2Unit t; feed.template next<false>(t, abort, 0, rank == 0);) {
+    for (T2Unit t; feed.template next<false>(t, abort, 0, rank == 0 && pid == 0);) {
         const int nh = t.n >> 1;           // this CTA's rows of the unit
         const int nbox = (nh + 31) >> 5;   // 32-row boxes of a non-gathered B
         const int rb = t.r0 + nh * rank;
         const uint32_t tx = (uint32_t)kT2ABytes + (T2<F>::kGather ? 0u : (uint32_t)nbox * 4096u);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+            if (NP > 1 && (int)(g % (uint32_t)NP) != pid) {
+                if (++stage == T2<F>::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                continue;
+            }
             if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
             const uint32_t a = sA + stage * kT2ABytes;
             const uint32_t b = sB + stage * kT2BBytes;
@@ -872,9 +895,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
         mbar_init(bars.drain(), 1);
         for (int w = 0; w < kEpiWarps; ++w) mbar_init(bars.ein(w), 1);
-        // consumers of a published unit: TMA, MMA or relay, epilogue warps
-        // and (gathering flavours) gather warps, in both CTAs
-        const uint32_t consumers = 2u * (2u + kEpiWarps + (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u));
+        // consumers of a published unit: TMA producers, MMA or relay,
+        // epilogue warps and (gathering flavours) gather warps, in both CTAs
+        const uint32_t consumers =
+            2u * (1u + (uint32_t)T2<F>::kProducers + kEpiWarps + (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u));
         for (int i = 0; i < kUR; ++i) {
             mbar_init(bars.ufull(i), 1);
             mbar_init(bars.uempty(i), consumers);
@@ -899,8 +923,14 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == kWarpTma) {
-        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, bars, abort, rank);
+    // producer id of this warp's lane 0, or -1
+    int pid = warp == kWarpTma ? 0 : -1;
+    if constexpr (!T2<F>::kGather) {
+        // the gather warps are free in the flavours fed by TMA alone
+        if (warp >= kWarpGather0 && warp < kWarpGather0 + T2<F>::kProducers - 1) pid = 1 + warp - kWarpGather0;
+    }
+    if (pid >= 0) {
+        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, bars, abort, rank, pid);
     } else if (warp == kWarpSched) {
         if (lane == 0 && rank == 0) t2_role_sched<F>(p, ring, bars, abort);
     } else if (warp >= kWarpGather0) {
@@ -926,7 +956,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, ring, bars, tmem_base,
                             sStage + warp * kStageEpiBytes, sStage, sIn + warp * kT2InBytes, abort, warp, lane, rank);
     }
-    if (warp == kWarpTma && lane == 0 && *abort) {
+    if (pid >= 0 && lane == 0 && *abort) {
         // bulk copies already issued land within microseconds; give them time
         const uint64_t t0 = global_timer_ns();
         while (global_timer_ns() - t0 < 2000000ull) {
