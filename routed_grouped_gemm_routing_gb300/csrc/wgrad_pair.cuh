@@ -25,6 +25,11 @@
 // blocks, the slab gathered again for every (tile, chunk).  An expert
 // without routed rows gets zeros.
 //
+// The streamed tiles of a unit start at tile (s mod T) so that the clusters
+// of one expert's stationary tiles read different rows at any moment, and
+// the weight-gradient stores are marked evict-first in L2 so that the
+// streamed rows, re-read by those clusters, stay there.
+//
 // Roles (per CTA, 14 warps): 0-3 epilogue, 4 TMA producer (streamed
 // operand), 5 MMA issuer on the even CTA / relay on the odd CTA (forwards
 // "this CTA's half of a slab block has landed"), 6-13 gather producers
@@ -121,14 +126,19 @@ __device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS
     for (WWalk w(p); w.valid(); w.next()) {
         const WUnit u = w.take();
         for (int t = 0; t < T; ++t) {
-            const int f0 = t * 256 + 128 * rank;
+            const int tt = (t + u.s) % T;  // streamed tiles rotated per stationary tile
+            const int f0 = tt * 256 + 128 * rank;
             for (int kb = 0; kb < u.nkb; ++kb) {
                 if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
                 if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * kWBlockBytes);
                 const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
                 const uint32_t dst = sS + stage * kWBlockBytes;
-                tma_load_2d_pair(dst, mS, f0, u.off + kb * kBK, fb);
-                tma_load_2d_pair(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb);
+                // the expert's streamed rows are read again by the other
+                // stationary tiles' clusters: keep them in L2 against the
+                // stream of weight-gradient stores (stored evict-first)
+                const uint64_t pol = l2_policy_evict_last();
+                tma_load_2d_pair_hint(dst, mS, f0, u.off + kb * kBK, fb, pol);
+                tma_load_2d_pair_hint(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb, pol);
                 if (++stage == kWStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -319,8 +329,9 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars 
             }
             tc_fence_after();
             const uint32_t tacc = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(warp * 32) << 16);
-            const int row0 = ((F == DW1) ? u.s : t) * 256 + 128 * rank + 32 * warp;
-            const int colb = ((F == DW1) ? t : u.s) * 256;
+            const int tt = (t + u.s) % T;
+            const int row0 = ((F == DW1) ? u.s : tt) * 256 + 128 * rank + 32 * warp;
+            const int colb = ((F == DW1) ? tt : u.s) * 256;
             const bool have_acc = u.nkb > 0;
 #pragma unroll 1
             for (int c64 = 0; c64 < 4; ++c64) {
@@ -350,7 +361,7 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars 
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(mC, col, row0, u.e, buf);
+                    tma_store_3d_hint(mC, col, row0, u.e, buf, l2_policy_evict_first());
                     bulk_commit();
                 }
                 ++nstore;
