@@ -245,7 +245,7 @@ def run_ours(args):
 
     from routed_grouped_gemm_routing_gb300 import binding as B
     from routed_grouped_gemm_routing_gb300 import build
-    from routed_grouped_gemm_routing_gb300.layer import MoEWorkspace, train_step_from_host
+    from routed_grouped_gemm_routing_gb300.layer import HostPipeline, MoEWorkspace
     from routed_grouped_gemm_routing_gb300.workloads import CONFIGS, make_layer_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -361,28 +361,29 @@ def run_ours(args):
     # end to end through the public API, from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        outs = dict(x=torch.empty_like(inp["x"]), idx=torch.empty_like(inp["topk_idx"]),
-                    w=torch.empty_like(inp["topk_w"]), dY=torch.empty_like(inp["dY"]), y=y, dx=dx, dW1=dW1,
-                    dW2=dW2, dw=dw)
         host = {n: inp[n].cpu().pin_memory() for n in ("x", "topk_idx", "topk_w", "dY")}
-        outs["y_h"] = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-        outs["dx_h"] = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-        outs["dw_h"] = torch.empty(T, k, dtype=torch.float32).pin_memory()
+        outs = {"y_h": torch.empty(T, H, dtype=torch.bfloat16).pin_memory(),
+                "dx_h": torch.empty(T, H, dtype=torch.bfloat16).pin_memory(),
+                "dw_h": torch.empty(T, k, dtype=torch.float32).pin_memory()}
+        pipe = HostPipeline(ws, inp["W1"], inp["W2"], dW1, dW2)
 
         def e2e_step():
-            train_step_from_host(host["x"], host["topk_idx"], host["topk_w"], host["dY"], inp["W1"], inp["W2"], ws,
-                                 outs)
+            pipe.submit(host["x"], host["topk_idx"], host["topk_w"], host["dY"], outs["y_h"], outs["dx_h"],
+                        outs["dw_h"])
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
+        pipe.synchronize()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
+        a.record(pipe.compute)
+        pipe.up.wait_stream(pipe.compute)
         for _ in range(args.steps):
             e2e_step()
-        b.record()
+        pipe.synchronize()
+        b.record(pipe.compute)
         torch.cuda.synchronize()
         ems = a.elapsed_time(b)
         if world > 1:
@@ -394,7 +395,8 @@ def run_ours(args):
         e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps,
                "note": "x, topk_idx, topk_weights, dY copied in from pinned host memory and y, dx, "
-                       "d topk_weights copied out every step; dW1/dW2 stay on the device"}
+                       "d topk_weights copied out every step (HostPipeline: uploads of step n+1 and downloads "
+                       "of step n overlap the kernels); dW1/dW2 stay on the device"}
 
     # the router stage in front of the layer (logits -> top-k ids and weights
     # -> routing tables), timed on its own: it is not part of the layer step

@@ -109,3 +109,82 @@ def train_step_from_host(x_h, topk_idx_h, topk_w_h, dY_h, W1, W2, ws: MoEWorkspa
     outs["y_h"].copy_(outs["y"], non_blocking=True)
     outs["dx_h"].copy_(outs["dx"], non_blocking=True)
     outs["dw_h"].copy_(outs["dw"], non_blocking=True)
+
+
+class HostPipeline:
+    """Forward+backward steps fed from pinned HOST buffers, with the copies
+    overlapped with the layer's kernels.
+
+    ``submit(x_h, topk_idx_h, topk_w_h, dY_h, y_h, dx_h, dw_h)`` enqueues one
+    step and returns at once: the host->device copies of the step's inputs go
+    on an upload stream, the routing prologue, forward and backward on the
+    compute stream (the current stream when the pipeline was made), and the
+    device->host copies of y (as soon as the forward is done) and of dx and
+    d(topk_weights) (after the backward) on a download stream.  Inputs and
+    outputs on the device are double-buffered, so step n+1's uploads run
+    during step n's kernels and step n's downloads during step n+1's.  The
+    weight gradients stay on the device in ``dW1``/``dW2`` (overwritten by
+    every step), where an optimizer would consume them.  Host buffers handed
+    to ``submit`` must stay untouched until ``synchronize()``."""
+
+    def __init__(self, ws: MoEWorkspace, W1, W2, dW1=None, dW2=None):
+        s = ws.shape
+        dev = ws.device
+        self.ws, self.W1, self.W2 = ws, W1, W2
+        self.compute = torch.cuda.current_stream(dev)
+        self.up = torch.cuda.Stream(dev)
+        self.down = torch.cuda.Stream(dev)
+        bf = torch.bfloat16
+
+        def slot():
+            return dict(x=torch.empty(s.T, s.H, dtype=bf, device=dev),
+                        idx=torch.empty(s.T, s.k, dtype=torch.int32, device=dev),
+                        w=torch.empty(s.T, s.k, dtype=torch.float32, device=dev),
+                        dY=torch.empty(s.T, s.H, dtype=bf, device=dev),
+                        y=torch.empty(s.T, s.H, dtype=bf, device=dev),
+                        dx=torch.empty(s.T, s.H, dtype=bf, device=dev),
+                        dw=torch.empty(s.T, s.k, dtype=torch.float32, device=dev),
+                        uploaded=torch.cuda.Event(), fwd_done=torch.cuda.Event(), bwd_done=torch.cuda.Event(),
+                        downloaded=torch.cuda.Event(), used=False)
+
+        self.slots = [slot(), slot()]
+        self.dW1 = torch.empty_like(W1) if dW1 is None else dW1
+        self.dW2 = torch.empty_like(W2) if dW2 is None else dW2
+        self.n = 0
+
+    def submit(self, x_h, topk_idx_h, topk_w_h, dY_h, y_h, dx_h, dw_h):
+        sl = self.slots[self.n % 2]
+        self.n += 1
+        s = self.ws.shape
+        if sl["used"]:
+            # the slot's previous step must be done with its inputs and
+            # outputs before they are overwritten
+            self.up.wait_event(sl["bwd_done"])
+            self.up.wait_event(sl["downloaded"])
+        sl["used"] = True
+        with torch.cuda.stream(self.up):
+            sl["x"].copy_(x_h, non_blocking=True)
+            sl["idx"].copy_(topk_idx_h, non_blocking=True)
+            sl["w"].copy_(topk_w_h, non_blocking=True)
+            sl["dY"].copy_(dY_h, non_blocking=True)
+            sl["uploaded"].record(self.up)
+        c = self.compute
+        c.wait_event(sl["uploaded"])
+        B.moe_route_prologue(s, sl["idx"], self.ws.route, stream=c)
+        B.moe_forward(s, sl["x"], self.W1, self.W2, sl["w"], self.ws.route, self.ws.saved, sl["y"], stream=c)
+        sl["fwd_done"].record(c)
+        B.moe_backward(s, sl["dY"], sl["x"], self.W1, self.W2, sl["w"], self.ws.route, self.ws.saved, self.ws.bwd,
+                       sl["dx"], self.dW1, self.dW2, sl["dw"], stream=c)
+        sl["bwd_done"].record(c)
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(sl["fwd_done"])
+            y_h.copy_(sl["y"], non_blocking=True)
+            self.down.wait_event(sl["bwd_done"])
+            dx_h.copy_(sl["dx"], non_blocking=True)
+            dw_h.copy_(sl["dw"], non_blocking=True)
+            sl["downloaded"].record(self.down)
+
+    def synchronize(self):
+        """Makes the compute stream wait for every copy enqueued so far."""
+        self.compute.wait_stream(self.up)
+        self.compute.wait_stream(self.down)

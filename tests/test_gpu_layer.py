@@ -210,3 +210,37 @@ def test_autograd_wrapper_matches_abi():
     assert torch.equal(y, ref.y)
     assert torch.equal(x.grad, ref.dx) and torch.equal(W1.grad, ref.dW1) and torch.equal(W2.grad, ref.dW2)
     assert torch.equal(w.grad, ref.dw)
+
+
+def test_host_pipeline_matches_abi():
+    """Three steps through HostPipeline (uploads of step n+1 and downloads of
+    step n overlapping the kernels, double-buffered device slots) give the
+    same bytes as three direct runs on the device."""
+    from routed_grouped_gemm_routing_gb300.layer import HostPipeline, MoEWorkspace
+
+    shape = LayerShape("pipe", T=200, H=256, I=128, E=6, k=3)
+    batches = [_inputs(shape, 20 + i) for i in range(3)]
+    W1, W2 = batches[0]["W1"], batches[0]["W2"]
+    refs = []
+    for inp in batches:
+        inp = dict(inp, W1=W1, W2=W2)
+        run = GpuRun(shape.T, shape.H, shape.I, shape.E, shape.k)
+        run.run(inp)
+        torch.cuda.synchronize()
+        refs.append((run.y.cpu(), run.dx.cpu(), run.dw.cpu(), run.dW1.clone(), run.dW2.clone()))
+    ws = MoEWorkspace(shape.T, shape.H, shape.I, shape.E, shape.k)
+    pipe = HostPipeline(ws, W1, W2)
+    hosts, outs = [], []
+    for inp in batches:
+        h = {n: inp[n].cpu().pin_memory() for n in ("x", "topk_idx", "topk_w", "dY")}
+        o = (torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(shape.T, shape.k, dtype=torch.float32).pin_memory())
+        hosts.append(h)
+        outs.append(o)
+        pipe.submit(h["x"], h["topk_idx"], h["topk_w"], h["dY"], *o)
+    pipe.synchronize()
+    torch.cuda.synchronize()
+    for (y, dx, dw), (ry, rdx, rdw, _, _) in zip(outs, refs):
+        assert torch.equal(y, ry) and torch.equal(dx, rdx) and torch.equal(dw, rdw)
+    assert torch.equal(pipe.dW1, refs[-1][3]) and torch.equal(pipe.dW2, refs[-1][4])
