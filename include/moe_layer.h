@@ -170,6 +170,22 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
                  const float* topk_w, void* route_ws, const void* saved, void* bwd_ws,
                  void* dx, void* dW1, void* dW2, float* dtopk_w, void* stream);
 
+/* moe_backward with FP32 main-gradient accumulation, for training loops that
+ * sum weight gradients over micro-batches in FP32 buffers.  The pages have no
+ * counterpart: an addition of this library next to their backward (Mega MoE
+ * README, "Pipeline", backward paragraph).  Identical to moe_backward except
+ * that the weight gradients are not written as bf16: main_grad_W1 f32[E,H,2I] and
+ * main_grad_W2 f32[E,I,H] (device, row-major, 16-byte aligned, caller-owned)
+ * get main_grad += dW element-wise, from the FP32 accumulators, never rounded
+ * to bf16.  An expert with no routed slot adds nothing; T = 0 adds nothing.
+ * Each element receives exactly one addition per call, so the result does
+ * not depend on the launch order (deterministic); calls on the same buffers
+ * must not overlap on the GPU.  dx and dtopk_w are overwritten as in
+ * moe_backward.  Errors as for moe_backward. */
+int moe_backward_main_grad(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
+                           const float* topk_w, void* route_ws, const void* saved, void* bwd_ws, void* dx,
+                           float* main_grad_W1, float* main_grad_W2, float* dtopk_w, void* stream);
+
 /* Inference forward for callers that cannot allocate device memory when
  * they run the layer: for example a plugin inside an inference engine that
  * gets no workspace from its host, or a serving loop that must not call

@@ -67,8 +67,9 @@ def lib():
             L.moe_router_topk.argtypes = [P(MoeShape)] + [vp] * 5
             L.moe_forward.argtypes = [P(MoeShape)] + [vp] * 8
             L.moe_backward.argtypes = [P(MoeShape)] + [vp] * 13
+            L.moe_backward_main_grad.argtypes = [P(MoeShape)] + [vp] * 13
             L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
-            for n in ("moe_workspace_layout", "moe_route_prologue", "moe_router_topk", "moe_forward", "moe_backward",
+            for n in ("moe_workspace_layout", "moe_route_prologue", "moe_router_topk", "moe_forward", "moe_backward", "moe_backward_main_grad",
                       "moe_read_status"):
                 getattr(L, n).restype = ctypes.c_int
             L.moe_trace_begin.argtypes = [vp, ctypes.c_int]
@@ -160,6 +161,22 @@ def moe_backward(shape: MoeShape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws
         _ptr(bwd_ws, torch.uint8, L.bwd_bytes, "bwd_ws"), _ptr(dx, bf, T * H, "dx"),
         _ptr(dW1, bf, E * H * 2 * I, "dW1"), _ptr(dW2, bf, E * I * H, "dW2"),
         _ptr(dtopk_w, torch.float32, T * k, "dtopk_w"), _stream(stream)))
+
+
+def moe_backward_main_grad(shape: MoeShape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, main_grad_W1,
+                           main_grad_W2, dtopk_w, stream=None):
+    """moe_backward, but main_grad_W1 / main_grad_W2 (float32, same shapes as
+    W1 / W2) get += dW1 / dW2 in FP32 instead of bf16 dW being written."""
+    L = moe_workspace_layout(shape)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    bf, f32 = torch.bfloat16, torch.float32
+    _check(lib().moe_backward_main_grad(
+        ctypes.byref(shape), _ptr(dY, bf, T * H, "dY"), _ptr(x, bf, T * H, "x"), _ptr(W1, bf, E * H * 2 * I, "W1"),
+        _ptr(W2, bf, E * I * H, "W2"), _ptr(topk_w, f32, T * k, "topk_w"),
+        _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), _ptr(saved, torch.uint8, L.saved_bytes, "saved"),
+        _ptr(bwd_ws, torch.uint8, L.bwd_bytes, "bwd_ws"), _ptr(dx, bf, T * H, "dx"),
+        _ptr(main_grad_W1, f32, E * H * 2 * I, "main_grad_W1"), _ptr(main_grad_W2, f32, E * I * H, "main_grad_W2"),
+        _ptr(dtopk_w, f32, T * k, "dtopk_w"), _stream(stream)))
 
 
 def moe_read_status(shape: MoeShape, route_ws, stream=None) -> list[int]:

@@ -18,6 +18,8 @@ int launch_gemm_l2_dgrad(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_l1_dgrad(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw1(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw2(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_dw1_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_dw2_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 
 int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     switch (f) {
@@ -27,12 +29,15 @@ int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaS
         case L1_DGRAD: return launch_gemm_l1_dgrad(a, m, grid, st);
         case DW1: return launch_gemm_dw1(a, m, grid, st);
         case DW2: return launch_gemm_dw2(a, m, grid, st);
+        case DW1_MG: return launch_gemm_dw1_mg(a, m, grid, st);
+        case DW2_MG: return launch_gemm_dw2_mg(a, m, grid, st);
         default: return (int)cudaErrorInvalidValue;
     }
 }
 
 namespace {
-const char* const kGemmNames[] = {"gemm_l1_fwd", "gemm_l2_fwd", "gemm_l2_dgrad", "gemm_l1_dgrad", "gemm_dw1", "gemm_dw2"};
+const char* const kGemmNames[] = {"gemm_l1_fwd", "gemm_l2_fwd", "gemm_l2_dgrad", "gemm_l1_dgrad",
+                                  "gemm_dw1",    "gemm_dw2",    "gemm_dw1_mg",   "gemm_dw2_mg"};
 }  // namespace
 
 int launch_gemm(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
@@ -145,12 +150,13 @@ EncodeTiledFn encode_fn(std::string* err) {
 // bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
 // bytes for dims 1..rank-1.
 int make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-             const cuuint32_t* box, const char* what, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+             const cuuint32_t* box, const char* what, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B,
+             CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     std::string err;
     EncodeTiledFn fn = encode_fn(&err);
     if (!fn) return fail(MOE_ECUDA, err);
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
+    CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -177,6 +183,14 @@ int map_3d(CUtensorMap* m, const void* p, int E, int R, int C, int box_c, int bo
     cuuint64_t str[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 2 * (cuuint64_t)R};
     cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)box_r, 1};
     return make_map(m, p, 3, dims, str, box, what);
+}
+
+// [E][R][C] f32 (a main gradient), box 32 x 32 x 1 (128-byte rows)
+int map_3d_f32(CUtensorMap* m, const void* p, int E, int R, int C, const char* what) {
+    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)R, (cuuint64_t)E};
+    cuuint64_t str[2] = {(cuuint64_t)C * 4, (cuuint64_t)C * 4 * (cuuint64_t)R};
+    cuuint32_t box[3] = {32, 32, 1};
+    return make_map(m, p, 3, dims, str, box, what, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
 }
 
 // W1 [E][H][2I] viewed as [E][H][2][I] so that the gate and up halves are
@@ -385,9 +399,12 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     return MOE_OK;
 }
 
-int moe_backward(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
-                 const float* topk_w, void* route_ws, const void* saved, void* bwd_ws, void* dx, void* dW1,
-                 void* dW2, float* dtopk_w, void* stream) {
+// Body of moe_backward (main_grad false: dW1/dW2 bf16, overwritten) and of
+// moe_backward_main_grad (main_grad true: dW1/dW2 are the FP32 main
+// gradients, added to).
+static int backward_impl(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
+                  const float* topk_w, void* route_ws, const void* saved, void* bwd_ws, void* dx, void* dW1, void* dW2,
+                  float* dtopk_w, void* stream, bool main_grad) {
     Ctx c;
     int rc = prepare(shape, &c);
     if (rc) return rc;
@@ -402,6 +419,7 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     const int H = shape->H, I = shape->I, E = shape->E;
     cudaStream_t st = (cudaStream_t)stream;
     if (shape->T == 0) {
+        if (main_grad) return MOE_OK;  // nothing to add
         cudaError_t ce = cudaMemsetAsync(dW1, 0, (size_t)E * H * 2 * I * 2, st);
         if (ce == cudaSuccess) ce = cudaMemsetAsync(dW2, 0, (size_t)E * I * H * 2, st);
         if (ce != cudaSuccess) return cuda_fail((int)ce, "zeroing weight gradients");
@@ -442,28 +460,32 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     GemmMaps m3;
     memset(&m3, 0, sizeof m3);
     if ((rc = map_2d(&m3.a, aw, L.rows_cap, I, 64, 64, "aw"))) return rc;
-    if ((rc = map_3d(&m3.c0, dW2, E, I, H, 64, 32, "dW2 (store)"))) return rc;
+    if ((rc = main_grad ? map_3d_f32(&m3.c0, dW2, E, I, H, "main_grad_W2 (reduce-add)")
+                        : map_3d(&m3.c0, dW2, E, I, H, 64, 32, "dW2 (store)")))
+        return rc;
     // units: (expert, 256 features of H); each streams the expert's aw in
     // tiles of 256 features of I
     GemmArgs g3 = base_args(shape, L, route);
     g3.m_tiles = cdiv(H, 256);
     g3.n_tiles = cdiv(I, 256);
     g3.gsrc = static_cast<const __nv_bfloat16*>(dY);
-    e = launch_gemm(DW2, g3, m3, E * g3.m_tiles, st);
+    e = launch_gemm(main_grad ? DW2_MG : DW2, g3, m3, E * g3.m_tiles, st);
     if (e) return cuda_fail(e, "dW2 launch");
 
     // dW1[e] = x_e^T . dh_e (variable K, x re-gathered)
     GemmMaps m4;
     memset(&m4, 0, sizeof m4);
     if ((rc = map_2d(&m4.b, dh, L.rows_cap, 2 * I, 64, 64, "dh (rows)"))) return rc;
-    if ((rc = map_3d(&m4.c0, dW1, E, H, 2 * I, 64, 32, "dW1 (store)"))) return rc;
+    if ((rc = main_grad ? map_3d_f32(&m4.c0, dW1, E, H, 2 * I, "main_grad_W1 (reduce-add)")
+                        : map_3d(&m4.c0, dW1, E, H, 2 * I, 64, 32, "dW1 (store)")))
+        return rc;
     // units: (expert, 256 features of H); each streams the expert's dh in
     // tiles of 256 features of 2I
     GemmArgs g4 = base_args(shape, L, route);
     g4.m_tiles = cdiv(H, 256);
     g4.n_tiles = cdiv(2 * I, 256);
     g4.gsrc = static_cast<const __nv_bfloat16*>(x);
-    e = launch_gemm(DW1, g4, m4, E * g4.m_tiles, st);
+    e = launch_gemm(main_grad ? DW1_MG : DW1, g4, m4, E * g4.m_tiles, st);
     if (e) return cuda_fail(e, "dW1 launch");
 
     // L1 dgrad: dxp = dh . W1[e]^T; units of 256 features of H
@@ -488,6 +510,20 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
     trace_post(st, "dw_reduce");
     if (e) return cuda_fail(e, "d(topk_weights) reduce launch");
     return MOE_OK;
+}
+
+int moe_backward(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
+                 const float* topk_w, void* route_ws, const void* saved, void* bwd_ws, void* dx, void* dW1,
+                 void* dW2, float* dtopk_w, void* stream) {
+    return backward_impl(shape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, dW1, dW2, dtopk_w, stream,
+                         false);
+}
+
+int moe_backward_main_grad(const moe_shape* shape, const void* dY, const void* x, const void* W1, const void* W2,
+                           const float* topk_w, void* route_ws, const void* saved, void* bwd_ws, void* dx,
+                           float* main_grad_W1, float* main_grad_W2, float* dtopk_w, void* stream) {
+    return backward_impl(shape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, main_grad_W1, main_grad_W2,
+                         dtopk_w, stream, true);
 }
 
 int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, void* stream) {

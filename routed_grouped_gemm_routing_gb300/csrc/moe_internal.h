@@ -36,7 +36,8 @@ constexpr int kGemmSmemBytes = 1024 + kStages * (kStageABytes + kStageBBytes) + 
 //   L1_DGRAD  dxp = dh . W1[e]^T
 //   DW1       dW1[e] = gather(x)^T . dh        (K = the expert's rows)
 //   DW2       dW2[e] = aw^T . gather(dY)       (K = the expert's rows)
-enum Flavour : int { L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5 };
+//   DW1_MG, DW2_MG  the same, added in FP32 to the caller's FP32 main gradient
+enum Flavour : int { L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5, DW1_MG = 6, DW2_MG = 7 };
 
 struct GemmArgs {
     int T, H, I, E, k;

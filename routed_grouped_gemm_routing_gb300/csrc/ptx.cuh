@@ -158,6 +158,15 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, int c0, 
                  : "memory");
 }
 
+// Element-wise reduce-add of a shared-memory box into global memory (the
+// tensor map's type, here f32): dst[...] += box.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, int c0, int c1, int c2, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups still read their shared-memory source.
 template <int N>

@@ -307,8 +307,11 @@ __device__ void w_role_relay(const GemmArgs& p, WBars bars, volatile int* abort)
 
 // ---------------------------------------------------------------- epilogue
 // Warp w drains TMEM lanes 32w..32w+31 (32 output rows) x 256 columns as four
-// 32 x 64 boxes in the 128-byte swizzle, each leaving by TMA store.
-template <int F>
+// 32 x 64 bf16 boxes in the 128-byte swizzle, each leaving by TMA store.
+// kMG (FP32 main-grad accumulation): eight 32 x 32 FP32 boxes instead, each
+// added element-wise to the caller's FP32 gradient by a TMA reduce-add; an
+// expert without routed rows adds nothing.
+template <int F, bool kMG>
 __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars bars, uint32_t tmem_base,
                                 uint32_t stage, volatile int* abort, int warp, int lane, int rank) {
     const uint32_t tempty_leader[2] = {cluster_addr_of(bars.tempty(0), 0), cluster_addr_of(bars.tempty(1), 0)};
@@ -333,38 +336,60 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars 
             const int row0 = ((F == DW1) ? u.s : tt) * 256 + 128 * rank + 32 * warp;
             const int colb = ((F == DW1) ? tt : u.s) * 256;
             const bool have_acc = u.nkb > 0;
+            if constexpr (kMG) {
 #pragma unroll 1
-            for (int c64 = 0; c64 < 4; ++c64) {
-                const int col = colb + 64 * c64;
-                if (row0 >= rows_out || col >= cols_out) break;
-                uint32_t pk[32];
-                {
-                    uint32_t r0[32], r1[32];
-                    if (have_acc) {
-                        tmem_ld32_nowait(tacc + 64 * c64, r0);
-                        tmem_ld32_nowait(tacc + 64 * c64 + 32, r1);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                for (int c32 = 0; c32 < 8 && have_acc; ++c32) {
+                    const int col = colb + 32 * c32;
+                    if (row0 >= rows_out || col >= cols_out) break;
+                    uint32_t r0[32];
+                    tmem_ld32_nowait(tacc + 32 * c32, r0);
+                    tmem_ld_wait();
+                    const uint32_t buf = stage + (nstore & 1u) * 4096u;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    stage_row_sw128(buf, lane, r0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_3d(mC, col, row0, u.e, buf);
+                        bulk_commit();
                     }
+                    ++nstore;
+                }
+            } else {
+#pragma unroll 1
+                for (int c64 = 0; c64 < 4; ++c64) {
+                    const int col = colb + 64 * c64;
+                    if (row0 >= rows_out || col >= cols_out) break;
+                    uint32_t pk[32];
+                    {
+                        uint32_t r0[32], r1[32];
+                        if (have_acc) {
+                            tmem_ld32_nowait(tacc + 64 * c64, r0);
+                            tmem_ld32_nowait(tacc + 64 * c64 + 32, r1);
+                            tmem_ld_wait();
+                        } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        pk[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
-                        pk[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+                            for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            pk[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+                            pk[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+                        }
                     }
+                    const uint32_t buf = stage + (nstore & 1u) * 4096u;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    stage_row_sw128(buf, lane, pk);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d_hint(mC, col, row0, u.e, buf, l2_policy_evict_first());
+                        bulk_commit();
+                    }
+                    ++nstore;
                 }
-                const uint32_t buf = stage + (nstore & 1u) * 4096u;
-                if (lane == 0) bulk_wait_read<1>();
-                __syncwarp();
-                stage_row_sw128(buf, lane, pk);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d_hint(mC, col, row0, u.e, buf, l2_policy_evict_first());
-                    bulk_commit();
-                }
-                ++nstore;
             }
             tc_fence_before();
             __syncwarp();
@@ -376,8 +401,9 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars 
 }
 
 // mapS: the streamed operand (dh for dW1, aw for dW2), box 64 x 64;
-// mapC: the weight gradient [E][rows][cols], box 64 x 32.
-template <int F>
+// mapC: the weight gradient [E][rows][cols], bf16 box 64 x 32 (kMG: the FP32
+// main gradient, box 32 x 32).
+template <int F, bool kMG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_wgrad_pair_kernel(const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapC,
                           const GemmArgs p) {
@@ -450,7 +476,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             w_role_relay(p, bars, abort);
         }
     } else {
-        w_role_epilogue<F>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
+        w_role_epilogue<F, kMG>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
     }
     if (warp == kWarpTma && lane == 0 && *abort) {
         const uint64_t t0 = global_timer_ns();
@@ -471,7 +497,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // (persistent, static unit stride).  a.m_tiles = stationary tiles per expert
 // (ceil(H / 256)), a.n_tiles = streamed tiles (ceil(2I / 256) for dW1,
 // ceil(I / 256) for dW2).
-template <int F>
+template <int F, bool kMG = false>
 int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensorMap& mapC, cudaStream_t st) {
     static int clusters_fit[kMaxDevices] = {};
     int dev = 0;
@@ -491,14 +517,14 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
     cfg.numAttrs = 1;
     if (clusters_fit[dev] == 0) {
         // set once per device, outside any stream capture (on the first call)
-        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
+        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F, kMG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
         if (e != cudaSuccess) return (int)e;
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return (int)e;
         cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, moe_wgrad_pair_kernel<F>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, moe_wgrad_pair_kernel<F, kMG>, &cfg);
         if (e != cudaSuccess) return (int)e;
         if (n < 1) return (int)cudaErrorInvalidConfiguration;
         clusters_fit[dev] = n;
@@ -507,7 +533,7 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
     if (units <= 0) return 0;
     const int clusters = units < clusters_fit[dev] ? (int)units : clusters_fit[dev];
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-    e = cudaLaunchKernelEx(&cfg, moe_wgrad_pair_kernel<F>, mapS, mapC, a);
+    e = cudaLaunchKernelEx(&cfg, moe_wgrad_pair_kernel<F, kMG>, mapS, mapC, a);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }

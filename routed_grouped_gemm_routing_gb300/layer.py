@@ -43,7 +43,7 @@ def _dims(x, W1, W2, topk_idx):
 
 class MoEFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, x, W1, W2, topk_idx, topk_weights, ws=None, activation_clamp=0.0):
+    def forward(ctx, x, W1, W2, topk_idx, topk_weights, ws=None, activation_clamp=0.0, main_grad=False):
         T, H, I, E, k = _dims(x, W1, W2, topk_idx)
         if ws is None or (ws.shape.T, ws.shape.H, ws.shape.I, ws.shape.E, ws.shape.k) != (T, H, I, E, k):
             ws = MoEWorkspace(T, H, I, E, k, device=x.device, activation_clamp=activation_clamp)
@@ -59,6 +59,7 @@ class MoEFunction(torch.autograd.Function):
         ctx.save_for_backward(x, W1, W2, w)
         ctx.ws = ws
         ctx.w_dtype = topk_weights.dtype
+        ctx.main_grad = main_grad
         return y
 
     @staticmethod
@@ -68,23 +69,37 @@ class MoEFunction(torch.autograd.Function):
         s = ws.shape
         dev = x.device
         dx = torch.empty_like(x)
+        dw = torch.empty(s.T, s.k, dtype=torch.float32, device=dev)
+        if ctx.main_grad:
+            # FP32 main gradients: W.main_grad += dW; no bf16 gradient
+            B.moe_backward_main_grad(s, dy.to(torch.bfloat16).contiguous(), x, W1.contiguous(), W2.contiguous(), w,
+                                     ws.route, ws.saved, ws.bwd, dx, W1.main_grad, W2.main_grad, dw)
+            return dx, None, None, None, dw.to(ctx.w_dtype), None, None, None
         dW1 = torch.empty_like(W1)
         dW2 = torch.empty_like(W2)
-        dw = torch.empty(s.T, s.k, dtype=torch.float32, device=dev)
         B.moe_backward(s, dy.to(torch.bfloat16).contiguous(), x, W1.contiguous(), W2.contiguous(), w, ws.route,
                        ws.saved, ws.bwd, dx, dW1, dW2, dw)
-        return dx, dW1, dW2, None, dw.to(ctx.w_dtype), None, None
+        return dx, dW1, dW2, None, dw.to(ctx.w_dtype), None, None, None
 
 
 def moe_layer(x, W1, W2, topk_idx, topk_weights, workspace: MoEWorkspace | None = None,
-              activation_clamp: float = 0.0):
+              activation_clamp: float = 0.0, accumulate_main_grad: bool = False):
     """y = sum_j topk_weights[:, j] * SwiGLU-MLP_{topk_idx[:, j]}(x), bf16.
 
     x bf16 [T,H]; W1 bf16 [E,H,2I] (gate | up); W2 bf16 [E,I,H];
     topk_idx int32/int64 [T,k] (-1 = dropped slot); topk_weights float [T,k].
     Differentiable in x, W1, W2 and topk_weights.  activation_clamp > 0
-    clamps both SwiGLU inputs to [-c, c] (gradients pass inside only)."""
-    return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace, float(activation_clamp))
+    clamps both SwiGLU inputs to [-c, c] (gradients pass inside only).
+    accumulate_main_grad: W1.main_grad and W2.main_grad (float32 tensors of
+    W1's and W2's shapes, set by the caller) get += dW1 / dW2 in FP32 and the
+    autograd gradients of W1 and W2 are None."""
+    if accumulate_main_grad:
+        for n, W in (("W1", W1), ("W2", W2)):
+            mg = getattr(W, "main_grad", None)
+            if mg is None or mg.dtype != torch.float32 or tuple(mg.shape) != tuple(W.shape):
+                raise ValueError(f"accumulate_main_grad needs {n}.main_grad: float32 of {n}'s shape")
+    return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace, float(activation_clamp),
+                             bool(accumulate_main_grad))
 
 
 def train_step_from_host(x_h, topk_idx_h, topk_w_h, dY_h, W1, W2, ws: MoEWorkspace, outs: dict):
