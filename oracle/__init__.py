@@ -71,6 +71,12 @@ def _lib():
                 for n in ("forward", "backward_tokens", "backward_experts"):
                     getattr(L, f"oracle_{n}_{suf}").restype = None
             L.oracle_num_threads.restype = ctypes.c_int
+            L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_decode.restype = ctypes.c_double
+            L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+            L.oracle_e4m3_encode.restype = ctypes.c_uint8
+            L.oracle_quantize_fp8.argtypes = [i32, i32, i32, vp, vp, vp]
+            L.oracle_quantize_fp8.restype = None
             _LIB = L
     return _LIB
 
@@ -101,6 +107,39 @@ def router_topk(logits: np.ndarray, k: int):
     w = np.zeros((max(T, 1), k), np.float32)
     _lib().oracle_router_topk(T, E, k, _p(lg), _p(idx), _p(w))
     return idx[:T], w[:T]
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one E4M3 byte (OCP FP8: bias 7, 3 mantissa bits, no
+    infinities, 0x7F / 0xFF NaN)."""
+    return float(_lib().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(v: float) -> int:
+    """E4M3 byte of v: round to nearest, ties to even, saturating at +-448."""
+    return int(_lib().oracle_e4m3_encode(float(v)))
+
+
+def quantize_fp8(x_bits: np.ndarray, gran: int = 32):
+    """Per-token FP8 quantization with UE8M0 block scales (DeepGEMM Mega-MoE
+    article, usage example: per-token cast, granularity 32).  x_bits: bf16
+    bit patterns [T, H] (uint16).  Returns q uint8 [T, H] (E4M3 bytes) and
+    sf uint8 [T, H // gran] (biased exponents: scale = 2^(sf - 127))."""
+    xb = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H = xb.shape
+    if H % gran:
+        raise ValueError("H must be a multiple of the granularity")
+    q = np.zeros((max(T, 1), H), np.uint8)
+    sf = np.zeros((max(T, 1), H // gran), np.uint8)
+    _lib().oracle_quantize_fp8(T, H, gran, _p(xb), _p(q), _p(sf))
+    return q[:T], sf[:T]
+
+
+def dequantize_fp8(q: np.ndarray, sf: np.ndarray, gran: int = 32) -> np.ndarray:
+    """decode(q) * 2^(sf - 127), float64 [T, H]."""
+    table = np.array([e4m3_decode(c) for c in range(256)], np.float64)
+    scale = np.ldexp(1.0, sf.astype(np.int64) - 127)
+    return table[q] * np.repeat(scale, gran, axis=1)
 
 
 def route(topk_idx: np.ndarray, E: int, bm: int = 128) -> dict:

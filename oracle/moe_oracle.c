@@ -27,6 +27,97 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* ------------------------------------------------------- FP8 activations */
+
+/*
+ * Per-token FP8 quantization of the layer input with power-of-two block
+ * scales (DeepGEMM Mega-MoE article, usage example: the activations are cast
+ * per token to FP8 with UE8M0 scale factors at a granularity of 32 elements
+ * along the hidden dimension before dispatch).  For token t and group g
+ * (elements 32g .. 32g+31 of the row):
+ *   amax = max |x|;  e = the smallest integer with 448 * 2^e >= amax
+ *   (e = 0 when amax = 0; e clamped to [-127, 127]);  sf[t, g] = e + 127
+ *   (UE8M0: the byte is the biased exponent of the scale 2^e);
+ *   q[t, i] = E4M3(x[t, i] / 2^e), round to nearest, ties to even, finite
+ *   values saturating at +-448.
+ * E4M3 (OCP FP8): sign bit, 4 exponent bits (bias 7), 3 mantissa bits; field
+ * f > 0: (1 + m/8) 2^(f-7); f = 0: (m/8) 2^-6; f = 15, m = 7 is NaN, so the
+ * largest finite value is 1.75 * 2^8 = 448.  The dequantized value is
+ * decode(q) * 2^(sf - 127).  Plain loops; x is given as bfloat16 bits.
+ */
+double oracle_e4m3_decode(uint8_t c) {
+    const int s = c >> 7, f = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (f == 15 && m == 7) return NAN;
+    if (f == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, f - 7);
+    return s ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(double v) {
+    if (isnan(v)) return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E; /* 448 = f 15, m 6 */
+    /* spacing of the representable values around a */
+    double step;
+    if (a < ldexp(1.0, -6)) {
+        step = ldexp(1.0, -9);
+    } else {
+        int ex;
+        frexp(a, &ex); /* a = r 2^ex, r in [0.5, 1): floor(log2 a) = ex - 1 */
+        step = ldexp(1.0, ex - 1 - 3);
+    }
+    const double n = a / step;           /* exact: a has few bits, step a power of two */
+    double r = floor(n);
+    const double frac = n - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0; /* nearest, ties to even */
+    const double q = r * step;
+    if (q == 0.0) return sign;
+    if (q < ldexp(1.0, -6)) return sign | (uint8_t)(q / ldexp(1.0, -9)); /* subnormal, f = 0 */
+    int ex;
+    const double fr = frexp(q, &ex); /* q = fr 2^ex: exponent field ex - 1 + 7 */
+    const int f = ex - 1 + 7;
+    const int m = (int)(fr * 16.0) - 8; /* (1 + m/8) = 2 fr */
+    return sign | (uint8_t)(f << 3) | (uint8_t)m;
+}
+
+static int fp8_group_exponent(double amax) {
+    if (amax == 0.0) return 0;
+    /* smallest e with 448 * 2^e >= amax, where 448 * 2^e = 0.875 * 2^(e + 9) */
+    int p;
+    const double r = frexp(amax, &p); /* amax = r 2^p, r in [0.5, 1) */
+    int e = r <= 0.875 ? p - 9 : p - 8;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+void oracle_quantize_fp8(int T, int H, int gran, const uint16_t* x, uint8_t* q, uint8_t* sf) {
+    const int G = H / gran;
+    for (int t = 0; t < T; ++t) {
+        for (int g = 0; g < G; ++g) {
+            double amax = 0.0;
+            for (int i = 0; i < gran; ++i) {
+                uint32_t b = (uint32_t)x[(size_t)t * H + (size_t)g * gran + i] << 16;
+                float v;
+                memcpy(&v, &b, 4);
+                if (fabs((double)v) > amax) amax = fabs((double)v);
+            }
+            const int e = fp8_group_exponent(amax);
+            sf[(size_t)t * G + g] = (uint8_t)(e + 127);
+            for (int i = 0; i < gran; ++i) {
+                uint32_t b = (uint32_t)x[(size_t)t * H + (size_t)g * gran + i] << 16;
+                float v;
+                memcpy(&v, &b, 4);
+                q[(size_t)t * H + (size_t)g * gran + i] = oracle_e4m3_encode(ldexp((double)v, -e));
+            }
+        }
+    }
+}
+
 /* ----------------------------------------------------------------- router */
 
 /*
