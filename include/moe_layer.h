@@ -170,6 +170,28 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
                  const float* topk_w, void* route_ws, const void* saved, void* bwd_ws,
                  void* dx, void* dW1, void* dW2, float* dtopk_w, void* stream);
 
+/* FP8 dispatch of the layer input (DeepGEMM Mega-MoE article, usage example:
+ * per-token cast of the activations to FP8 with UE8M0 scale factors at a
+ * granularity of 32 before dispatch).  x bf16[T,H] (H a multiple of 64) ->
+ * x_fp8 u8[T,H] and x_sf u8[T,H/32], device, row-major, caller-owned: for
+ * each token and each group of 32 consecutive elements, e = the smallest
+ * integer with 448 * 2^e >= max|x| over the group (0 for an all-zero group,
+ * clamped to [-127, 127]); x_sf = e + 127 (UE8M0: the scale is 2^(x_sf-127));
+ * x_fp8 = OCP E4M3 bytes of x / 2^e, rounded to nearest even, saturating at
+ * +-448.  Non-finite inputs are not supported.  Kernels on `stream` only.
+ * Errors as for moe_route_prologue. */
+int moe_quantize_fp8(const moe_shape* shape, const void* x, uint8_t* x_fp8, uint8_t* x_sf, void* stream);
+
+/* moe_forward with the input given as moe_quantize_fp8's x_fp8 / x_sf: the
+ * L1 GEMM gathers the E4M3 rows and their scales and widens them to bf16 in
+ * shared memory (exactly: an E4M3 value times a power of two is a bf16
+ * value), so the result equals moe_forward on the dequantized input
+ * decode(x_fp8) * 2^(x_sf - 127); gathered bytes are halved.  Everything
+ * else (saved, y, route_ws, errors) as for moe_forward; moe_backward may
+ * follow with x = the dequantized input. */
+int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const void* W1,
+                    const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream);
+
 /* moe_backward with FP32 main-gradient accumulation, for training loops that
  * sum weight gradients over micro-batches in FP32 buffers.  The pages have no
  * counterpart: an addition of this library next to their backward (Mega MoE

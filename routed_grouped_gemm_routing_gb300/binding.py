@@ -68,8 +68,11 @@ def lib():
             L.moe_forward.argtypes = [P(MoeShape)] + [vp] * 8
             L.moe_backward.argtypes = [P(MoeShape)] + [vp] * 13
             L.moe_backward_main_grad.argtypes = [P(MoeShape)] + [vp] * 13
+            L.moe_quantize_fp8.argtypes = [P(MoeShape)] + [vp] * 4
+            L.moe_forward_fp8.argtypes = [P(MoeShape)] + [vp] * 9
             L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
             for n in ("moe_workspace_layout", "moe_route_prologue", "moe_router_topk", "moe_forward", "moe_backward", "moe_backward_main_grad",
+                      "moe_quantize_fp8", "moe_forward_fp8",
                       "moe_read_status"):
                 getattr(L, n).restype = ctypes.c_int
             L.moe_trace_begin.argtypes = [vp, ctypes.c_int]
@@ -161,6 +164,27 @@ def moe_backward(shape: MoeShape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws
         _ptr(bwd_ws, torch.uint8, L.bwd_bytes, "bwd_ws"), _ptr(dx, bf, T * H, "dx"),
         _ptr(dW1, bf, E * H * 2 * I, "dW1"), _ptr(dW2, bf, E * I * H, "dW2"),
         _ptr(dtopk_w, torch.float32, T * k, "dtopk_w"), _stream(stream)))
+
+
+def moe_quantize_fp8(shape: MoeShape, x, x_fp8, x_sf, stream=None):
+    """Per-token FP8 quantization: x bf16 [T, H] -> x_fp8 uint8 [T, H] (E4M3
+    bytes) and x_sf uint8 [T, H // 32] (UE8M0 scale exponents)."""
+    T, H = shape.T, shape.H
+    _check(lib().moe_quantize_fp8(ctypes.byref(shape), _ptr(x, torch.bfloat16, T * H, "x"),
+                                  _ptr(x_fp8, torch.uint8, T * H, "x_fp8"), _ptr(x_sf, torch.uint8, T * H // 32, "x_sf"),
+                                  _stream(stream)))
+
+
+def moe_forward_fp8(shape: MoeShape, x_fp8, x_sf, W1, W2, topk_w, route_ws, saved, y, stream=None):
+    """moe_forward on the FP8-dispatched input (x_fp8, x_sf from moe_quantize_fp8)."""
+    L = moe_workspace_layout(shape)
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    bf = torch.bfloat16
+    _check(lib().moe_forward_fp8(
+        ctypes.byref(shape), _ptr(x_fp8, torch.uint8, T * H, "x_fp8"), _ptr(x_sf, torch.uint8, T * H // 32, "x_sf"),
+        _ptr(W1, bf, E * H * 2 * I, "W1"), _ptr(W2, bf, E * I * H, "W2"), _ptr(topk_w, torch.float32, T * k, "topk_w"),
+        _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), _ptr(saved, torch.uint8, L.saved_bytes, "saved"),
+        _ptr(y, bf, T * H, "y"), _stream(stream)))
 
 
 def moe_backward_main_grad(shape: MoeShape, dY, x, W1, W2, topk_w, route_ws, saved, bwd_ws, dx, main_grad_W1,

@@ -1,0 +1,81 @@
+// FP8 dispatch of the layer input (DeepGEMM Mega-MoE article, usage example:
+// activations cast per token to FP8 with UE8M0 scale factors at a
+// granularity of 32 elements before they are dispatched): the quantization
+// kernel, and the instantiation of the L1 GEMM whose gather reads the E4M3
+// rows.
+#include "grouped_gemm_2sm.cuh"
+
+namespace moe {
+namespace {
+
+// Exponent e of the group's scale 2^e: the smallest e with 448 * 2^e >= amax
+// (448 = 0.875 * 2^9 is the largest finite E4M3 value); 0 for an all-zero
+// group; clamped to the UE8M0 range [-127, 127].
+__device__ __forceinline__ int fp8_group_exponent(float amax) {
+    if (amax == 0.0f) return 0;
+    int p;
+    const float r = frexpf(amax, &p);  // amax = r 2^p, r in [0.5, 1)
+    const int e = r <= 0.875f ? p - 9 : p - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// One warp per 256 consecutive elements of x (row-major [T, H], H a multiple
+// of 32, so no 32-element group straddles two rows): lane l takes elements
+// 8l..8l+7; the four lanes of a group combine their maxima by shuffles.
+// Writes q[i] = E4M3(x[i] / 2^e) (round to nearest even, saturating) and
+// sf[g] = e + 127.  HBM-bound: 2 bytes read and 33/32 bytes written per
+// element.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, long long n,
+                                                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+    const int lane = threadIdx.x & 31;
+    const long long nchunk = (n + 255) / 256;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < nchunk; w += nwarps) {
+        const long long e0 = w * 256 + (long long)lane * 8;
+        const bool ok = e0 < n;
+        const uint4 raw = ok ? __ldg(reinterpret_cast<const uint4*>(x + e0)) : make_uint4(0u, 0u, 0u, 0u);
+        float v[8];
+        unpack_bf16x8(raw, v);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int e = fp8_group_exponent(amax);
+        if (ok) {
+            uint32_t word[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t acc = 0;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 f = make_float2(ldexpf(v[4 * h + 2 * j], -e), ldexpf(v[4 * h + 2 * j + 1], -e));
+                    const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+                    acc |= (uint32_t)two << (16 * j);
+                }
+                word[h] = acc;
+            }
+            *reinterpret_cast<uint2*>(q + e0) = make_uint2(word[0], word[1]);
+            if ((lane & 3) == 0) sf[e0 >> 5] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+}  // namespace
+
+int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t* sf, int num_sms, cudaStream_t st) {
+    if (n <= 0) return 0;
+    const long long nchunk = (n + 255) / 256;
+    long long blocks = (nchunk + 7) / 8;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    quantize_fp8_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, n, q, sf);
+    return (int)cudaGetLastError();
+}
+
+// L1 GEMM + SwiGLU with the gathered rows read as E4M3 + UE8M0 scales
+int launch_gemm_l1_fwd_fp8(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
+    return launch_gemm_pair<L1_FWD_FP8>(a, m, max_units, st);
+}
+
+}  // namespace moe

@@ -254,6 +254,16 @@ struct T2<L1_FWD> {
     static constexpr int kProducers = 1;  // TMA producer threads (one TMA issue stream each)
     static constexpr int kInBytes = 0;
 };
+// FP8 dispatch: the same GEMM, its gathered rows read as E4M3 bytes with
+// one UE8M0 scale per 32 elements and widened to bf16 on the way into
+// shared memory (exact: an E4M3 value times a power of two fits bf16).
+template <>
+struct T2<L1_FWD_FP8> : T2<L1_FWD> {};
+template <int F>
+__host__ __device__ constexpr bool t2_is_l1() {
+    return F == L1_FWD || F == L1_FWD_FP8;
+}
+
 template <>
 struct T2<L2_FWD> {
     static constexpr bool kGather = false, kAMN = true;
@@ -514,7 +524,7 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
             // there with both halves' bytes
             if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * tx);
             const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
-            if constexpr (F == L1_FWD) {
+            if constexpr (t2_is_l1<F>()) {
                 // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
                 tma_load_4d_pair(a, mA, t.f0, 0, k0, t.e, fb);
                 tma_load_4d_pair(a + 8192, mA, t.f0, 1, k0, t.e, fb);
@@ -564,22 +574,69 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, T2
             if (r < nh) s = __ldg(p.perm + rbase + r);
             tok[q] = r < nh ? (s >= 0 ? s / k : -1) : -2;  // -2: row not in this unit
         }
-        for (int kb = 0; kb < nkb; ++kb) {
-            if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
-            const uint32_t b = sB + stage * kT2BBytes;
-            const int col = kb * kBK + c * 8;
+        if constexpr (F == L1_FWD_FP8) {
+            // register path: the next block's bytes and scales are loaded
+            // while this block is widened and stored
+            const int G = H >> 5;
+            uint2 cur[4], nxt[4];
+            uint32_t cs[4], ns[4];
+            auto load = [&](int kb, uint2 (&d)[4], uint32_t (&sc)[4]) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tk = tok[q];
-                if (tk == -2) continue;
-                const int r = gw * 16 + rb + 4 * q;
-                const __nv_bfloat16* g = src + (size_t)(tk < 0 ? 0 : tk) * (size_t)H + col;
-                cp_async_16(b + r * 128 + ((c ^ (r & 7)) << 4), g, tk < 0 ? 0u : 16u);
+                for (int q = 0; q < 4; ++q) {
+                    const int tk = tok[q];
+                    if (tk >= 0) {
+                        d[q] = __ldg(reinterpret_cast<const uint2*>(p.gsrc8 + (size_t)tk * (size_t)H + kb * kBK + c * 8));
+                        sc[q] = __ldg(p.gsf + (size_t)tk * (size_t)G + kb * 2 + (c >> 2));
+                    } else {
+                        d[q] = make_uint2(0u, 0u);
+                        sc[q] = 127u;
+                    }
+                }
+            };
+            load(0, cur, cs);
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (kb + 1 < nkb) load(kb + 1, nxt, ns);
+                if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                const uint32_t b = sB + stage * kT2BBytes;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (tok[q] == -2) continue;
+                    const int r = gw * 16 + rb + 4 * q;
+                    const float sc = fp8_scale(cs[q]);
+                    st_shared_v4(b + r * 128 + ((c ^ (r & 7)) << 4), e4m3x2_to_bf16x2(cur[q].x & 0xffffu, sc),
+                                 e4m3x2_to_bf16x2(cur[q].x >> 16, sc), e4m3x2_to_bf16x2(cur[q].y & 0xffffu, sc),
+                                 e4m3x2_to_bf16x2(cur[q].y >> 16, sc));
+                }
+                fence_proxy_async_smem();  // generic-proxy stores, read by the tensor core
+                mbar_arrive(bars.full(stage));
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    cur[q] = nxt[q];
+                    cs[q] = ns[q];
+                }
+                if (++stage == T2<F>::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            cp_async_arrive_noinc(bars.full(stage));
-            if (++stage == T2<F>::kStages) {
-                stage = 0;
-                phase ^= 1u;
+        } else {
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                const uint32_t b = sB + stage * kT2BBytes;
+                const int col = kb * kBK + c * 8;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int tk = tok[q];
+                    if (tk == -2) continue;
+                    const int r = gw * 16 + rb + 4 * q;
+                    const __nv_bfloat16* g = src + (size_t)(tk < 0 ? 0 : tk) * (size_t)H + col;
+                    cp_async_16(b + r * 128 + ((c ^ (r & 7)) << 4), g, tk < 0 ? 0u : 16u);
+                }
+                cp_async_arrive_noinc(bars.full(stage));
+                if (++stage == T2<F>::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     }
@@ -695,7 +752,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
             const int row0 = t.r0 + 32 * c32;
             float v[32];
             tmem_ld32(tacc + 32 * c32, v);
-            if constexpr (F == L1_FWD) {
+            if constexpr (t2_is_l1<F>()) {
                 // lanes 0-63: gate features f0..f0+63, lanes 64-127: up features f0..f0+63
                 const int I = p.I;
                 const int pr = warp & 1;
@@ -924,7 +981,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         if constexpr (!T2<F>::kGather || F == L2_DGRAD) tma_prefetch_map(&mapB);
         if constexpr (F == L2_DGRAD) tma_prefetch_map(&mapD);
         tma_prefetch_map(&mapC0);
-        if constexpr (F == L1_FWD || F == L2_DGRAD) tma_prefetch_map(&mapC1);
+        if constexpr (t2_is_l1<F>() || F == L2_DGRAD) tma_prefetch_map(&mapC1);
     }
     tc_fence_before();
     cluster_sync();

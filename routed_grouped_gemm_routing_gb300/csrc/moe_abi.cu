@@ -20,6 +20,7 @@ int launch_gemm_dw1(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw2(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw1_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw2_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_l1_fwd_fp8(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 
 int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     switch (f) {
@@ -31,13 +32,15 @@ int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaS
         case DW2: return launch_gemm_dw2(a, m, grid, st);
         case DW1_MG: return launch_gemm_dw1_mg(a, m, grid, st);
         case DW2_MG: return launch_gemm_dw2_mg(a, m, grid, st);
+        case L1_FWD_FP8: return launch_gemm_l1_fwd_fp8(a, m, grid, st);
         default: return (int)cudaErrorInvalidValue;
     }
 }
 
 namespace {
 const char* const kGemmNames[] = {"gemm_l1_fwd", "gemm_l2_fwd", "gemm_l2_dgrad", "gemm_l1_dgrad",
-                                  "gemm_dw1",    "gemm_dw2",    "gemm_dw1_mg",   "gemm_dw2_mg"};
+                                  "gemm_dw1",    "gemm_dw2",    "gemm_dw1_mg",   "gemm_dw2_mg",
+                                  "gemm_l1_fwd_fp8"};
 }  // namespace
 
 int launch_gemm(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
@@ -341,14 +344,18 @@ int moe_router_topk(const moe_shape* shape, const float* logits, int32_t* topk_i
     return MOE_OK;
 }
 
-int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2, const float* topk_w,
-                void* route_ws, void* saved, void* y, void* stream) {
+// Body of moe_forward (x bf16) and of moe_forward_fp8 (x8 E4M3 bytes and
+// xsf UE8M0 scales instead of x).
+static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8, const uint8_t* xsf, const void* W1,
+                        const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream) {
     Ctx c;
     int rc = prepare(shape, &c);
     if (rc) return rc;
-    if (!W1 || !W2 || !route_ws || !saved || (shape->T > 0 && (!x || !topk_w || !y)))
+    const bool fp8 = x8 != nullptr || xsf != nullptr;
+    if (!W1 || !W2 || !route_ws || !saved ||
+        (shape->T > 0 && (!topk_w || !y || (fp8 ? (!x8 || !xsf) : !x))))
         return fail(MOE_EINVAL, "NULL pointer argument");
-    const void* ptrs[] = {x, W1, W2, topk_w, route_ws, saved, y};
+    const void* ptrs[] = {x, x8, xsf, W1, W2, topk_w, route_ws, saved, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
     if ((rc = query_device(&c, route_ws))) return rc;
@@ -373,8 +380,10 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
     g1.K = H;
     g1.n_tiles = cdiv(I, 2 * 64);
     g1.gsrc = static_cast<const __nv_bfloat16*>(x);
+    g1.gsrc8 = x8;
+    g1.gsf = xsf;
     g1.cmask = cmask;
-    int e = launch_gemm(L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
+    int e = launch_gemm(fp8 ? L1_FWD_FP8 : L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
     if (e) return cuda_fail(e, "L1 grouped GEMM launch");
 
     // L2 grouped GEMM + routing-weight epilogue -> o; units of 256 features
@@ -396,6 +405,38 @@ int moe_forward(const moe_shape* shape, const void* x, const void* W1, const voi
                        static_cast<__nv_bfloat16*>(y), c.sms, st);
     trace_post(st, "combine_fwd");
     if (e) return cuda_fail(e, "combine launch");
+    return MOE_OK;
+}
+
+int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2, const float* topk_w,
+                void* route_ws, void* saved, void* y, void* stream) {
+    return forward_impl(shape, x, nullptr, nullptr, W1, W2, topk_w, route_ws, saved, y, stream);
+}
+
+int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const void* W1,
+                    const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream) {
+    if (!x_fp8 || !x_sf) {
+        if (shape && shape->T > 0) return fail(MOE_EINVAL, "NULL pointer argument");
+    }
+    return forward_impl(shape, nullptr, x_fp8, x_sf, W1, W2, topk_w, route_ws, saved, y, stream);
+}
+
+int moe_quantize_fp8(const moe_shape* shape, const void* x, uint8_t* x_fp8, uint8_t* x_sf, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (shape->T > 0 && (!x || !x_fp8 || !x_sf)) return fail(MOE_EINVAL, "NULL pointer argument");
+    const void* ptrs[] = {x, x_fp8, x_sf};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if (shape->T == 0) return MOE_OK;
+    if ((rc = query_device(&c, x))) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    trace_pre(st);
+    const int e = launch_quantize_fp8(static_cast<const __nv_bfloat16*>(x), (long long)shape->T * shape->H, x_fp8,
+                                      x_sf, c.sms, st);
+    trace_post(st, "quantize_fp8");
+    if (e) return cuda_fail(e, "FP8 quantization launch");
     return MOE_OK;
 }
 

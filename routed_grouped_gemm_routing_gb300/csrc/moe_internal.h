@@ -37,7 +37,10 @@ constexpr int kGemmSmemBytes = 1024 + kStages * (kStageABytes + kStageBBytes) + 
 //   DW1       dW1[e] = gather(x)^T . dh        (K = the expert's rows)
 //   DW2       dW2[e] = aw^T . gather(dY)       (K = the expert's rows)
 //   DW1_MG, DW2_MG  the same, added in FP32 to the caller's FP32 main gradient
-enum Flavour : int { L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5, DW1_MG = 6, DW2_MG = 7 };
+//   L1_FWD_FP8  L1_FWD with the gathered rows read as E4M3 + UE8M0 scales
+enum Flavour : int {
+    L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5, DW1_MG = 6, DW2_MG = 7, L1_FWD_FP8 = 8
+};
 
 struct GemmArgs {
     int T, H, I, E, k;
@@ -60,6 +63,8 @@ struct GemmArgs {
     const __nv_bfloat16* h_in;  // saved h (L2_DGRAD epilogue)
     const __nv_bfloat16* a_in;  // saved a (L2_DGRAD epilogue)
     float* outf;                // dw_part (L2_DGRAD epilogue); bf16 outputs leave by TMA store
+    const uint8_t* gsrc8;       // L1_FWD_FP8: E4M3 rows [T, H]
+    const uint8_t* gsf;         // L1_FWD_FP8: UE8M0 scales [T, H / 32]
 };
 
 // Tensor maps of one grouped-GEMM launch: operands A, B (loads), up to two
@@ -90,6 +95,7 @@ int launch_combine(const __nv_bfloat16* rows, const int32_t* inv, int T, int k, 
                    int num_sms, cudaStream_t st);
 int launch_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w, int num_sms,
                        cudaStream_t st);
+int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t* sf, int num_sms, cudaStream_t st);
 int launch_dw_reduce(const float* dw_part, int cols, const int32_t* inv, long long slots, float* out, int num_sms,
                      cudaStream_t st);
 

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace moe {
@@ -308,6 +309,18 @@ __device__ __forceinline__ void stage_row_sw64(uint32_t box, int r, const uint32
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         st_shared_v4(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+}
+
+// 2^(s - 127) for a UE8M0 scale byte s (s = 0: the subnormal 2^-127).
+__device__ __forceinline__ float fp8_scale(uint32_t s) {
+    return s == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+}
+// Two E4M3 bytes (low byte first) times sc, as two bf16 (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+    return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
