@@ -428,6 +428,44 @@ def run_ours(args):
                   "note": "median of 20 runs of moe_router_topk (router kernel + routing prologue) on the "
                           "workload's logits; not part of the layer step"}
 
+    # the FP8-dispatch forward (per-token E4M3 input with UE8M0 scales per 32
+    # elements), timed beside the bf16 forward: a variant, not the layer step
+    fp8 = None
+    if not args.no_fp8:
+        xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
+        xsf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+
+        def fwd_fp8():
+            B.moe_quantize_fp8(ws.shape, inp["x"], xq, xsf)
+            B.moe_forward_fp8(ws.shape, xq, xsf, inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
+
+        def fwd_bf16():
+            B.moe_forward(ws.shape, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
+
+        B.moe_route_prologue(ws.shape, inp["topk_idx"], ws.route)
+        per = {}
+        for name, fn in (("fp8", fwd_fp8), ("bf16", fwd_bf16)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            ftrace = B.KernelTrace(max_launches=8 * 10)
+            with ftrace:
+                for _ in range(10):
+                    fn()
+            torch.cuda.synchronize()
+            kk = {}
+            for kn, d in ftrace.durations_ms():
+                kk.setdefault(kn, []).append(d)
+            per[name] = {kn: statistics.median(v) for kn, v in kk.items()}
+        q_bytes = T * H * 2 + T * H + T * H // 32
+        fp8 = {"forward_ms": sum(per["fp8"].values()), "bf16_forward_ms": sum(per["bf16"].values()),
+               "kernels_ms": per["fp8"], "bf16_kernels_ms": per["bf16"],
+               "quantize_gbs": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9,
+               "quantize_frac_of_hbm": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+               "forward_tflops": 6.0 * H * I * T * k / (sum(per["fp8"].values()) / 1e3) / 1e12,
+               "note": "median of 10 runs of moe_quantize_fp8 + moe_forward_fp8 (and of moe_forward) on the "
+                       "workload; the L1 GEMM gathers E4M3 rows and widens them to bf16; not part of the step"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -467,6 +505,7 @@ def run_ours(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "router": router,
+        "fp8_forward": fp8,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -485,6 +524,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-router", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--activation-clamp", type=float, default=0.0,
                     help="SwiGLU input clamp c > 0 (0: none, the default workload)")
     ap.add_argument("--cpu-tokens", type=int, default=4)

@@ -258,7 +258,11 @@ struct T2<L1_FWD> {
 // one UE8M0 scale per 32 elements and widened to bf16 on the way into
 // shared memory (exact: an E4M3 value times a power of two fits bf16).
 template <>
-struct T2<L1_FWD_FP8> : T2<L1_FWD> {};
+struct T2<L1_FWD_FP8> : T2<L1_FWD> {
+    static constexpr int kStages = 4;
+    static constexpr int kFp8Slots = 4;  // staging ring of raw E4M3 blocks
+    static constexpr int kInBytes = kFp8Slots * (128 * 64 + 128 * 4);
+};
 template <int F>
 __host__ __device__ constexpr bool t2_is_l1() {
     return F == L1_FWD || F == L1_FWD_FP8;
@@ -294,7 +298,9 @@ constexpr int t2_smem_bytes() {
     return 1024 + T2<F>::kStages * (kT2ABytes + kT2BBytes) + kEpiWarps * kStageEpiBytes + T2<F>::kInBytes +
            kT2TailBytes;
 }
-static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448, "shared memory per CTA");
+static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448 &&
+                  t2_smem_bytes<L1_FWD_FP8>() <= 232448,
+              "shared memory per CTA");
 static_assert(T2<L1_FWD>::kProducers == 1 && T2<L2_DGRAD>::kProducers == 1 && T2<L2_FWD>::kProducers <= 1 + kGatherWarps &&
                   T2<L1_DGRAD>::kProducers <= 1 + kGatherWarps,
               "producer warps");
@@ -552,8 +558,8 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
 // 128-byte-swizzled K-major layout; rows past the unit's half are left alone
 // (the MMA reads only n / 2 rows).  Padding rows (perm = -1) are zero-filled.
 template <int F>
-__device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, T2Bars bars, volatile int* abort,
-                               int gw, int lane, int rank) {
+__device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, uint32_t stg, T2Bars bars,
+                               volatile int* abort, int gw, int lane, int rank) {
     const int c = lane & 7;
     const int rb = lane >> 3;
     const int H = p.H;
@@ -575,50 +581,88 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, T2
             tok[q] = r < nh ? (s >= 0 ? s / k : -1) : -2;  // -2: row not in this unit
         }
         if constexpr (F == L1_FWD_FP8) {
-            // register path: the next block's bytes and scales are loaded
-            // while this block is widened and stored
+            // Raw E4M3 blocks (64 bytes per row) and the row's aligned scale
+            // word come into a staging ring by cp.async, kFp8Slots - 1 blocks
+            // ahead; each thread widens the chunks it copied itself (its own
+            // cp.async.wait_group makes them visible) and the quad of a row
+            // shares the scale word after a warp barrier.  Thread (row pair,
+            // c4): rows gw*16 + (lane >> 2) + 8 q, 16-element chunk c4.
+            constexpr int S = T2<F>::kFp8Slots;
+            constexpr uint32_t kSlot = 128 * 64 + 128 * 4;
+            const int c4 = lane & 3;
             const int G = H >> 5;
-            uint2 cur[4], nxt[4];
-            uint32_t cs[4], ns[4];
-            auto load = [&](int kb, uint2 (&d)[4], uint32_t (&sc)[4]) {
+            int tq[2];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int tk = tok[q];
-                    if (tk >= 0) {
-                        d[q] = __ldg(reinterpret_cast<const uint2*>(p.gsrc8 + (size_t)tk * (size_t)H + kb * kBK + c * 8));
-                        sc[q] = __ldg(p.gsf + (size_t)tk * (size_t)G + kb * 2 + (c >> 2));
-                    } else {
-                        d[q] = make_uint2(0u, 0u);
-                        sc[q] = 127u;
+            for (int q = 0; q < 2; ++q) {
+                const int r = gw * 16 + (lane >> 2) + 8 * q;
+                int sl = -1;
+                if (r < nh) sl = __ldg(p.perm + rbase + r);
+                tq[q] = r < nh ? (sl >= 0 ? sl / k : -1) : -2;
+            }
+            auto issue = [&](int kb) {
+                const uint32_t slot = stg + (uint32_t)(kb % S) * kSlot;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int tk = tq[q];
+                    if (tk == -2) continue;
+                    const int r = gw * 16 + (lane >> 2) + 8 * q;
+                    const size_t t0 = (size_t)(tk < 0 ? 0 : tk);
+                    cp_async_16(slot + r * 64 + c4 * 16, p.gsrc8 + t0 * (size_t)H + kb * kBK + c4 * 16,
+                                tk < 0 ? 0u : 16u);
+                    if (c4 == 0) {
+                        // the aligned 4-byte word holding the row's two scales of
+                        // this block (at byte a & 3 = 0 or 2 of it); when they are
+                        // its low half only those 2 bytes are read, so the copy
+                        // never runs past the end of x_sf
+                        const size_t a = t0 * (size_t)G + (size_t)kb * 2;
+                        cp_async_4(slot + 128 * 64 + r * 4, p.gsf + (a & ~(size_t)3),
+                                   tk < 0 ? 0u : ((a & 3) ? 4u : 2u));
                     }
                 }
             };
-            load(0, cur, cs);
+#pragma unroll 1
+            for (int j = 0; j < S - 1; ++j) {
+                if (j < nkb) issue(j);
+                cp_async_commit();
+            }
             for (int kb = 0; kb < nkb; ++kb) {
-                if (kb + 1 < nkb) load(kb + 1, nxt, ns);
+                if (kb + S - 1 < nkb) issue(kb + S - 1);
+                cp_async_commit();
+                cp_async_wait_group<S - 1>();
+                __syncwarp();
                 if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
                 const uint32_t b = sB + stage * kT2BBytes;
+                const uint32_t slot = stg + (uint32_t)(kb % S) * kSlot;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (tok[q] == -2) continue;
-                    const int r = gw * 16 + rb + 4 * q;
-                    const float sc = fp8_scale(cs[q]);
-                    st_shared_v4(b + r * 128 + ((c ^ (r & 7)) << 4), e4m3x2_to_bf16x2(cur[q].x & 0xffffu, sc),
-                                 e4m3x2_to_bf16x2(cur[q].x >> 16, sc), e4m3x2_to_bf16x2(cur[q].y & 0xffffu, sc),
-                                 e4m3x2_to_bf16x2(cur[q].y >> 16, sc));
+                for (int q = 0; q < 2; ++q) {
+                    const int tk = tq[q];
+                    if (tk == -2) continue;
+                    const int r = gw * 16 + (lane >> 2) + 8 * q;
+                    const int4 raw = ld_shared_v4s(slot + r * 64 + c4 * 16);
+                    uint32_t word;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(word) : "r"(slot + 128 * 64 + r * 4) : "memory");
+                    // this chunk's group is kb * 2 + c4 / 2: its byte inside the aligned word
+                    const size_t a = (size_t)(tk < 0 ? 0 : tk) * (size_t)G + (size_t)kb * 2 + (size_t)(c4 >> 1);
+                    const float sc = fp8_scale((word >> (8 * (uint32_t)(a & 3))) & 0xffu);
+                    const uint32_t w0 = (uint32_t)raw.x, w1 = (uint32_t)raw.y, w2 = (uint32_t)raw.z, w3 = (uint32_t)raw.w;
+                    const uint32_t row = b + r * 128;
+                    const uint32_t sw = (uint32_t)(r & 7);
+                    st_shared_v4(row + (((uint32_t)(2 * c4) ^ sw) << 4), e4m3x2_to_bf16x2(w0 & 0xffffu, sc),
+                                 e4m3x2_to_bf16x2(w0 >> 16, sc), e4m3x2_to_bf16x2(w1 & 0xffffu, sc),
+                                 e4m3x2_to_bf16x2(w1 >> 16, sc));
+                    st_shared_v4(row + (((uint32_t)(2 * c4 + 1) ^ sw) << 4), e4m3x2_to_bf16x2(w2 & 0xffffu, sc),
+                                 e4m3x2_to_bf16x2(w2 >> 16, sc), e4m3x2_to_bf16x2(w3 & 0xffffu, sc),
+                                 e4m3x2_to_bf16x2(w3 >> 16, sc));
                 }
                 fence_proxy_async_smem();  // generic-proxy stores, read by the tensor core
                 mbar_arrive(bars.full(stage));
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    cur[q] = nxt[q];
-                    cs[q] = ns[q];
-                }
+                __syncwarp();  // the slot's scale words are read before it is refilled
                 if (++stage == T2<F>::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
+            cp_async_wait_group<0>();
         } else {
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
@@ -999,7 +1043,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     } else if (warp == kWarpSched) {
         if (lane == 0 && rank == 0) t2_role_sched<F>(p, ring, bars, abort);
     } else if (warp >= kWarpGather0) {
-        if constexpr (T2<F>::kGather) t2_role_gather<F>(p, ring, sB, bars, abort, warp - kWarpGather0, lane, rank);
+        if constexpr (T2<F>::kGather) t2_role_gather<F>(p, ring, sB, sIn, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
         if (rank == 0) {
