@@ -326,6 +326,9 @@ def run_ours(args):
     launches_per_step = trace.count / args.steps
     kernels = {n: {"launches": len(v), "avg_ms": statistics.mean(v), "total_ms": sum(v),
                    "share": sum(v) / ms} for n, v in per.items()}
+    fwd_names = ("route_hist", "route_scan", "route_place", "gemm_l1_fwd", "gemm_l2_fwd", "combine_fwd")
+    forward_ms = sum(v["avg_ms"] for n, v in kernels.items() if n in fwd_names)
+    backward_ms = sum(v["avg_ms"] for n, v in kernels.items() if n not in fwd_names)
     gemms = {n: v for n, v in kernels.items() if n in GEMM_FLOP_FACTOR}
     dom = max(gemms, key=lambda n: gemms[n]["total_ms"])
     dom_flops = GEMM_FLOP_FACTOR[dom] * H * I * shape.slots
@@ -357,6 +360,33 @@ def run_ours(args):
     roofline.update({"algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
                      "arithmetic_intensity": dom_flops / dom_bytes, "ridge_flop_per_byte": ridge,
                      "achieved_tflops": dom_flops / dom_s / 1e12, "achieved_gbs": dom_bytes / dom_s / 1e9})
+
+    # the same step captured once in a CUDA graph and replayed (every launch
+    # of the step is capturable: no host synchronisation, no allocation)
+    graph = None
+    if not args.no_graph:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            step()
+        torch.cuda.current_stream().wait_stream(gs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record()
+        for _ in range(args.steps):
+            g.replay()
+        gb.record()
+        torch.cuda.synchronize()
+        gms = ga.elapsed_time(gb) / args.steps
+        graph = {"ms_per_step": gms, "value": flops_step / (gms / 1e3) / 1e12, "unit": "TFLOP/s",
+                 "note": "the prologue + forward + backward step captured once and replayed"}
+        del g
 
     # end to end through the public API, from pinned host buffers
     e2e = None
@@ -482,7 +512,9 @@ def run_ours(args):
         dt = time.perf_counter() - t0
         cpu = {"value": flops * reps / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                "host_cores_available": cpu_cores(), "kind": "oracle", "sample": f"{reps} x ({desc})",
-               "seconds": dt}
+               "seconds": dt,
+               "extrapolated_full_step_s": flops_step / (flops * reps / dt),
+               "extrapolated_note": "the whole layer step at the sample's FLOP rate (extrapolated, not run)"}
 
     if rank != 0:
         dist.destroy_process_group()
@@ -490,7 +522,8 @@ def run_ours(args):
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms / args.steps, "forward_ms": forward_ms, "backward_ms": backward_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded Gaussian inputs and weights, Gaussian-logit top-k routing)",
         "config": config_dict(shape, world, args.activation_clamp),
         "routed_tokens_per_s": tok_s,
@@ -503,6 +536,7 @@ def run_ours(args):
         "kernels": kernels,
         "roofline": roofline,
         "e2e": e2e,
+        "graph": graph,
         "cpu_baseline": cpu,
         "router": router,
         "fp8_forward": fp8,
@@ -525,6 +559,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-router", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--activation-clamp", type=float, default=0.0,
                     help="SwiGLU input clamp c > 0 (0: none, the default workload)")
     ap.add_argument("--cpu-tokens", type=int, default=4)
