@@ -10,15 +10,12 @@
 
 namespace moe {
 
-// Weight-gradient tile: 128 x 256 of dW[e], 64 routed rows of K per stage (the
-// row-grouped SM-pair kernels use the same 64-deep K blocks).
+// Tile sizes of the SM-pair GEMMs: 128 TMEM lanes (output rows or features)
+// per CTA, accumulators of up to 256 columns, 64-deep K blocks.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kStageABytes = kBM * kBK * 2;  // 16 KiB
-constexpr int kStageBBytes = kBN * kBK * 2;  // 32 KiB
-constexpr int kGatherWarps = 8;             // warps issuing the cp.async row gathers
+constexpr int kGatherWarps = 8;  // warps issuing the cp.async row gathers
 // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer, 6.. gather producers
 constexpr int kWarpTma = 4;
 constexpr int kWarpMma = 5;
@@ -27,7 +24,6 @@ constexpr int kGemmThreads = 32 * (kWarpGather0 + kGatherWarps);
 constexpr int kMaxDevices = 64;
 constexpr int kEpiWarps = 4;
 constexpr int kStageEpiBytes = 8192;  // per epilogue warp: TMA-store staging
-constexpr int kGemmSmemBytes = 1024 + kStages * (kStageABytes + kStageBBytes) + kEpiWarps * kStageEpiBytes + 256;
 
 // The six grouped GEMMs of the layer.
 //   L1_FWD    h = gather(x) . W1[e]            + SwiGLU epilogue -> h, a

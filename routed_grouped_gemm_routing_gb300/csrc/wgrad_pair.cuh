@@ -16,7 +16,7 @@
 //   dW1: A = slab (M = H features), B = dh (N = 2I features)
 //   dW2: A = aw   (M = I features), B = slab (N = H features)
 // so each CTA's TMEM holds 128 output rows x 256 output columns of dW[e]
-// and leaves through the same TMA-store epilogue as the one-SM tiles.
+// and leaves through a TMA-store epilogue (32-row boxes of 64 columns).
 // The token operand is gathered once per unit instead of once per output
 // tile (16x fewer gathered bytes for dW1, 8x for dW2), and each SM streams
 // 16 KiB per K block instead of 48 KiB.
