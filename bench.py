@@ -54,6 +54,25 @@ def gemm_alg_bytes(name: str, T: int, H: int, I: int, E: int, k: int) -> float:
     }[name]
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over the ranks (the job takes as long as its
+    slowest replica); x itself with one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job rate: the units every rank processed in `steps` steps over
+    the job's time (the maximum over ranks), per second."""
+    return world * units_per_rank_step * steps / (ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -305,19 +324,14 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     status = B.moe_read_status(s, ws.route)
     if status[B.STATUS_FLAGS] != 0:
         raise RuntimeError(f"kernel status flags {status[B.STATUS_FLAGS]:#x} in the timed region")
 
     flops_step = shape.flops_forward() + shape.flops_backward()
-    secs = ms / 1e3
-    value = world * flops_step * args.steps / secs / 1e12
-    tok_s = world * shape.slots * args.steps / secs
+    value = job_rate(flops_step, args.steps, world, ms) / 1e12
+    tok_s = job_rate(shape.slots, args.steps, world, ms)
 
     # per-kernel device times (rank-local)
     per = {}
@@ -415,14 +429,10 @@ def run_ours(args):
         pipe.synchronize()
         b.record(pipe.compute)
         torch.cuda.synchronize()
-        ems = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(a.elapsed_time(b), world, dev)
         h2d = sum(host[n].numel() * host[n].element_size() for n in host)
         d2h = sum(outs[n].numel() * outs[n].element_size() for n in ("y_h", "dx_h", "dw_h"))
-        e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_rate(flops_step, args.steps, world, ems) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps,
                "note": "x, topk_idx, topk_weights, dY copied in from pinned host memory and y, dx, "
                        "d topk_weights copied out every step (HostPipeline: uploads of step n+1 and downloads "
