@@ -54,7 +54,7 @@ constexpr int kT2ABytes = 128 * kBK * 2;  // this CTA's 128 features x 64 of K
 constexpr int kT2BBytes = 128 * kBK * 2;  // up to 128 routed rows x 64 of K
 constexpr int kT2InBytes = 3 * 2048;      // L2 dgrad epilogue inputs per warp: h gate, h up, a boxes
 constexpr int kUR = 4;                    // slots of the unit ring
-constexpr int kT2NumBars = 2 * kT2Stages + 9 + kEpiWarps + 2 * kUR + 1;
+constexpr int kT2NumBars = 2 * kT2Stages + 9 + 2 * kEpiWarps + 2 * kUR + 1;
 constexpr int kT2TailBytes = 512;         // barriers, TMEM address, abort flag, unit ring
 constexpr int kT2RingOff = (8 * kT2NumBars + 8 + 15) & ~15;
 static_assert(kT2RingOff + 16 * kUR <= kT2TailBytes, "barrier area");
@@ -80,6 +80,10 @@ struct T2Bars {
         return base + 8u * (2 * kT2Stages + 9 + kEpiWarps + kUR + i);
     }
     __device__ __forceinline__ uint32_t ustart() const { return base + 8u * (2 * kT2Stages + 9 + kEpiWarps + 2 * kUR); }
+    // L2 dgrad epilogue: the input boxes of warp w's buffer b have landed
+    __device__ __forceinline__ uint32_t ein(int w, uint32_t b) const {
+        return b == 0 ? ein(w) : base + 8u * (2 * kT2Stages + 9 + kEpiWarps + 2 * kUR + 1 + w);
+    }
 };
 
 // ------------------------------------------------------- cluster helpers
@@ -780,11 +784,15 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if constexpr (F == L2_DGRAD) {
             if (lane == 0 && t.f0 + 32 * warp < p.I) {
-                const uint32_t eb = bars.ein(warp);
+                // the unit's first chunk, into buffer nin & 1, whose last
+                // stores (chunk nin - 2) must have read it
+                bulk_wait_read<1>();
+                const uint32_t cur = (nin & 1u) ? stage : in_box;
+                const uint32_t eb = bars.ein(warp, nin & 1u);
                 mbar_arrive_expect_tx(eb, (uint32_t)kT2InBytes);
-                tma_load_2d(in_box, mapH, t.f0 + 32 * warp, t.r0, eb);
-                tma_load_2d(in_box + 2048, mapH, p.I + t.f0 + 32 * warp, t.r0, eb);
-                tma_load_2d(in_box + 4096, mapAs, t.f0 + 32 * warp, t.r0, eb);
+                tma_load_2d(cur, mapH, t.f0 + 32 * warp, t.r0, eb);
+                tma_load_2d(cur + 2048, mapH, p.I + t.f0 + 32 * warp, t.r0, eb);
+                tma_load_2d(cur + 4096, mapAs, t.f0 + 32 * warp, t.r0, eb);
             }
         }
         if (!warp_wait(bars.tfull(acc), acc_phase, abort)) break;
@@ -879,60 +887,65 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                 ++xchunk;
             } else if constexpr (F == L2_DGRAD) {
                 // g = dY . W2^T; da = w g; SwiGLU^T from the saved h; aw = w a;
-                // d(topk weight) partial = sum over this warp's features of g a
+                // d(topk weight) partial = sum over this warp's features of g a.
+                // Chunk nin (counted over the launch) has its saved h and a
+                // boxes in buffer nin & 1 (in_box or stage) and overwrites
+                // them in place with its three output boxes; the next chunk's
+                // inputs come into the other buffer meanwhile.
                 const int I = p.I;
                 const int col = t.f0 + 32 * warp;
-                const bool colok = col < I;
-                const int sl = __ldg(p.perm + row0 + lane);
-                const float wl = sl >= 0 ? __ldg(p.topk_w + sl) : 0.0f;
-                if (colok) {
-                    if (!warp_wait(bars.ein(warp), nin & 1u, abort)) {
+                if (col < I) {
+                    const int sl = __ldg(p.perm + row0 + lane);
+                    const float wl = sl >= 0 ? __ldg(p.topk_w + sl) : 0.0f;
+                    const uint32_t cur = (nin & 1u) ? stage : in_box;
+                    if (lane == 0 && c32 + 1 < (t.n >> 5)) {
+                        bulk_wait_read<0>();  // the other buffer's stores (previous chunk) have read it
+                        const uint32_t nxt = (nin & 1u) ? in_box : stage;
+                        const uint32_t eb = bars.ein(warp, (nin + 1u) & 1u);
+                        mbar_arrive_expect_tx(eb, (uint32_t)kT2InBytes);
+                        tma_load_2d(nxt, mapH, col, row0 + 32, eb);
+                        tma_load_2d(nxt + 2048, mapH, I + col, row0 + 32, eb);
+                        tma_load_2d(nxt + 4096, mapAs, col, row0 + 32, eb);
+                    }
+                    if (!warp_wait(bars.ein(warp, nin & 1u), (nin >> 1) & 1u, abort)) {
                         ok = false;
                         break;
                     }
-                    ++nin;
-                }
-                {
-                    float prod[32];
+                    {
+                        float prod[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) prod[j] = colok ? v[j] * lds_sw64(in_box + 4096, j, lane) : 0.0f;
-                    // lane j ends with the sum over the warp's 32 features of row j
-                    transpose_reduce_step<16>(prod, lane);
-                    transpose_reduce_step<8>(prod, lane);
-                    transpose_reduce_step<4>(prod, lane);
-                    transpose_reduce_step<2>(prod, lane);
-                    transpose_reduce_step<1>(prod, lane);
-                    if (colok) p.outf[(size_t)(row0 + lane) * (size_t)p.dw_cols + (size_t)(col >> 5)] = prod[0];
-                }
-                if (lane == 0) bulk_wait_read<0>();
-                __syncwarp();
-                // the forward's clamp decisions of this warp's features: lane
-                // l loads the words of row row0 + l, row j's are shuffled out
-                uint32_t gmask = 0xffffffffu, umask = 0xffffffffu;
-                if (p.clamp < INFINITY && colok) {
-                    const size_t words = (size_t)(2 * I / 32);
-                    gmask = __ldg(p.cmask + (size_t)(row0 + lane) * words + (size_t)(col / 32));
-                    umask = __ldg(p.cmask + (size_t)(row0 + lane) * words + (size_t)((I + col) / 32));
-                }
-                if (p.clamp < INFINITY)
-                    swiglu_t_chunk<true>(stage, in_box, colok, lane, wl, v, p.clamp, gmask, umask);
-                else
-                    swiglu_t_chunk<false>(stage, in_box, colok, lane, wl, v, p.clamp, gmask, umask);
-                // the input boxes are consumed: bring in the next chunk's
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && colok) {
-                    if (c32 + 1 < (t.n >> 5)) {
-                        const uint32_t eb = bars.ein(warp);
-                        mbar_arrive_expect_tx(eb, (uint32_t)kT2InBytes);
-                        tma_load_2d(in_box, mapH, col, row0 + 32, eb);
-                        tma_load_2d(in_box + 2048, mapH, I + col, row0 + 32, eb);
-                        tma_load_2d(in_box + 4096, mapAs, col, row0 + 32, eb);
+                        for (int j = 0; j < 32; ++j) prod[j] = v[j] * lds_sw64(cur + 4096, j, lane);
+                        // lane j ends with the sum over the warp's 32 features of row j
+                        transpose_reduce_step<16>(prod, lane);
+                        transpose_reduce_step<8>(prod, lane);
+                        transpose_reduce_step<4>(prod, lane);
+                        transpose_reduce_step<2>(prod, lane);
+                        transpose_reduce_step<1>(prod, lane);
+                        p.outf[(size_t)(row0 + lane) * (size_t)p.dw_cols + (size_t)(col >> 5)] = prod[0];
                     }
-                    tma_store_2d(om.c0, col, row0, stage);
-                    tma_store_2d(om.c0, I + col, row0, stage + 2048);
-                    tma_store_2d(om.c1, col, row0, stage + 4096);
-                    bulk_commit();
+                    // the forward's clamp decisions of this warp's features: lane
+                    // l loads the words of row row0 + l, row j's are shuffled out
+                    uint32_t gmask = 0xffffffffu, umask = 0xffffffffu;
+                    if (p.clamp < INFINITY) {
+                        const size_t words = (size_t)(2 * I / 32);
+                        gmask = __ldg(p.cmask + (size_t)(row0 + lane) * words + (size_t)(col / 32));
+                        umask = __ldg(p.cmask + (size_t)(row0 + lane) * words + (size_t)((I + col) / 32));
+                    }
+                    // element (row j, feature lane) of each box is read, then
+                    // overwritten, by this lane only: in place is safe
+                    if (p.clamp < INFINITY)
+                        swiglu_t_chunk<true>(cur, cur, true, lane, wl, v, p.clamp, gmask, umask);
+                    else
+                        swiglu_t_chunk<false>(cur, cur, true, lane, wl, v, p.clamp, gmask, umask);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(om.c0, col, row0, cur);
+                        tma_store_2d(om.c0, I + col, row0, cur + 2048);
+                        tma_store_2d(om.c1, col, row0, cur + 4096);
+                        bulk_commit();
+                    }
+                    ++nin;
                 }
             } else {
                 // one output: o = w (a . W2) (L2 forward) or dxp = dh . W1^T (L1 dgrad)
@@ -1003,7 +1016,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             mbar_init(bars.xempty(a), 1);
         }
         mbar_init(bars.drain(), 1);
-        for (int w = 0; w < kEpiWarps; ++w) mbar_init(bars.ein(w), 1);
+        for (int w = 0; w < kEpiWarps; ++w) {
+            mbar_init(bars.ein(w, 0), 1);
+            mbar_init(bars.ein(w, 1), 1);
+        }
         // consumers of a published unit: TMA producers, MMA or relay,
         // epilogue warps and (gathering flavours) gather warps, in both CTAs
         const uint32_t consumers =
