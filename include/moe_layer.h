@@ -192,6 +192,13 @@ int moe_quantize_fp8(const moe_shape* shape, const void* x, uint8_t* x_fp8, uint
 int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const void* W1,
                     const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream);
 
+/* The inverse of moe_quantize_fp8: x_out bf16[T,H] = decode(x_fp8) *
+ * 2^(x_sf - 127), exactly (every such value is a bf16 value).  The backward
+ * of an FP8-dispatched forward is moe_backward with x = this dequantized
+ * input (the input the forward actually multiplied).  Errors as for
+ * moe_quantize_fp8. */
+int moe_dequantize_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, void* x_out, void* stream);
+
 /* moe_backward with FP32 main-gradient accumulation, for training loops that
  * sum weight gradients over micro-batches in FP32 buffers.  The pages have no
  * counterpart: an addition of this library next to their backward (Mega MoE

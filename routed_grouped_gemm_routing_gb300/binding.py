@@ -69,10 +69,11 @@ def lib():
             L.moe_backward.argtypes = [P(MoeShape)] + [vp] * 13
             L.moe_backward_main_grad.argtypes = [P(MoeShape)] + [vp] * 13
             L.moe_quantize_fp8.argtypes = [P(MoeShape)] + [vp] * 4
+            L.moe_dequantize_fp8.argtypes = [P(MoeShape)] + [vp] * 4
             L.moe_forward_fp8.argtypes = [P(MoeShape)] + [vp] * 9
             L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
             for n in ("moe_workspace_layout", "moe_route_prologue", "moe_router_topk", "moe_forward", "moe_backward", "moe_backward_main_grad",
-                      "moe_quantize_fp8", "moe_forward_fp8",
+                      "moe_quantize_fp8", "moe_dequantize_fp8", "moe_forward_fp8",
                       "moe_read_status"):
                 getattr(L, n).restype = ctypes.c_int
             L.moe_trace_begin.argtypes = [vp, ctypes.c_int]
@@ -173,6 +174,14 @@ def moe_quantize_fp8(shape: MoeShape, x, x_fp8, x_sf, stream=None):
     _check(lib().moe_quantize_fp8(ctypes.byref(shape), _ptr(x, torch.bfloat16, T * H, "x"),
                                   _ptr(x_fp8, torch.uint8, T * H, "x_fp8"), _ptr(x_sf, torch.uint8, T * H // 32, "x_sf"),
                                   _stream(stream)))
+
+
+def moe_dequantize_fp8(shape: MoeShape, x_fp8, x_sf, x_out, stream=None):
+    """x_out bf16 [T, H] = decode(x_fp8) * 2^(x_sf - 127) (exact)."""
+    T, H = shape.T, shape.H
+    _check(lib().moe_dequantize_fp8(ctypes.byref(shape), _ptr(x_fp8, torch.uint8, T * H, "x_fp8"),
+                                    _ptr(x_sf, torch.uint8, T * H // 32, "x_sf"),
+                                    _ptr(x_out, torch.bfloat16, T * H, "x_out"), _stream(stream)))
 
 
 def moe_forward_fp8(shape: MoeShape, x_fp8, x_sf, W1, W2, topk_w, route_ws, saved, y, stream=None):

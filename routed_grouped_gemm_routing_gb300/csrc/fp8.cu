@@ -61,7 +61,36 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* 
     }
 }
 
+// The inverse: x_out[i] = decode(q[i]) * 2^(sf[g] - 127) as bf16 (exact), one
+// thread per 8 elements.
+__global__ void __launch_bounds__(256) dequantize_fp8_kernel(const uint8_t* __restrict__ q,
+                                                             const uint8_t* __restrict__ sf, long long n,
+                                                             __nv_bfloat16* __restrict__ out) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i * 8 < n; i += stride) {
+        const long long e0 = i * 8;
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + e0));
+        const float sc = fp8_scale(__ldg(sf + (e0 >> 5)));
+        uint4 o;
+        o.x = e4m3x2_to_bf16x2(raw.x & 0xffffu, sc);
+        o.y = e4m3x2_to_bf16x2(raw.x >> 16, sc);
+        o.z = e4m3x2_to_bf16x2(raw.y & 0xffffu, sc);
+        o.w = e4m3x2_to_bf16x2(raw.y >> 16, sc);
+        *reinterpret_cast<uint4*>(out + e0) = o;
+    }
+}
+
 }  // namespace
+
+int launch_dequantize_fp8(const uint8_t* q, const uint8_t* sf, long long n, __nv_bfloat16* out, int num_sms,
+                          cudaStream_t st) {
+    if (n <= 0) return 0;
+    long long blocks = (n / 8 + 255) / 256;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    dequantize_fp8_kernel<<<(unsigned)blocks, 256, 0, st>>>(q, sf, n, out);
+    return (int)cudaGetLastError();
+}
 
 int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t* sf, int num_sms, cudaStream_t st) {
     if (n <= 0) return 0;

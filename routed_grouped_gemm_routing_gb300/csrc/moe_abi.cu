@@ -421,6 +421,25 @@ int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t*
     return forward_impl(shape, nullptr, x_fp8, x_sf, W1, W2, topk_w, route_ws, saved, y, stream);
 }
 
+int moe_dequantize_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, void* x_out, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (shape->T > 0 && (!x_fp8 || !x_sf || !x_out)) return fail(MOE_EINVAL, "NULL pointer argument");
+    const void* ptrs[] = {x_fp8, x_sf, x_out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if (shape->T == 0) return MOE_OK;
+    if ((rc = query_device(&c, x_out))) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    trace_pre(st);
+    const int e = launch_dequantize_fp8(x_fp8, x_sf, (long long)shape->T * shape->H,
+                                        static_cast<__nv_bfloat16*>(x_out), c.sms, st);
+    trace_post(st, "dequantize_fp8");
+    if (e) return cuda_fail(e, "FP8 dequantization launch");
+    return MOE_OK;
+}
+
 int moe_quantize_fp8(const moe_shape* shape, const void* x, uint8_t* x_fp8, uint8_t* x_sf, void* stream) {
     Ctx c;
     int rc = prepare(shape, &c);

@@ -92,6 +92,8 @@ int launch_combine(const __nv_bfloat16* rows, const int32_t* inv, int T, int k, 
 int launch_router_topk(const float* logits, int T, int E, int k, int32_t* topk_idx, float* topk_w, int num_sms,
                        cudaStream_t st);
 int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t* sf, int num_sms, cudaStream_t st);
+int launch_dequantize_fp8(const uint8_t* q, const uint8_t* sf, long long n, __nv_bfloat16* out, int num_sms,
+                          cudaStream_t st);
 int launch_dw_reduce(const float* dw_part, int cols, const int32_t* inv, long long slots, float* out, int num_sms,
                      cudaStream_t st);
 

@@ -4,7 +4,10 @@
   oracle's per-token quantization (integer output: exact bar);
 * moe_forward_fp8: y within the comparison bar of the oracle's forward on the
   dequantized input, and bit for bit equal to moe_forward run on that
-  dequantized input in bf16 (the widened shared-memory operand is the same)."""
+  dequantized input in bf16 (the widened shared-memory operand is the same);
+* moe_dequantize_fp8 bit-exact against the oracle's dequantization, and the
+  FP8 training step (quantize, FP8 forward, dequantize, backward) equal to
+  the bf16 layer on the dequantized input."""
 import numpy as np
 import pytest
 import torch
@@ -93,3 +96,37 @@ def test_forward_fp8_parity(T, H, I, E, k, seed):
     err = np.abs(xd.float().cpu().numpy() - xf)
     assert np.all(err <= np.abs(xf) * 2.0 ** -4 + 1e-30 + np.repeat(
         np.ldexp(1.0, sf.cpu().numpy().astype(np.int64) - 127), 32, axis=1) * 2.0 ** -10)
+
+
+@pytest.mark.parametrize("T,H", [(257, 512), (64, 7168)])
+def test_dequantize_bit_exact(T, H):
+    shape = B.shape_of(T, H, 64, 4, 2)
+    x = _x_with_ranges(T, H, seed=3 * T + H)
+    q, sf = _quantize_gpu(shape, x.cuda())
+    out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.moe_dequantize_fp8(shape, q, sf, out)
+    torch.cuda.synchronize()
+    ref = _dequantized_bf16(q.cpu().numpy(), sf.cpu().numpy())
+    assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_fp8_training_step_equals_bf16_on_the_dequantized_input():
+    """quantize -> forward_fp8 -> dequantize -> backward gives, bit for bit,
+    the bf16 layer's forward and backward on the dequantized input."""
+    T, H, I, E, k = 300, 256, 192, 6, 3
+    shape = LayerShape("fp8train", T=T, H=H, I=I, E=E, k=k)
+    inp = {n: v.cuda() for n, v in make_layer_inputs(shape, seed=44, device="cpu").items()}
+    s = B.shape_of(T, H, I, E, k)
+    q, sf = _quantize_gpu(s, inp["x"])
+    run = GpuRun(T, H, I, E, k)
+    B.moe_route_prologue(run.shape, inp["topk_idx"], run.route)
+    B.moe_forward_fp8(run.shape, q, sf, inp["W1"], inp["W2"], inp["topk_w"], run.route, run.saved, run.y)
+    xd = torch.empty_like(inp["x"])
+    B.moe_dequantize_fp8(run.shape, q, sf, xd)
+    B.moe_backward(run.shape, inp["dY"], xd, inp["W1"], inp["W2"], inp["topk_w"], run.route, run.saved, run.bwd,
+                   run.dx, run.dW1, run.dW2, run.dw)
+    ref = GpuRun(T, H, I, E, k)
+    ref.run(dict(inp, x=xd))
+    torch.cuda.synchronize()
+    for a, b in ((run.y, ref.y), (run.dx, ref.dx), (run.dW1, ref.dW1), (run.dW2, ref.dW2), (run.dw, ref.dw)):
+        assert torch.equal(a, b)
