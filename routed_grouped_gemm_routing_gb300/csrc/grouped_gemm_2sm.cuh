@@ -256,6 +256,7 @@ struct T2<L1_FWD> {
     static constexpr int kFeatPerCta = 64;  // 64 gate + 64 up features
     static constexpr int kStages = 6;
     static constexpr int kProducers = 1;  // TMA producer threads (one TMA issue stream each)
+    static constexpr int kEpiHalves = 1;  // epilogue warps per TMEM lane quadrant
     static constexpr int kInBytes = 0;
 };
 // FP8 dispatch: the same GEMM, its gathered rows read as E4M3 bytes with
@@ -278,6 +279,9 @@ struct T2<L2_FWD> {
     static constexpr int kFeatPerCta = 128;
     static constexpr int kStages = 6;
     static constexpr int kProducers = 4;  // TMA producer threads (one TMA issue stream each)
+    // its units are short (K = I): a second set of epilogue warps (free
+    // gather warps) takes every other 32-row chunk
+    static constexpr int kEpiHalves = 2;
     static constexpr int kInBytes = 0;
 };
 template <>
@@ -286,6 +290,7 @@ struct T2<L2_DGRAD> {
     static constexpr int kFeatPerCta = 128;
     static constexpr int kStages = 5;
     static constexpr int kProducers = 1;  // TMA producer threads (one TMA issue stream each)
+    static constexpr int kEpiHalves = 1;  // epilogue warps per TMEM lane quadrant
     static constexpr int kInBytes = kEpiWarps * kT2InBytes;
 };
 template <>
@@ -294,6 +299,7 @@ struct T2<L1_DGRAD> {
     static constexpr int kFeatPerCta = 128;
     static constexpr int kStages = 6;
     static constexpr int kProducers = 4;  // TMA producer threads (one TMA issue stream each)
+    static constexpr int kEpiHalves = 1;
     static constexpr int kInBytes = 0;
 };
 
@@ -305,6 +311,9 @@ constexpr int t2_smem_bytes() {
 static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448 &&
                   t2_smem_bytes<L1_FWD_FP8>() <= 232448,
               "shared memory per CTA");
+static_assert(T2<L2_FWD>::kProducers - 1 + kEpiWarps * (T2<L2_FWD>::kEpiHalves - 1) <= kGatherWarps &&
+                  T2<L1_DGRAD>::kEpiHalves == 1 && T2<L1_FWD>::kEpiHalves == 1 && T2<L2_DGRAD>::kEpiHalves == 1,
+              "free gather warps");
 static_assert(T2<L1_FWD>::kProducers == 1 && T2<L2_DGRAD>::kProducers == 1 && T2<L2_FWD>::kProducers <= 1 + kGatherWarps &&
                   T2<L1_DGRAD>::kProducers <= 1 + kGatherWarps,
               "producer warps");
@@ -772,7 +781,7 @@ __device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
 template <int F>
 __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMap* mapH, const CUtensorMap* mapAs,
                                  uint32_t ring, T2Bars bars, uint32_t tmem_base, uint32_t stage, uint32_t stage_of_warp0,
-                                 uint32_t in_box, volatile int* abort, int warp, int lane, int rank) {
+                                 uint32_t in_box, volatile int* abort, int warp, int lane, int rank, int half) {
     const uint32_t tempty_leader[2] = {cluster_addr_of(bars.tempty(0), 0), cluster_addr_of(bars.tempty(1), 0)};
     int it = 0;
     uint32_t nstore = 0;
@@ -800,7 +809,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
         const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
 #pragma unroll 1
-        for (int c32 = 0; c32 < (t.n >> 5) && ok; ++c32) {
+        for (int c32 = half; c32 < (t.n >> 5) && ok; c32 += T2<F>::kEpiHalves) {
             const int row0 = t.r0 + 32 * c32;
             float v[32];
             tmem_ld32(tacc + 32 * c32, v);
@@ -1011,7 +1020,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bars.tfull(a), 1);
-            mbar_init(bars.tempty(a), 2 * kEpiWarps);
+            mbar_init(bars.tempty(a), 2 * kEpiWarps * T2<F>::kEpiHalves);
             mbar_init(bars.xfull(a), 1);
             mbar_init(bars.xempty(a), 1);
         }
@@ -1023,7 +1032,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         // consumers of a published unit: TMA producers, MMA or relay,
         // epilogue warps and (gathering flavours) gather warps, in both CTAs
         const uint32_t consumers =
-            2u * (1u + (uint32_t)T2<F>::kProducers + kEpiWarps + (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u));
+            2u * (1u + (uint32_t)T2<F>::kProducers + kEpiWarps * (uint32_t)T2<F>::kEpiHalves +
+                  (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u));
         for (int i = 0; i < kUR; ++i) {
             mbar_init(bars.ufull(i), 1);
             mbar_init(bars.uempty(i), consumers);
@@ -1058,6 +1068,13 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, bars, abort, rank, pid);
     } else if (warp == kWarpSched) {
         if (lane == 0 && rank == 0) t2_role_sched<F>(p, ring, bars, abort);
+    } else if (T2<F>::kEpiHalves > 1 && warp >= kWarpGather0 + T2<F>::kProducers - 1 &&
+               warp < kWarpGather0 + T2<F>::kProducers - 1 + kEpiWarps) {
+        // second epilogue warp of TMEM lane quadrant warp % 4: the odd
+        // chunks, staged in the upper half of that quadrant's buffer
+        const int q = warp & 3;
+        t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, ring, bars, tmem_base,
+                            sStage + q * kStageEpiBytes + 4096, sStage, sIn + q * kT2InBytes, abort, q, lane, rank, 1);
     } else if (warp >= kWarpGather0) {
         if constexpr (T2<F>::kGather) t2_role_gather<F>(p, ring, sB, sIn, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
@@ -1079,7 +1096,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         }
     } else {
         t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, ring, bars, tmem_base,
-                            sStage + warp * kStageEpiBytes, sStage, sIn + warp * kT2InBytes, abort, warp, lane, rank);
+                            sStage + warp * kStageEpiBytes, sStage, sIn + warp * kT2InBytes, abort, warp, lane, rank,
+                            0);
     }
     if (pid >= 0 && lane == 0 && *abort) {
         // bulk copies already issued land within microseconds; give them time
