@@ -314,6 +314,17 @@ static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 
 static_assert(T2<L2_FWD>::kProducers - 1 + kEpiWarps * (T2<L2_FWD>::kEpiHalves - 1) <= kGatherWarps &&
                   T2<L1_DGRAD>::kEpiHalves == 1 && T2<L1_FWD>::kEpiHalves == 1 && T2<L2_DGRAD>::kEpiHalves == 1,
               "free gather warps");
+// A producer waits on the empty barrier of its block's stage by parity; the
+// wait is unambiguous only if that barrier is at most one phase behind, which
+// the producer's own previous block (kProducers earlier) guarantees only
+// when kProducers <= kStages.
+template <int F>
+constexpr bool t2_producers_ok() {
+    return T2<F>::kProducers <= T2<F>::kStages;
+}
+static_assert(t2_producers_ok<L1_FWD>() && t2_producers_ok<L2_FWD>() && t2_producers_ok<L2_DGRAD>() &&
+                  t2_producers_ok<L1_DGRAD>() && t2_producers_ok<L1_FWD_FP8>(),
+              "round-robin producers within the ring depth");
 static_assert(T2<L1_FWD>::kProducers == 1 && T2<L2_DGRAD>::kProducers == 1 && T2<L2_FWD>::kProducers <= 1 + kGatherWarps &&
                   T2<L1_DGRAD>::kProducers <= 1 + kGatherWarps,
               "producer warps");
