@@ -78,35 +78,66 @@ struct WUnit {
     int nch;  // K chunks of at most kWSlabKb blocks
 };
 
-// Static walk over units cluster, cluster + clusters, ...; the expert's
-// count and offset for the next unit are read while the current one runs.
+// Experts in decreasing order of routed rows (ties by id), built in shared
+// memory at kernel start when E <= kWSortMaxE, just past the kernel's fixed
+// shared memory: the units of the heaviest experts are dealt first.
+constexpr int kWSortMaxE = 2048;
+static_assert(kWSmemBytes + 8 * kWSortMaxE <= 232448, "shared memory per CTA with the expert order");
+__device__ __forceinline__ const int32_t* w_order_smem() {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    return reinterpret_cast<const int32_t*>(smem_raw + (base - raw) + (kWSmemBytes - 1024));
+}
+
+// Static walk.  Units (expert, stationary tile) are numbered heaviest expert
+// first and dealt to the clusters in rounds, serpentine (round r goes to
+// clusters 0..n-1 when r is even, n-1..0 when odd), so that with skewed
+// routing every cluster gets a similar share of the rows; all roles of a
+// CTA walk the same sequence.  The next unit's count and offset are read
+// while the current one runs.
 struct WWalk {
     const GemmArgs& p;
-    int total, unit, step;
+    const int32_t* order;  // experts by decreasing count, or nullptr (expert id order)
+    int total, n, ncl, c, unit;
     int cnt, off;
     __device__ __forceinline__ WWalk(const GemmArgs& p_)
-        : p(p_), total(p_.E * p_.m_tiles), unit((int)blockIdx.x >> 1), step((int)gridDim.x >> 1) {
+        : p(p_),
+          order(p_.E <= kWSortMaxE ? w_order_smem() : nullptr),
+          total(p_.E * p_.m_tiles),
+          n(0),
+          ncl((int)gridDim.x >> 1),
+          c((int)blockIdx.x >> 1) {
+        unit = map(0);
         if (unit < total) load(unit);
     }
+    __device__ __forceinline__ int map(int r) const { return r * ncl + ((r & 1) ? ncl - 1 - c : c); }
+    __device__ __forceinline__ int expert(int u) const {
+        const int i = u / p.m_tiles;
+        return order ? order[i] : i;
+    }
     __device__ __forceinline__ void load(int u) {
-        const int e = u / p.m_tiles;
+        const int e = expert(u);
         cnt = __ldg(p.counts + e);
         off = __ldg(p.offs + e);
     }
     __device__ __forceinline__ bool valid() const { return unit < total; }
     __device__ __forceinline__ WUnit take() {
         WUnit w;
-        w.e = unit / p.m_tiles;
-        w.s = unit - w.e * p.m_tiles;
+        w.e = expert(unit);
+        w.s = unit % p.m_tiles;
         w.cnt = cnt;
         w.off = off;
         w.nkb = (cnt + kBK - 1) / kBK;
         w.nch = (w.nkb + kWSlabKb - 1) / kWSlabKb;
-        const int nxt = unit + step;
+        const int nxt = map(n + 1);
         if (nxt < total) load(nxt);
         return w;
     }
-    __device__ __forceinline__ void next() { unit += step; }
+    __device__ __forceinline__ void next() {
+        ++n;
+        unit = map(n);
+    }
 };
 
 // K blocks [kb0, kb1) of chunk c.
@@ -449,6 +480,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_map(&mapS);
         tma_prefetch_map(&mapC);
     }
+    if (p.E <= kWSortMaxE) {
+        // rank of expert e = the experts with more routed rows, or as many
+        // and a smaller id; order[rank] = e
+        int32_t* ord = reinterpret_cast<int32_t*>(base_ptr + (kWSmemBytes - 1024));
+        int32_t* cnt = ord + p.E;
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = __ldg(p.counts + e);
+        __syncthreads();
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+            const int ce = cnt[e];
+            int r = 0;
+            for (int f = 0; f < p.E; ++f) {
+                const int cf = cnt[f];
+                r += (cf > ce || (cf == ce && f < e)) ? 1 : 0;
+            }
+            ord[r] = e;
+        }
+        // visible to every role after the cluster barrier below
+    }
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
@@ -511,13 +560,16 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = kWSmemBytes;
+    // the expert order (and the counts it is built from) follow the fixed part
+    const int sort_bytes = a.E <= kWSortMaxE ? 8 * a.E : 0;
+    cfg.dynamicSmemBytes = kWSmemBytes + (size_t)sort_bytes;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (clusters_fit[dev] == 0) {
         // set once per device, outside any stream capture (on the first call)
-        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F, kMG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
+        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F, kMG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kWSmemBytes + 8 * kWSortMaxE);
         if (e != cudaSuccess) return (int)e;
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
