@@ -8,7 +8,9 @@ of sampled experts (most and least loaded, one below block M when present,
 random others).  Properties that hold at any size cover the rest: routing
 tables bit-exact over the whole routing, every output finite, the combine
 equal to the slot-ordered FP32 sum of the weighted rows for every token, and
-zero weight gradients for experts that got no slot."""
+zero weight gradients for experts that got no slot.  At the V3 shape the FP8
+dispatch forward and the FP32 main-gradient backward are also checked bit
+for bit against the bf16 path."""
 import numpy as np
 import pytest
 import torch
@@ -88,3 +90,36 @@ def test_full_size(name, n_tok, n_exp):
     print(name, "experts", exps, "counts", [int(counts[e]) for e in exps])
     for n, r in report.items():
         print(name, n, {q: f"{v:.3e}" for q, v in r.items()})
+
+
+def test_full_size_fp8_dispatch_and_main_grad():
+    """The V3-shaped layer through the two variants, against the bf16 path
+    on the same GPU: the FP8-dispatch forward equals the bf16 forward on the
+    dequantized input bit for bit, and the FP32 main-gradient backward from
+    zero main gradients rounds to the bf16 weight gradients bit for bit."""
+    shape = CONFIGS["v3"]
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    inp = make_layer_inputs(shape, seed=5, device="cuda")
+    s = B.shape_of(T, H, I, E, k)
+    q = torch.empty(T, H, dtype=torch.uint8, device="cuda")
+    sf = torch.empty(T, H // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_fp8(s, inp["x"], q, sf)
+    xd = torch.empty_like(inp["x"])
+    B.moe_dequantize_fp8(s, q, sf, xd)
+    ref = GpuRun(T, H, I, E, k)
+    ref.run(dict(inp, x=xd))
+    y8 = torch.empty_like(ref.y)
+    B.moe_forward_fp8(ref.shape, q, sf, inp["W1"], inp["W2"], inp["topk_w"], ref.route, ref.saved, y8)
+    torch.cuda.synchronize()
+    assert torch.equal(y8, ref.y)
+    # the saved activations are again those of the dequantized input: main-grad backward
+    mg1 = torch.zeros(E, H, 2 * I, dtype=torch.float32, device="cuda")
+    mg2 = torch.zeros(E, I, H, dtype=torch.float32, device="cuda")
+    dx = torch.empty_like(ref.dx)
+    dw = torch.empty_like(ref.dw)
+    B.moe_backward_main_grad(ref.shape, inp["dY"], xd, inp["W1"], inp["W2"], inp["topk_w"], ref.route, ref.saved,
+                             ref.bwd, dx, mg1, mg2, dw)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, ref.dx) and torch.equal(dw, ref.dw)
+    assert torch.equal(mg1.to(torch.bfloat16), ref.dW1)
+    assert torch.equal(mg2.to(torch.bfloat16), ref.dW2)
