@@ -88,3 +88,23 @@ def test_null_and_misaligned_pointers_rejected_before_device_use(lib):
     fake[3] += 4  # misaligned topk_w
     assert lib.moe_backward(ctypes.byref(s), *fake) == B.MOE_EUNSUPPORTED
     assert "aligned" in B.moe_last_error()
+
+
+def test_variant_entry_points_reject_bad_arguments_before_device_use(lib):
+    s = B.shape_of(64, 128, 64, 8, 2)
+    # FP32 main-gradient backward: same checks as moe_backward
+    assert lib.moe_backward_main_grad(ctypes.byref(s), *([None] * 13)) == B.MOE_EINVAL
+    fake = [4096 * (i + 1) for i in range(13)]
+    fake[10] += 8  # misaligned main_grad_W2
+    assert lib.moe_backward_main_grad(ctypes.byref(s), *fake) == B.MOE_EUNSUPPORTED
+    # FP8 dispatch entry points
+    assert lib.moe_quantize_fp8(ctypes.byref(s), None, None, None, None) == B.MOE_EINVAL
+    assert lib.moe_dequantize_fp8(ctypes.byref(s), None, None, None, None) == B.MOE_EINVAL
+    assert lib.moe_forward_fp8(ctypes.byref(s), *([None] * 9)) == B.MOE_EINVAL
+    assert lib.moe_quantize_fp8(ctypes.byref(s), 4096, 8192 + 4, 16384, None) == B.MOE_EUNSUPPORTED
+    bad = B.MoeShape(64, 96, 64, 8, 2, 128)  # H not a multiple of 64
+    assert lib.moe_quantize_fp8(ctypes.byref(bad), 4096, 8192, 16384, None) == B.MOE_EUNSUPPORTED
+    # no tokens: nothing to do, no device touched
+    z = B.shape_of(0, 128, 64, 8, 2)
+    assert lib.moe_quantize_fp8(ctypes.byref(z), None, None, None, None) == 0
+    assert lib.moe_dequantize_fp8(ctypes.byref(z), None, None, None, None) == 0
