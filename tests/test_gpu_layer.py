@@ -99,6 +99,41 @@ def test_one_hot_expert_long_k():
     _full_check(shape, _inputs(shape, 7, mutate))
 
 
+@pytest.mark.parametrize("main_grad", [False, True])
+def test_experts_around_the_weight_gradient_slab(main_grad):
+    """Experts with 320 routed rows (the most the weight-gradient slab holds),
+    321 (one row past it: a second K chunk of one row) and 700, and one empty
+    expert, with H = 320 (the last 256-feature tile half past H) and I = 192,
+    the workspaces starting as NaN bytes; also through the FP32 main-gradient
+    entry point."""
+    sizes = [320, 321, 700, 0, 59]
+    T, H, I, E, k = sum(sizes), 320, 192, len(sizes), 1
+    shape = LayerShape("slab_edges", T=T, H=H, I=I, E=E, k=k)
+
+    def mutate(inp):
+        g = torch.Generator().manual_seed(12)
+        idx = torch.cat([torch.full((n,), e, dtype=torch.int32) for e, n in enumerate(sizes)])
+        inp["topk_idx"] = idx[torch.randperm(T, generator=g)].view(T, 1)
+
+    inp = _inputs(shape, 13, mutate)
+    if not main_grad:
+        run = _full_check(shape, inp)
+        assert torch.all(run.dW1[3] == 0) and torch.all(run.dW2[3] == 0)
+        return
+    run = GpuRun(T, H, I, E, k)
+    run.poison()
+    run.run(inp)
+    mg1 = torch.zeros(E, H, 2 * I, device="cuda")
+    mg2 = torch.zeros(E, I, H, device="cuda")
+    B.moe_backward_main_grad(run.shape, inp["dY"], inp["x"], inp["W1"], inp["W2"], inp["topk_w"], run.route,
+                             run.saved, run.bwd, run.dx, mg1, mg2, run.dw)
+    torch.cuda.synchronize()
+    ref = oracle_all(inp, E)
+    compare("main_grad_W1", f32(mg1), ref["dW1"])
+    compare("main_grad_W2", f32(mg2), ref["dW2"])
+    assert torch.equal(mg1.to(torch.bfloat16), run.dW1) and torch.equal(mg2.to(torch.bfloat16), run.dW2)
+
+
 def test_skewed_routing_small():
     shape = LayerShape("skew_small", T=512, H=256, I=192, E=32, k=4, skew_c=1.0)
     inp = _inputs(shape, 8)
