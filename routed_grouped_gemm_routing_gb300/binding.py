@@ -116,6 +116,9 @@ def _ptr(t, dtype, numel=None, name="tensor"):
         return None
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():

@@ -98,8 +98,9 @@ def moe_layer(x, W1, W2, topk_idx, topk_weights, workspace: MoEWorkspace | None 
             mg = getattr(W, "main_grad", None)
             if mg is None or mg.dtype != torch.float32 or tuple(mg.shape) != tuple(W.shape):
                 raise ValueError(f"accumulate_main_grad needs {n}.main_grad: float32 of {n}'s shape")
-    return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace, float(activation_clamp),
-                             bool(accumulate_main_grad))
+    with torch.cuda.device(x.device):
+        return MoEFunction.apply(x, W1, W2, topk_idx, topk_weights, workspace, float(activation_clamp),
+                                 bool(accumulate_main_grad))
 
 
 def train_step_from_host(x_h, topk_idx_h, topk_w_h, dY_h, W1, W2, ws: MoEWorkspace, outs: dict):
