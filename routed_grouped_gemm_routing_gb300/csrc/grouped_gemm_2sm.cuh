@@ -45,6 +45,8 @@
 // status word, and both CTAs leave through the closing cluster barrier.
 #pragma once
 
+#include <atomic>
+
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -1131,7 +1133,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
 // feed until none is left).
 template <int F>
 int launch_gemm_pair(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
-    static int clusters_fit[kMaxDevices] = {};
+    // filled on the first call per device; host threads may race to fill it
+    // with the same value
+    static std::atomic<int> clusters_fit[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
@@ -1147,7 +1151,8 @@ int launch_gemm_pair(const GemmArgs& a, const GemmMaps& m, int max_units, cudaSt
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (clusters_fit[dev] == 0) {
+    int fit = clusters_fit[dev].load(std::memory_order_relaxed);
+    if (fit == 0) {
         // set once per device, outside any stream capture (on the first call)
         e = cudaFuncSetAttribute(moe_gemm_pair_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  t2_smem_bytes<F>());
@@ -1160,10 +1165,11 @@ int launch_gemm_pair(const GemmArgs& a, const GemmMaps& m, int max_units, cudaSt
         e = cudaOccupancyMaxActiveClusters(&n, moe_gemm_pair_kernel<F>, &cfg);
         if (e != cudaSuccess) return (int)e;
         if (n < 1) return (int)cudaErrorInvalidConfiguration;
-        clusters_fit[dev] = n;
+        fit = n;
+        clusters_fit[dev].store(n, std::memory_order_relaxed);
     }
     if (max_units <= 0) return 0;
-    const int clusters = max_units < clusters_fit[dev] ? max_units : clusters_fit[dev];
+    const int clusters = max_units < fit ? max_units : fit;
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     e = cudaLaunchKernelEx(&cfg, moe_gemm_pair_kernel<F>, m.a, m.b, m.c0, m.c1, m.d, a);
     if (e != cudaSuccess) return (int)e;

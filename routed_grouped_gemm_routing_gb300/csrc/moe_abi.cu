@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -98,7 +99,8 @@ int check_shape(const moe_shape* s) {
     if (!s) return fail(MOE_EINVAL, "shape is NULL");
     if (s->T < 0) return fail(MOE_EINVAL, "T must be >= 0");
     if (s->H <= 0 || s->I <= 0) return fail(MOE_EINVAL, "H and I must be > 0");
-    if (s->E < 1 || s->E > 1024) return fail(MOE_EINVAL, "E must be in [1, 1024]");
+    if (s->E < 1 || s->E > kMaxExperts) return fail(MOE_EINVAL, "E must be in [1, 1024]");
+    static_assert(kMaxExperts == 1024, "update the E range in the message");
     if (s->k < 1 || s->k > s->E) return fail(MOE_EINVAL, "k must be in [1, E]");
     if (s->H % 64 || s->I % 64) return fail(MOE_EUNSUPPORTED, "H and I must be multiples of 64");
     if (s->block_m != kBM) return fail(MOE_EUNSUPPORTED, "block_m must be 128");
@@ -115,18 +117,23 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // ---------------------------------------------------------------- devices
 int num_sms_current(int* out) {
-    static int cache[64] = {0};
+    // filled on first use; host threads may race to fill it with the same value
+    static std::atomic<int> cache[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
-        *out = cache[dev];
-        return 0;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached) {
+        const int n = cache[dev].load(std::memory_order_relaxed);
+        if (n > 0) {
+            *out = n;
+            return 0;
+        }
     }
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return (int)e;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    if (cached) cache[dev].store(n, std::memory_order_relaxed);
     *out = n;
     return 0;
 }

@@ -22,6 +22,7 @@ constexpr int kWarpMma = 5;
 constexpr int kWarpGather0 = 6;
 constexpr int kGemmThreads = 32 * (kWarpGather0 + kGatherWarps);
 constexpr int kMaxDevices = 64;
+constexpr int kMaxExperts = 1024;  // E accepted by the entry points
 constexpr int kEpiWarps = 4;
 constexpr int kStageEpiBytes = 8192;  // per epilogue warp: TMA-store staging
 

@@ -26,6 +26,7 @@
 // An expert's rows therefore hold its slots in increasing slot order: the
 // tables are bit-exact and reproducible, and need no atomics on global
 // memory (the block counts are plain per-block integer sums).
+#include <atomic>
 #include "moe_internal.h"
 
 namespace moe {
@@ -215,15 +216,17 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-int set_smem_once(const void* fn, int bytes, bool* done) {
+// Host threads may race through the first call; setting the attribute twice
+// is harmless.
+int set_smem_once(const void* fn, int bytes, std::atomic<bool>* done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
     if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
-    if (!done[dev]) {
+    if (!done[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return (int)e;
-        done[dev] = true;
+        done[dev].store(true, std::memory_order_release);
     }
     return 0;
 }
@@ -240,9 +243,9 @@ void route_block_split(long long tk, int* nblk, long long* per_blk) {
 
 int launch_route_prologue(const moe_shape& s, const moe_layout& L, const int32_t* topk_idx, uint8_t* route,
                           cudaStream_t st) {
-    // opt in once per device to the largest size any E <= 1024 needs
-    static bool done_hist[kMaxDevices] = {};
-    int e = set_smem_once((const void*)route_hist_kernel, (int)(sizeof(int) * (1 + kWarps) * 1024), done_hist);
+    // opt in once per device to the largest size any E <= kMaxExperts needs
+    static std::atomic<bool> done_hist[kMaxDevices] = {};
+    int e = set_smem_once((const void*)route_hist_kernel, (int)(sizeof(int) * (1 + kWarps) * kMaxExperts), done_hist);
     if (e) return e;
     const long long tk = (long long)s.T * s.k;
     int nblk = 0;

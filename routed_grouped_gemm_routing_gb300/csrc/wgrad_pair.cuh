@@ -79,10 +79,9 @@ struct WUnit {
 };
 
 // Experts in decreasing order of routed rows (ties by id), built in shared
-// memory at kernel start when E <= kWSortMaxE, just past the kernel's fixed
-// shared memory: the units of the heaviest experts are dealt first.
-constexpr int kWSortMaxE = 2048;
-static_assert(kWSmemBytes + 8 * kWSortMaxE <= 232448, "shared memory per CTA with the expert order");
+// memory at kernel start just past the kernel's fixed shared memory (8 bytes
+// per expert): the units of the heaviest experts are dealt first.
+static_assert(kWSmemBytes + 8 * kMaxExperts <= 232448, "shared memory per CTA with the expert order");
 __device__ __forceinline__ const int32_t* w_order_smem() {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -98,12 +97,12 @@ __device__ __forceinline__ const int32_t* w_order_smem() {
 // while the current one runs.
 struct WWalk {
     const GemmArgs& p;
-    const int32_t* order;  // experts by decreasing count, or nullptr (expert id order)
+    const int32_t* order;  // experts by decreasing count
     int total, n, ncl, c, unit;
     int cnt, off;
     __device__ __forceinline__ WWalk(const GemmArgs& p_)
         : p(p_),
-          order(p_.E <= kWSortMaxE ? w_order_smem() : nullptr),
+          order(w_order_smem()),
           total(p_.E * p_.m_tiles),
           n(0),
           ncl((int)gridDim.x >> 1),
@@ -112,10 +111,7 @@ struct WWalk {
         if (unit < total) load(unit);
     }
     __device__ __forceinline__ int map(int r) const { return r * ncl + ((r & 1) ? ncl - 1 - c : c); }
-    __device__ __forceinline__ int expert(int u) const {
-        const int i = u / p.m_tiles;
-        return order ? order[i] : i;
-    }
+    __device__ __forceinline__ int expert(int u) const { return order[u / p.m_tiles]; }
     __device__ __forceinline__ void load(int u) {
         const int e = expert(u);
         cnt = __ldg(p.counts + e);
@@ -480,7 +476,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_map(&mapS);
         tma_prefetch_map(&mapC);
     }
-    if (p.E <= kWSortMaxE) {
+    {
         // rank of expert e = the experts with more routed rows, or as many
         // and a smaller id; order[rank] = e
         int32_t* ord = reinterpret_cast<int32_t*>(base_ptr + (kWSmemBytes - 1024));
@@ -548,7 +544,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ceil(I / 256) for dW2).
 template <int F, bool kMG = false>
 int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensorMap& mapC, cudaStream_t st) {
-    static int clusters_fit[kMaxDevices] = {};
+    // filled on the first call per device; host threads may race to fill it
+    // with the same value
+    static std::atomic<int> clusters_fit[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return (int)e;
@@ -561,15 +559,16 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     // the expert order (and the counts it is built from) follow the fixed part
-    const int sort_bytes = a.E <= kWSortMaxE ? 8 * a.E : 0;
-    cfg.dynamicSmemBytes = kWSmemBytes + (size_t)sort_bytes;
+    if (a.E < 1 || a.E > kMaxExperts) return (int)cudaErrorInvalidValue;
+    cfg.dynamicSmemBytes = kWSmemBytes + 8 * (size_t)a.E;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (clusters_fit[dev] == 0) {
+    int fit = clusters_fit[dev].load(std::memory_order_relaxed);
+    if (fit == 0) {
         // set once per device, outside any stream capture (on the first call)
         e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F, kMG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kWSmemBytes + 8 * kWSortMaxE);
+                                 kWSmemBytes + 8 * kMaxExperts);
         if (e != cudaSuccess) return (int)e;
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -579,11 +578,12 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
         e = cudaOccupancyMaxActiveClusters(&n, moe_wgrad_pair_kernel<F, kMG>, &cfg);
         if (e != cudaSuccess) return (int)e;
         if (n < 1) return (int)cudaErrorInvalidConfiguration;
-        clusters_fit[dev] = n;
+        fit = n;
+        clusters_fit[dev].store(n, std::memory_order_relaxed);
     }
     const long long units = (long long)a.E * a.m_tiles;
     if (units <= 0) return 0;
-    const int clusters = units < clusters_fit[dev] ? (int)units : clusters_fit[dev];
+    const int clusters = units < fit ? (int)units : fit;
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     e = cudaLaunchKernelEx(&cfg, moe_wgrad_pair_kernel<F, kMG>, mapS, mapC, a);
     if (e != cudaSuccess) return (int)e;
