@@ -55,6 +55,7 @@ def _check(logits: np.ndarray, k: int):
 
 @pytest.mark.parametrize("T,E,k,seed", [
     (300, 64, 6, 0), (257, 37, 5, 1), (64, 7, 7, 2), (100, 1024, 1, 3), (40, 200, 33, 4), (9, 1024, 1024, 5),
+    (130, 100, 4, 6), (50, 500, 9, 7), (33, 32, 32, 8), (70, 33, 3, 9), (60, 993, 17, 10),
 ])
 def test_random_logits(T, E, k, seed):
     rng = np.random.default_rng(seed)
@@ -69,6 +70,11 @@ def test_ties_nan_and_infinities():
     lg[5, [1, 7, 30]] = np.inf
     lg[6, ::3] = np.nan
     lg[7, 10] = np.inf
+    lg[8, :] = -1.0
+    lg[8, [3, 20]] = [0.0, -0.0]      # equal keys: +0 at the lower id
+    lg[9, :] = -1.0
+    lg[9, [2, 40]] = [-0.0, 0.0]      # equal keys: -0 at the lower id
+    lg[10, ::2] = -0.0                # -0 and (integer-valued) others
     _check(lg, 4)
     _check(lg, 45)
 

@@ -57,6 +57,16 @@ def test_ties_go_to_the_lower_expert_id():
     assert idx[2].tolist() == [0, 1, 2, 3] and np.allclose(w[2], 0.25)
 
 
+def test_signed_zeros_are_equal_keys():
+    """-0 and +0 are the same number: their order comes from the expert id."""
+    lg = np.full((2, 6), -1.0, np.float32)
+    lg[0, [1, 4]] = [0.0, -0.0]
+    lg[1, [1, 4]] = [-0.0, 0.0]
+    idx, w = oracle.router_topk(lg, 3)
+    assert idx[0].tolist() == [1, 4, 0] and idx[1].tolist() == [1, 4, 0]
+    np.testing.assert_allclose(w[0], np.array([1, 1, np.exp(-1.0)]) / (2 + np.exp(-1.0)), rtol=1e-7)
+
+
 def test_shift_invariance():
     lg = np.random.default_rng(5).standard_normal((20, 12)).astype(np.float32)
     i0, w0 = oracle.router_topk(lg, 3)
