@@ -372,7 +372,10 @@ __device__ __forceinline__ void transpose_reduce_step(float (&v)[32], int lane) 
 //   dup = da * silu(gate),  aw = w a
 // into the three output boxes.  kClamp: gate and up clamped to [-c, c] and
 // the gradients masked by the forward's decisions (bit lane of row j's
-// gmask / umask word, lane j holding row j's words).
+// gmask / umask word, lane j holding row j's words).  s(z) = 1 / (1 + e^-z)
+// with the hardware exponential and the fast divide (within 2 ulp, and 0
+// once e^-z overflows, which is the limit): with a full-precision divide
+// this arithmetic outlasted the MMAs of a unit when K is short.
 template <bool kClamp>
 __device__ __forceinline__ void swiglu_t_chunk(uint32_t stage, uint32_t in_box, bool colok, int lane, float wl,
                                                const float (&v)[32], float c, uint32_t gmask, uint32_t umask) {
@@ -393,7 +396,7 @@ __device__ __forceinline__ void swiglu_t_chunk(uint32_t stage, uint32_t in_box, 
             pg = (float)((__shfl_sync(0xffffffffu, gmask, j) >> lane) & 1u);
             pu = (float)((__shfl_sync(0xffffffffu, umask, j) >> lane) & 1u);
         }
-        const float sg = 1.0f / (1.0f + __expf(-gc));
+        const float sg = __fdividef(1.0f, 1.0f + __expf(-gc));
         sts_sw64(stage, j, lane, da * uc * sg * (1.0f + gc * (1.0f - sg)) * pg);
         sts_sw64(stage + 2048, j, lane, da * gc * sg * pu);
         sts_sw64(stage + 4096, j, lane, wv * av);
@@ -872,7 +875,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                     stage_col_sw64(buf, lane, v);
                     if (p.clamp == INFINITY) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = v[j] / (1.0f + __expf(-v[j])) * u[j];
+                        for (int j = 0; j < 32; ++j) v[j] = __fdividef(v[j], 1.0f + __expf(-v[j])) * u[j];
                     } else {
                         if (col < I) {
                         // record the FP32 clamp decisions for the backward:
@@ -894,7 +897,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const float g = clamp_in(v[j], p.clamp);
-                            v[j] = g / (1.0f + __expf(-g)) * clamp_in(u[j], p.clamp);
+                            v[j] = __fdividef(g, 1.0f + __expf(-g)) * clamp_in(u[j], p.clamp);
                         }
                     }
                     stage_col_sw64(buf + 2048, lane, v);
