@@ -1,6 +1,8 @@
 // Inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// cp.async, and the 5th-generation tensor core (tcgen05: TMEM allocation,
-// MMA, commit, TMEM loads).  Written against the public PTX ISA.
+// cp.async, and the 5th-generation tensor core (tcgen05 fences, TMEM loads,
+// shared-memory and instruction descriptors; the SM-pair allocation, MMA and
+// commit forms sit with the kernels that use them).  Written against the
+// public PTX ISA.
 #pragma once
 
 #include <cuda.h>
@@ -49,15 +51,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Returns false (and
-// raises *abort) after kWaitLimitNs, or as soon as another role raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// raises *abort) after limit_ns (the kernels keep the kWaitLimitNs default),
+// or as soon as another role raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }
@@ -73,47 +77,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2, int c3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-        : "memory");
-}
-
-// TMA loads delivered to the same shared-memory offset of every CTA in
-// `mask` (this CTA's cluster), each signalling its own mbarrier at `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, int c0, int c1, uint32_t bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2,
-                                               uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap* m, int c0, int c1, int c2, int c3,
-                                               uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "h"(mask)
         : "memory");
 }
 
@@ -132,12 +95,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int c0, int c
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                      reinterpret_cast<uint64_t>(m)),
                  "r"(c0), "r"(c1), "r"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, int c0, int c1, int c2, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
                  : "memory");
 }
 // L2 eviction-priority policies for the .L2::cache_hint forms below.
@@ -206,35 +163,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ------------------------------------------------------------------- tcgen05
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem] x B[smem], bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 // Issue a load of 32 consecutive fp32 columns of this warp's 32 TMEM lanes
 // (no wait: call tmem_ld_wait before using the registers).
@@ -251,15 +184,6 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[3
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Like tc_commit, but arrives on the mbarrier at offset `bar` of every CTA in
-// `mask` (this CTA's cluster).
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     bar),
-                 "h"(mask)
-                 : "memory");
-}
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -311,13 +235,6 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t box, int r, const uint3
     for (int c = 0; c < 8; ++c)
         st_shared_v4(box + r * 128 + ((c ^ (r & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
 }
-// Row r of a 32-row box 32 bf16 (64 bytes) wide, 64-byte swizzle: chunk c
-// lands at chunk c^((r/2)%4).
-__device__ __forceinline__ void stage_row_sw64(uint32_t box, int r, const uint32_t (&p)[16]) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        st_shared_v4(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
-}
 
 // 2^(s - 127) for a UE8M0 scale byte s (s = 0: the subnormal 2^-127).
 __device__ __forceinline__ float fp8_scale(uint32_t s) {
@@ -342,27 +259,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
         float2 t = __bfloat1622float2(p[i]);
         f[2 * i] = t.x;
         f[2 * i + 1] = t.y;
-    }
-}
-// Stores 32 floats as 32 bf16 (64 bytes, 16-byte aligned destination).
-__device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        d[q] = u;
-    }
-}
-__device__ __forceinline__ void load_bf16x32(const void* src, float (&v)[32]) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u = __ldg(s + q);
-        unpack_bf16x8(u, v + 8 * q);
     }
 }
 
