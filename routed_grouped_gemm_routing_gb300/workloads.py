@@ -62,6 +62,9 @@ CONFIGS = {
     "v3": LayerShape("v3", T=8192, H=7168, I=2048, E=256, k=8),
     "wide": LayerShape("wide", T=4096, H=7168, I=3072, E=384, k=6),
     "skew": LayerShape("skew", T=8192, H=7168, I=2048, E=256, k=8, skew_c=0.5),
+    # twice as sharp: the top expert takes nearly every token and many
+    # experts get no slot at all (a correctness case for empty experts)
+    "skew_c1": LayerShape("skew_c1", T=8192, H=7168, I=2048, E=256, k=8, skew_c=1.0),
     # V3 expert shapes with 16 experts and 512 tokens: the same ~256 routed
     # rows per expert as the V3 layer in ~3 GB of device memory (kernel
     # profiling captures must stay small).

@@ -4,8 +4,9 @@ skewed-V3-shaped layers) in the launch configuration the benchmark times.
 The oracle cannot cover every output at these sizes, so it checks what it
 can compute one by one: y, dx and d(topk_weights) of sampled tokens (from a
 sub-problem holding those tokens and their experts) and the full dW1 / dW2
-of sampled experts (most and least loaded, one below block M when present,
-random others).  Properties that hold at any size cover the rest: routing
+of sampled experts (most and least loaded, one below block M and one empty
+when present, two random others); 512 sampled tokens per workload, and a
+skewed routing sharp enough to leave experts empty.  Properties that hold at any size cover the rest: routing
 tables bit-exact over the whole routing, every output finite, the combine
 equal to the slot-ordered FP32 sum of the weighted rows for every token, and
 zero weight gradients for experts that got no slot.  At the V3 shape the FP8
@@ -15,7 +16,8 @@ import numpy as np
 import pytest
 import torch
 
-from moe_testlib import GpuRun, check_tables, compare, f32, oracle_experts, oracle_route, oracle_tokens
+from moe_testlib import (GpuRun, check_tables, compare, f32, oracle_all, oracle_experts, oracle_route,
+                         oracle_tokens)
 from routed_grouped_gemm_routing_gb300 import binding as B
 from routed_grouped_gemm_routing_gb300 import build
 from routed_grouped_gemm_routing_gb300.workloads import CONFIGS, make_layer_inputs
@@ -29,20 +31,31 @@ def _lib():
     B.lib()
 
 
-def _pick_experts(counts, n, rng):
+def _pick_experts(counts, rng, heaviest=True, n_random=2):
+    """Most-loaded (unless heaviest=False), least-loaded non-empty, one below
+    block M, one empty (when the routing has them) and n_random random
+    non-empty experts (at most 1024 rows each when the most loaded one is
+    left out, to bound the oracle's time)."""
     order = np.argsort(counts, kind="stable")
     nonzero = order[counts[order] > 0]
-    picks = [int(order[-1]), int(nonzero[0])]
-    small = np.nonzero((counts > 0) & (counts < 128))[0]
-    if len(small):
-        picks.append(int(small[0]))
-    rest = [e for e in rng.permutation(len(counts)) if e not in picks and counts[e] > 0]
-    picks += [int(e) for e in rest[: max(0, n - len(picks))]]
-    return picks[:n]
+    picks = [int(order[-1])] if heaviest else []
+    picks.append(int(nonzero[0]))
+    for cand in (np.nonzero((counts > 0) & (counts < 128))[0], np.nonzero(counts == 0)[0]):
+        cand = [int(e) for e in cand if int(e) not in picks]
+        if cand:
+            picks.append(cand[0])
+    cap = np.inf if heaviest else 1024
+    rest = [int(e) for e in rng.permutation(len(counts)) if int(e) not in picks and 0 < counts[e] <= cap]
+    return picks + rest[:n_random]
 
 
-@pytest.mark.parametrize("name,n_tok,n_exp", [("v2lite", 48, 4), ("v3", 6, 3), ("skew", 6, 3), ("wide", 4, 3)])
-def test_full_size(name, n_tok, n_exp):
+# (workload, sampled tokens, weight-gradient experts include the most loaded)
+CASES = [("v2lite", 512, True), ("v3", 512, True), ("skew", 512, True), ("wide", 512, True),
+         ("skew_c1", 128, False)]
+
+
+@pytest.mark.parametrize("name,n_tok,heaviest", CASES)
+def test_full_size(name, n_tok, heaviest):
     shape = CONFIGS[name]
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     inp = make_layer_inputs(shape, seed=0, device="cuda")
@@ -72,24 +85,39 @@ def test_full_size(name, n_tok, n_exp):
         r = inv[:, j]
         acc += torch.where((r >= 0)[:, None], o[r.clamp(min=0)].float(), torch.zeros((), device="cuda"))
     assert torch.equal(acc.to(torch.bfloat16), run.y)
+    del acc, o
 
     rng = np.random.default_rng(1234)
-    toks = np.sort(rng.choice(T, size=n_tok, replace=False))
+    toks = np.sort(rng.choice(T, size=min(n_tok, T), replace=False))
     y_ref, dx_ref, dw_ref = oracle_tokens(inp, E, toks)
     tt = torch.as_tensor(toks, device="cuda")
     report = {}
-    compare("y[sampled tokens]", f32(run.y[tt]), y_ref, report=report)
-    compare("dx[sampled tokens]", f32(run.dx[tt]), dx_ref, report=report)
-    compare("dtopk_w[sampled tokens]", f32(run.dw[tt]), dw_ref, bf16_output=False, report=report)
+    compare(f"{name} y[{len(toks)} tokens]", f32(run.y[tt]), y_ref, report=report)
+    compare(f"{name} dx[{len(toks)} tokens]", f32(run.dx[tt]), dx_ref, report=report)
+    compare(f"{name} dtopk_w[{len(toks)} tokens]", f32(run.dw[tt]), dw_ref, bf16_output=False, report=report)
 
-    exps = _pick_experts(counts, n_exp, rng)
-    dW1_ref, dW2_ref = oracle_experts(inp, E, exps)
-    et = torch.as_tensor(exps, device="cuda")
-    compare("dW1[sampled experts]", f32(run.dW1[et]), dW1_ref, report=report)
-    compare("dW2[sampled experts]", f32(run.dW2[et]), dW2_ref, report=report)
+    exps = _pick_experts(counts, rng, heaviest=heaviest)
     print(name, "experts", exps, "counts", [int(counts[e]) for e in exps])
-    for n, r in report.items():
-        print(name, n, {q: f"{v:.3e}" for q, v in r.items()})
+    dW1_ref, dW2_ref = oracle_experts(inp, E, exps)
+    for i, e in enumerate(exps):
+        compare(f"{name} dW1[{e}] ({int(counts[e])} rows)", f32(run.dW1[e]), dW1_ref[i], report=report)
+        compare(f"{name} dW2[{e}] ({int(counts[e])} rows)", f32(run.dW2[e]), dW2_ref[i], report=report)
+
+
+def test_full_size_tiny_every_output():
+    """The tiny layer (T=64, H=128, I=64, E=8, k=2): every output and
+    gradient against the oracle over the whole problem."""
+    shape = CONFIGS["tiny"]
+    inp = {k_: v.cuda() for k_, v in make_layer_inputs(shape, seed=0, device="cpu").items()}
+    run = GpuRun(shape.T, shape.H, shape.I, shape.E, shape.k)
+    run.poison()
+    run.run(inp)
+    torch.cuda.synchronize()
+    check_tables(run, oracle_route(inp, shape.E))
+    ref = oracle_all(inp, shape.E)
+    for n, got in (("y", run.y), ("dx", run.dx), ("dW1", run.dW1), ("dW2", run.dW2)):
+        compare(f"tiny {n}", f32(got), ref[n])
+    compare("tiny dtopk_w", f32(run.dw), ref["dtopk_w"], bf16_output=False)
 
 
 def test_full_size_fp8_dispatch_and_main_grad():

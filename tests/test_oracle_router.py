@@ -12,7 +12,6 @@ import torch
 import oracle
 from routed_grouped_gemm_routing_gb300.workloads import make_routing
 
-scipy_special = pytest.importorskip("scipy.special")
 
 
 def _key(lg):
@@ -23,6 +22,7 @@ def _key(lg):
 
 @pytest.mark.parametrize("T,E,k,seed", [(64, 8, 2, 0), (33, 37, 5, 1), (16, 256, 8, 2), (5, 6, 6, 3)])
 def test_matches_stable_argsort_and_softmax(T, E, k, seed):
+    scipy_special = pytest.importorskip("scipy.special")  # only this pin needs scipy
     lg = np.random.default_rng(seed).standard_normal((T, E)).astype(np.float32)
     idx, w = oracle.router_topk(lg, k)
     key = _key(lg)
@@ -79,7 +79,9 @@ def test_k_equals_e_is_a_full_softmax():
     lg = np.random.default_rng(6).standard_normal((7, 10)).astype(np.float32)
     idx, w = oracle.router_topk(lg, 10)
     assert all(sorted(r) == list(range(10)) for r in idx.tolist())
-    full = scipy_special.softmax(lg.astype(np.float64), axis=1)
+    z = lg.astype(np.float64)
+    full = np.exp(z - z.max(axis=1, keepdims=True))  # FP64 softmax written out with numpy
+    full /= full.sum(axis=1, keepdims=True)
     np.testing.assert_allclose(w, np.take_along_axis(full, idx, axis=1), rtol=2e-7)
 
 
