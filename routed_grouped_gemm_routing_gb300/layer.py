@@ -14,7 +14,13 @@ from . import binding as B
 
 
 class MoEWorkspace:
-    """Caller-owned device buffers of one layer shape (reused across steps)."""
+    """Caller-owned device buffers of one layer shape (reused across steps).
+
+    The routing tables and the saved activations of a forward live in the
+    workspace until its backward reads them.  ``generation`` counts the
+    forwards that wrote into it: a backward raises if another forward has
+    overwritten the workspace since its own forward (two micro-batches or two
+    layers sharing one workspace before their backwards)."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, device=None, activation_clamp: float = 0.0):
         self.shape = B.shape_of(T, H, I, E, k, activation_clamp=activation_clamp)
@@ -25,6 +31,7 @@ class MoEWorkspace:
         self.saved = torch.empty(max(L.saved_bytes, 16), dtype=torch.uint8, device=dev)
         self._bwd = None
         self.device = dev
+        self.generation = 0
 
     @property
     def bwd(self):
@@ -56,8 +63,10 @@ class MoEFunction(torch.autograd.Function):
         y = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
         B.moe_route_prologue(ws.shape, idx, ws.route)
         B.moe_forward(ws.shape, x, W1.contiguous(), W2.contiguous(), w, ws.route, ws.saved, y)
+        ws.generation += 1
         ctx.save_for_backward(x, W1, W2, w)
         ctx.ws = ws
+        ctx.ws_generation = ws.generation
         ctx.w_dtype = topk_weights.dtype
         ctx.main_grad = main_grad
         return y
@@ -66,6 +75,11 @@ class MoEFunction(torch.autograd.Function):
     def backward(ctx, dy):
         x, W1, W2, w = ctx.saved_tensors
         ws = ctx.ws
+        if ws.generation != ctx.ws_generation:
+            raise RuntimeError(
+                "moe_layer backward: its workspace was overwritten by a later forward (this forward wrote "
+                f"generation {ctx.ws_generation}, the workspace now holds generation {ws.generation}); give "
+                "forwards whose backwards are still pending workspaces of their own")
         s = ws.shape
         dev = x.device
         dx = torch.empty_like(x)

@@ -247,6 +247,29 @@ def test_autograd_wrapper_matches_abi():
     assert torch.equal(w.grad, ref.dw)
 
 
+def test_autograd_workspace_reuse_is_detected():
+    """Two forwards on one caller workspace before their backwards: the
+    first backward would read the second forward's routing and activations,
+    so it raises; the second backward is the layer's gradient (oracle)."""
+    from routed_grouped_gemm_routing_gb300.layer import MoEWorkspace, moe_layer
+
+    shape = LayerShape("reuse", T=96, H=128, I=64, E=5, k=2)
+    first, second = _inputs(shape, 30), _inputs(shape, 31)
+    ws = MoEWorkspace(shape.T, shape.H, shape.I, shape.E, shape.k)
+    xs, ys = [], []
+    for inp in (first, second):
+        x = inp["x"].clone().requires_grad_(True)
+        xs.append(x)
+        ys.append(moe_layer(x, inp["W1"], inp["W2"], inp["topk_idx"], inp["topk_w"], workspace=ws))
+    with pytest.raises(RuntimeError, match="overwritten by a later forward"):
+        ys[0].backward(first["dY"])
+    ys[1].backward(second["dY"])
+    torch.cuda.synchronize()
+    ref = oracle_all(second, shape.E)
+    compare("y (second forward)", f32(ys[1]), ref["y"])
+    compare("dx (second forward)", f32(xs[1].grad), ref["dx"])
+
+
 def test_host_pipeline_matches_abi():
     """Three steps through HostPipeline (uploads of step n+1 and downloads of
     step n overlapping the kernels, double-buffered device slots) give the
