@@ -223,26 +223,54 @@ int moe_backward_main_grad(const moe_shape* shape, const void* dY, const void* x
  * Same inputs and output as moe_route_prologue followed by moe_forward
  * (topk_idx int32[T,k], y bf16[T,H] overwritten), but the routing tables and
  * the per-row intermediates live in a static 32 MiB device array inside the
- * library, which every GPU that loads the library holds until exit.  Allocates
- * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * library (MOE_NOALLOC_SCRATCH_BYTES), which every GPU that loads the library
+ * holds until exit.  Allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *  - status_out: NULL, or device memory for MOE_STATUS_WORDS int32 (16-byte
+ *    aligned) that receives this call's status words (the routing counts of
+ *    MOE_STATUS_MPAD.. and the timeout bit of MOE_STATUS_FLAGS) by a
+ *    device-to-device copy on `stream` after the kernels.  The words
+ *    themselves live in the static array, which the caller cannot address,
+ *    and the next call overwrites them.
  *  - Size limit: route_bytes (rounded up to 256) + saved_bytes of
- *    moe_workspace_layout must be <= 32 MiB (e.g. the V3 shape up to T = 1,
- *    the T=64, H=128, I=64, E=8, k=2 shape with room to spare); larger shapes
- *    return MOE_EUNSUPPORTED with a message naming the bytes needed.
+ *    moe_workspace_layout must be <= MOE_NOALLOC_SCRATCH_BYTES (e.g. the V3
+ *    shape up to T = 1, the T=64, H=128, I=64, E=8, k=2 shape with room to
+ *    spare); larger shapes return MOE_EUNSUPPORTED with a message naming the
+ *    bytes needed.
  *  - The first call on each device looks up the array's device address with
- *    cudaGetSymbolAddress (the device owning W1 is made current); make that
- *    first call before any stream capture.
+ *    cudaGetSymbolAddress (the device owning W1 is made current) and keeps it
+ *    for the life of the process; make that first call before any stream
+ *    capture, and do not use this entry point after a cudaDeviceReset of
+ *    that device.
  *  - Every call shares the one array and leaves its contents behind; each call
  *    rewrites every table it reads first, so results never depend on an
  *    earlier call.  Calls that overlap on the GPU (other streams, other host
  *    threads) race on the array: serialise them.
  *  - Forward only: the saved activations are not kept for a backward pass. */
+#define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* W1, const void* W2,
-                        const int32_t* topk_idx, const float* topk_w, void* y, void* stream);
+                        const int32_t* topk_idx, const float* topk_w, void* y, int32_t* status_out, void* stream);
 
 /* Copies the MOE_STATUS_WORDS status words of route_ws to host memory
  * `out` (int32[16]).  SYNCHRONISES `stream`; not for use under capture. */
 int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, void* stream);
+
+/* Diagnostic of the failure path (not part of the layer; the pages have no
+ * counterpart): every wait of the GEMM kernels on an mbarrier is bounded
+ * (2 s); a wait that runs out raises the kernel's abort flag, the other
+ * roles leave their waits, and bit 0 of MOE_STATUS_FLAGS in route_ws is set
+ * for the host.  This call runs that path on purpose with the same wait
+ * helpers, in one small kernel on `stream`, on a barrier nothing arrives on:
+ * one warp gives up after limit_ns (1 us .. 100 ms), and the warps using the
+ * two other wait forms (limit 4 * limit_ns) leave on its abort flag.  It
+ * sets bit 0 of route_ws's MOE_STATUS_FLAGS word and nothing else there
+ * (the next moe_route_prologue clears it).  elapsed_ns: NULL or device
+ * memory for 3 int64 that receive each warp's waiting time in ns (-1 if its
+ * wait had succeeded).  No fault, no hang: the kernel ends within
+ * 4 * limit_ns.  Errors as for moe_route_prologue (MOE_EINVAL for a limit out
+ * of range). */
+int moe_selftest_wait_timeout(const moe_shape* shape, void* route_ws, uint64_t limit_ns, int64_t* elapsed_ns,
+                              void* stream);
 
 /* Tracing.  moe_trace_begin hands the library `capacity` CUDA events
  * (cudaEvent_t passed as void*, created by the caller with timing enabled).

@@ -295,16 +295,35 @@ class KernelTrace:
         return [(self.names[i], self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(n)]
 
 
-def moe_forward_noalloc(shape: MoeShape, x, W1, W2, topk_idx, topk_w, y, stream=None):
+def moe_selftest_wait_timeout(shape: MoeShape, route_ws, limit_ns: int, elapsed=None, stream=None):
+    """Runs the kernels' bounded-wait give-up path on purpose (diagnostic; see
+    include/moe_layer.h): sets bit 0 of route_ws's MOE_STATUS_FLAGS word.
+    elapsed: None or an int64 CUDA tensor of 3 elements (ns each waiting warp
+    spent before giving up)."""
+    L = moe_workspace_layout(shape)
+    fn = lib().moe_selftest_wait_timeout
+    fn.argtypes = [ctypes.POINTER(MoeShape), ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    _check(fn(ctypes.byref(shape), _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), int(limit_ns),
+              _ptr(elapsed, torch.int64, 3, "elapsed"), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20  # MOE_NOALLOC_SCRATCH_BYTES of include/moe_layer.h
+
+
+def moe_forward_noalloc(shape: MoeShape, x, W1, W2, topk_idx, topk_w, y, status_out=None, stream=None):
     """Routing prologue + forward with the library's static scratch instead of
     caller workspaces (for callers that cannot allocate device memory; see
-    include/moe_layer.h).  Overwrites y; keeps nothing for a backward pass."""
+    include/moe_layer.h).  Overwrites y; keeps nothing for a backward pass.
+    status_out: None or an int32 CUDA tensor of STATUS_WORDS elements that
+    receives the call's status words (copied on the stream, no sync)."""
     L = lib()
     fn = L.moe_forward_noalloc
-    fn.argtypes = [ctypes.POINTER(MoeShape)] + [ctypes.c_void_p] * 7
+    fn.argtypes = [ctypes.POINTER(MoeShape)] + [ctypes.c_void_p] * 8
     fn.restype = ctypes.c_int
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     bf = torch.bfloat16
     _check(fn(ctypes.byref(shape), _ptr(x, bf, T * H, "x"), _ptr(W1, bf, E * H * 2 * I, "W1"),
               _ptr(W2, bf, E * I * H, "W2"), _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
-              _ptr(topk_w, torch.float32, T * k, "topk_w"), _ptr(y, bf, T * H, "y"), _stream(stream)))
+              _ptr(topk_w, torch.float32, T * k, "topk_w"), _ptr(y, bf, T * H, "y"),
+              _ptr(status_out, torch.int32, STATUS_WORDS, "status_out"), _stream(stream)))

@@ -606,6 +606,24 @@ int moe_read_status(const moe_shape* shape, const void* route_ws, int32_t* out, 
     return MOE_OK;
 }
 
+int moe_selftest_wait_timeout(const moe_shape* shape, void* route_ws, uint64_t limit_ns, int64_t* elapsed_ns,
+                              void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!route_ws) return fail(MOE_EINVAL, "NULL pointer argument");
+    if (!aligned16(route_ws) || (reinterpret_cast<uintptr_t>(elapsed_ns) & 7u))
+        return fail(MOE_EUNSUPPORTED, "route_ws must be 16-byte and elapsed_ns 8-byte aligned");
+    if (limit_ns < 1000u || limit_ns > 100000000u)
+        return fail(MOE_EINVAL, "limit_ns must be in [1 us, 100 ms]");
+    if ((rc = query_device(&c, route_ws))) return rc;
+    int32_t* status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(route_ws) + c.L.status);
+    const int e = launch_wait_selftest(status, limit_ns, reinterpret_cast<long long*>(elapsed_ns),
+                                       (cudaStream_t)stream);
+    if (e) return cuda_fail(e, "bounded-wait self-test launch");
+    return MOE_OK;
+}
+
 int moe_trace_begin(void* const* events, int capacity) {
     if (capacity < 0 || (capacity > 0 && !events)) return fail(MOE_EINVAL, "bad trace event array");
     g_trace.events = capacity > 0 ? events : nullptr;
@@ -643,14 +661,16 @@ const char* moe_version(void) { return "moe_gb300 0.1 (sm_103a, tcgen05)"; }
 namespace moe {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr size_t kNoAllocScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;  // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on the current device (set-up on the
-// first call per device).
+// first call per device).  The address is kept for the life of the process:
+// after a cudaDeviceReset of that device it would be stale, so the entry
+// point is not for use across a device reset.
 int noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -672,13 +692,14 @@ int noalloc_scratch(void** out) {
 }  // namespace moe
 
 extern "C" int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* W1, const void* W2,
-                                   const int32_t* topk_idx, const float* topk_w, void* y, void* stream) {
+                                   const int32_t* topk_idx, const float* topk_w, void* y, int32_t* status_out,
+                                   void* stream) {
     Ctx c;
     int rc = prepare(shape, &c);
     if (rc) return rc;
     if (!W1 || !W2 || (shape->T > 0 && (!x || !topk_idx || !topk_w || !y)))
         return fail(MOE_EINVAL, "NULL pointer argument");
-    const void* ptrs[] = {x, W1, W2, topk_idx, topk_w, y};
+    const void* ptrs[] = {x, W1, W2, topk_idx, topk_w, y, status_out};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
     const size_t route_part = align_up(c.L.route_bytes, 256);
@@ -698,5 +719,13 @@ extern "C" int moe_forward_noalloc(const moe_shape* shape, const void* x, const 
     // The prologue rewrites every table and status word it owns on each call,
     // so nothing left by an earlier call is read.
     if ((rc = moe_route_prologue(shape, topk_idx, route, stream))) return rc;
-    return moe_forward(shape, x, W1, W2, topk_w, route, route + route_part, y, stream);
+    if ((rc = moe_forward(shape, x, W1, W2, topk_w, route, route + route_part, y, stream))) return rc;
+    if (status_out) {
+        // the status words stay in the static scratch, which the caller
+        // cannot address: copy them out (device to device, on the stream)
+        const cudaError_t e = cudaMemcpyAsync(status_out, route + c.L.status, sizeof(int32_t) * MOE_STATUS_WORDS,
+                                              cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail((int)e, "copying the status words out of the static scratch");
+    }
+    return MOE_OK;
 }
