@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 SOURCES = ["moe_abi.cu", "route_prologue.cu", "router.cu", "combine.cu", "gemm_fwd.cu", "gemm_dgrad.cu", "fp8.cu",
-           "gemm_wgrad.cu"]
+           "gemm_wgrad.cu", "selftest.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH_FLAGS + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", "-Xptxas", "-warn-spills"]
 

@@ -9,8 +9,9 @@ namespace moe {
 
 // Every lane of the warp waits; the warp proceeds only if all lanes saw the
 // phase complete, so warp-collective instructions never run diverged.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -22,7 +23,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // elected lane issues at the pipe's rate.  kCluster: acquire at cluster
 // scope (barriers that receive arrivals from the other CTA of the pair).
 template <bool kCluster>
-__device__ __forceinline__ bool warp_wait_uniform(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool warp_wait_uniform(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     auto poll = [&]() -> bool {
         if constexpr (kCluster) {
             uint32_t ok;
@@ -43,7 +45,7 @@ __device__ __forceinline__ bool warp_wait_uniform(uint32_t bar, uint32_t parity,
     for (uint32_t it = 1;; ++it) {
         if (poll()) return true;
         if ((it & 63u) == 0) {
-            const bool late = global_timer_ns() - t0 > kWaitLimitNs;
+            const bool late = global_timer_ns() - t0 > limit_ns;
             if (__any_sync(0xffffffffu, *abort != 0 || late)) {
                 if (late) *abort = 1;
                 return false;

@@ -95,6 +95,7 @@ int launch_router_topk(const float* logits, int T, int E, int k, int32_t* topk_i
 int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t* sf, int num_sms, cudaStream_t st);
 int launch_dequantize_fp8(const uint8_t* q, const uint8_t* sf, long long n, __nv_bfloat16* out, int num_sms,
                           cudaStream_t st);
+int launch_wait_selftest(int32_t* status, uint64_t limit_ns, long long* elapsed, cudaStream_t st);
 int launch_dw_reduce(const float* dw_part, int cols, const int32_t* inv, long long slots, float* out, int num_sms,
                      cudaStream_t st);
 
