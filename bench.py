@@ -38,8 +38,28 @@ GEMM_FLOP_FACTOR = {  # useful FLOPs per routed slot, in units of H*I
 
 
 def gemm_alg_bytes(name: str, T: int, H: int, I: int, E: int, k: int) -> float:
-    """Algorithmic DRAM bytes of one launch: every operand read once and every
-    output written once, routed rows unpadded (bf16 everywhere)."""
+    """Algorithmic DRAM bytes of one launch: the weights read once, a weight
+    gradient written once, x / dY read once, the saved h written once (L1
+    forward) and read once (L2 dgrad).  The row-ordered intermediates (a, o,
+    dh, aw, dxp) and gathered rows are kernel traffic, not algorithmic bytes
+    (gemm_planned_bytes)."""
+    W1, W2 = 2.0 * E * H * 2 * I, 2.0 * E * I * H
+    x = dY = 2.0 * T * H
+    h = 2.0 * T * k * 2 * I
+    return {
+        "gemm_l1_fwd": W1 + x + h,
+        "gemm_l2_fwd": W2,
+        "gemm_l2_dgrad": W2 + dY + h,
+        "gemm_dw2": dY + W2,
+        "gemm_dw1": x + W1,
+        "gemm_l1_dgrad": W1,
+    }[name]
+
+
+def gemm_planned_bytes(name: str, T: int, H: int, I: int, E: int, k: int) -> float:
+    """DRAM bytes of one launch as the kernels are planned: every operand
+    (intermediates included) read once and every output written once, routed
+    rows unpadded (bf16 everywhere)."""
     tk = T * k
     W1, W2 = 2.0 * E * H * 2 * I, 2.0 * E * I * H
     x = dY = 2.0 * T * H
@@ -151,10 +171,12 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- CPU oracle
-def oracle_sample(shape, inputs, n_tok, seed=0, clamp=0.0):
+def oracle_sample(shape, inputs, n_tok, n_exp=1, seed=0, clamp=0.0):
     """Host copies of a bounded sample of the workload for the CPU oracle:
-    n_tok tokens (forward, dx, d topk_weights) and the weight gradients of one
-    typically loaded expert.  Returns (callable running it, useful FLOPs,
+    n_tok tokens (forward, dx, d topk_weights) and the weight gradients of
+    n_exp experts taken at evenly spaced quantiles of the expert load (the
+    median one when n_exp = 1).  n_tok >= T: the whole problem (every token
+    and every expert).  Returns (callable running it, useful FLOPs,
     description)."""
     import numpy as np
     import torch
@@ -163,26 +185,35 @@ def oracle_sample(shape, inputs, n_tok, seed=0, clamp=0.0):
     from routed_grouped_gemm_routing_gb300.workloads import bf16_bits
 
     E, k, H, I = shape.E, shape.k, shape.H, shape.I
+    dev = inputs["x"].device
     idx_all = inputs["topk_idx"].cpu().numpy()
-    rng = np.random.default_rng(seed)
-    toks = np.sort(rng.choice(shape.T, size=n_tok, replace=False))
+    valid = (idx_all >= 0) & (idx_all < E)
+    counts = np.bincount(idx_all[valid].ravel(), minlength=E)
+    whole = n_tok >= shape.T
+    if whole:
+        toks = np.arange(shape.T)
+        exps = np.arange(E)
+    else:
+        rng = np.random.default_rng(seed)
+        toks = np.sort(rng.choice(shape.T, size=n_tok, replace=False))
+        order = np.argsort(counts, kind="stable")
+        exps = np.unique(order[[int((q + 0.5) * E / n_exp) for q in range(n_exp)]])
+
+    def sub(ids):
+        remap = np.full(E, -1, np.int64)
+        remap[ids] = np.arange(len(ids))
+        return remap
+
     idx = idx_all[toks].astype(np.int64)
-    involved = np.unique(idx[(idx >= 0) & (idx < E)])
-    remap = np.full(E, -1, np.int64)
-    remap[involved] = np.arange(len(involved))
-    idx_t = np.where((idx >= 0) & (idx < E), remap[np.clip(idx, 0, E - 1)], -1).astype(np.int32)
-    it = torch.as_tensor(involved, device=inputs["x"].device)
-    tt = torch.as_tensor(toks, device=inputs["x"].device)
+    vt = (idx >= 0) & (idx < E)
+    involved = np.unique(idx[vt])
+    idx_t = np.where(vt, sub(involved)[np.clip(idx, 0, E - 1)], -1).astype(np.int32)
+    it, tt = torch.as_tensor(involved, device=dev), torch.as_tensor(toks, device=dev)
     W1t, W2t = bf16_bits(inputs["W1"][it]), bf16_bits(inputs["W2"][it])
     xt, dYt = bf16_bits(inputs["x"][tt]), bf16_bits(inputs["dY"][tt])
     wt = inputs["topk_w"][tt].cpu().numpy().astype(np.float32)
-    counts = np.bincount(idx_all.ravel()[idx_all.ravel() >= 0], minlength=E)
-    e = int(np.argsort(counts, kind="stable")[E // 2])  # median-loaded expert
-    remap_e = np.full(E, -1, np.int64)
-    remap_e[e] = 0
-    valid = (idx_all >= 0) & (idx_all < E)
-    idx_e = np.where(valid, remap_e[np.clip(idx_all, 0, E - 1)], -1).astype(np.int32)
-    et = torch.as_tensor([e], device=inputs["x"].device)
+    idx_e = np.where(valid, sub(exps)[np.clip(idx_all, 0, E - 1)], -1).astype(np.int32)
+    et = torch.as_tensor(exps, device=dev)
     W1e, W2e = bf16_bits(inputs["W1"][et]), bf16_bits(inputs["W2"][et])
     xa, dYa = bf16_bits(inputs["x"]), bf16_bits(inputs["dY"])
     wa = inputs["topk_w"].cpu().numpy().astype(np.float32)
@@ -192,11 +223,39 @@ def oracle_sample(shape, inputs, n_tok, seed=0, clamp=0.0):
         oracle.backward_tokens(xt, W1t, W2t, idx_t, wt, dYt, clamp=clamp)
         oracle.backward_experts(xa, W1e, W2e, idx_e, wa, dYa, clamp=clamp)
 
-    slots = int(((idx >= 0) & (idx < E)).sum())
-    flops = 6.0 * H * I * slots + 6.0 * H * I * slots + 6.0 * H * I * int(counts[e])
-    desc = (f"{n_tok} tokens ({slots} routed slots): forward, dx, d topk_weights; plus dW1/dW2 of one "
-            f"median-loaded expert ({int(counts[e])} rows); oracle FP32, useful FLOPs counted as in the metric")
+    slots = int(vt.sum())
+    rows = int(counts[exps].sum())
+    flops = 6.0 * H * I * slots + 6.0 * H * I * slots + 6.0 * H * I * rows
+    if whole:
+        desc = (f"the whole layer ({shape.T} tokens, {slots} routed slots, {E} experts) forward and backward; "
+                f"oracle FP32")
+    else:
+        desc = (f"{len(toks)} tokens ({slots} routed slots): forward, dx, d topk_weights; plus dW1/dW2 of "
+                f"{len(exps)} experts at load quantiles ({rows} rows); oracle FP32, useful FLOPs counted as in "
+                f"the metric")
     return run, flops, desc
+
+
+def time_oracle(shape, inputs, n_tok, n_exp, seconds, seed=0, clamp=0.0):
+    """The oracle on a bounded sample, repeated until `seconds` have passed
+    (at least once); its rate scaled to the whole step."""
+    import oracle
+
+    oracle.build()
+    run, flops, desc = oracle_sample(shape, inputs, n_tok=n_tok, n_exp=n_exp, seed=seed, clamp=clamp)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    rate = flops * reps / dt
+    step_flops = shape.flops_forward() + shape.flops_backward()
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "host_cores_available": cpu_cores(), "kind": "oracle", "sample": f"{reps} x ({desc})",
+            "seconds": dt, "extrapolated_full_step_s": step_flops / rate,
+            "extrapolated_note": "the whole layer step at the sample's FLOP rate (extrapolated, not run)"}
 
 
 def cpu_cores():
@@ -258,14 +317,187 @@ def run_reference(args):
     return 0
 
 
+FWD_KERNELS = ("route_hist", "route_scan", "route_place", "gemm_l1_fwd", "gemm_l2_fwd", "combine_fwd")
+# every other BASELINE workload, timed after the headline one, one at a time
+# (each one's buffers are freed before the next is drawn): (name, config,
+# backward, timed steps, oracle sample tokens, oracle sample experts)
+OTHER_CONFIGS = (("tiny", "tiny", True, 100, 64, 0), ("v2lite", "v2lite", True, 20, 32, 2),
+                 ("wide_fwd", "wide", False, 10, 8, 1), ("wide", "wide", True, 10, 8, 1),
+                 ("skew", "skew", True, 10, 16, 1))
+
+
+def roofline_of(name, shape, avg_ms, peaks, peaks_src, config_key):
+    """The kernel's roofline object: algorithmic bytes (or FLOPs) per launch
+    over its average live duration, against the HBM roof below the ridge
+    point of the measured peaks and the sustained tensor roof above it."""
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    flops = GEMM_FLOP_FACTOR[name] * H * I * shape.slots
+    nbytes = gemm_alg_bytes(name, T, H, I, E, k)
+    sec = avg_ms / 1e3
+    ridge = float(peaks["bf16_tflops_sustained"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            ent = json.load(f).get(config_key, {}).get(name)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            traffic = ent["bytes_per_launch"]
+    if flops / nbytes < ridge:
+        achieved, peak = nbytes / sec / 1e9, float(peaks["hbm_gbs"])
+        r = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak, "unit": "GB/s",
+             "frac": achieved / peak, "traffic": traffic, "peak_source": f"hbm_gbs ({peaks_src}, copy bandwidth)"}
+    else:
+        achieved, peak = flops / sec / 1e12, float(peaks["bf16_tflops_sustained"])
+        r = {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+             "frac": achieved / peak, "traffic": traffic,
+             "peak_source": f"bf16_tflops_sustained ({peaks_src}); burst {float(peaks['bf16_tflops']):.1f}"}
+    r.update({"algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+              "planned_bytes_per_launch": gemm_planned_bytes(name, T, H, I, E, k),
+              "arithmetic_intensity": flops / nbytes, "ridge_flop_per_byte": ridge,
+              "achieved_tflops": flops / sec / 1e12, "achieved_gbs": nbytes / sec / 1e9})
+    return r
+
+
+class LayerBench:
+    """Device buffers of one workload and its timed steps (prologue +
+    forward, and backward unless forward-only) through the C ABI."""
+
+    def __init__(self, shape, dev, seed, activation_clamp=0.0, backward=True):
+        from routed_grouped_gemm_routing_gb300.layer import MoEWorkspace
+        from routed_grouped_gemm_routing_gb300.workloads import make_layer_inputs
+
+        import torch
+
+        self.shape, self.backward = shape, backward
+        T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+        self.inp = make_layer_inputs(shape, seed=seed, device=dev, with_grad_out=backward)
+        self.ws = MoEWorkspace(T, H, I, E, k, device=dev, activation_clamp=activation_clamp)
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        if backward:
+            self.dx = torch.empty_like(self.y)
+            self.dW1 = torch.empty_like(self.inp["W1"])
+            self.dW2 = torch.empty_like(self.inp["W2"])
+            self.dw = torch.empty(T, k, dtype=torch.float32, device=dev)
+
+    def step(self):
+        from routed_grouped_gemm_routing_gb300 import binding as B
+
+        s, inp, ws = self.ws.shape, self.inp, self.ws
+        B.moe_route_prologue(s, inp["topk_idx"], ws.route)
+        B.moe_forward(s, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, self.y)
+        if self.backward:
+            B.moe_backward(s, inp["dY"], inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved,
+                           ws.bwd, self.dx, self.dW1, self.dW2, self.dw)
+
+    def check_status(self, when):
+        from routed_grouped_gemm_routing_gb300 import binding as B
+
+        status = B.moe_read_status(self.ws.shape, self.ws.route)
+        if status[B.STATUS_FLAGS] != 0:
+            raise RuntimeError(f"kernel status flags {status[B.STATUS_FLAGS]:#x} {when}")
+
+    def timed(self, steps, warmup, world, dev, clock_index):
+        """Warm-up, then `steps` steps between CUDA events on the launching
+        stream (barrier + synchronize on both sides), every launch bracketed
+        by the library's trace events.  Returns (max-over-ranks ms, trace,
+        clocks)."""
+        import torch
+        import torch.distributed as dist
+
+        from routed_grouped_gemm_routing_gb300 import binding as B
+
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        self.check_status("after warm-up")
+        trace = B.KernelTrace(max_launches=16 * steps)
+        clocks = ClockSampler(clock_index)
+        clocks.start()
+        time.sleep(0.3)
+        stream = torch.cuda.current_stream()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        with trace:
+            for _ in range(steps):
+                self.step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        clk = clocks.stop()
+        self.check_status("in the timed region")
+        return max_over_ranks(t0.elapsed_time(t1), world, dev), trace, clk
+
+    def summary(self, ms, trace, steps, world, peaks, peaks_src, config_key):
+        """Rates, per-kernel times, the forward / backward split and the
+        dominant GEMM's roofline of a timed run."""
+        shape = self.shape
+        flops_step = shape.flops_forward() + (shape.flops_backward() if self.backward else 0.0)
+        value = job_rate(flops_step, steps, world, ms) / 1e12
+        per = {}
+        for name, d in trace.durations_ms():
+            per.setdefault(name, []).append(d)
+        kernels = {n: {"launches": len(v), "avg_ms": statistics.mean(v), "total_ms": sum(v),
+                       "share": sum(v) / ms} for n, v in per.items()}
+        gemms = {n: v for n, v in kernels.items() if n in GEMM_FLOP_FACTOR}
+        dom = max(gemms, key=lambda n: gemms[n]["total_ms"])
+        return {
+            "ms_per_step": ms / steps, "value": value, "unit": "TFLOP/s",
+            "routed_tokens_per_s": job_rate(shape.slots, steps, world, ms),
+            "pct_bf16_peak_burst": 100.0 * value / world / float(peaks["bf16_tflops"]),
+            "pct_bf16_peak_sustained": 100.0 * value / world / float(peaks["bf16_tflops_sustained"]),
+            "forward_ms": sum(v["avg_ms"] for n, v in kernels.items() if n in FWD_KERNELS),
+            "backward_ms": sum(v["avg_ms"] for n, v in kernels.items() if n not in FWD_KERNELS),
+            "gpu_launches": int(trace.count), "launches_per_step": trace.count / steps,
+            "kernels": kernels,
+            "roofline": roofline_of(dom, shape, gemms[dom]["avg_ms"], peaks, peaks_src, config_key),
+        }
+
+
+def run_other_configs(args, dev, world, rank, peaks, peaks_src):
+    """Every other BASELINE workload on this GPU, one after another; the
+    V3-shaped headline's buffers are already freed."""
+    import numpy as np
+    import torch
+
+    from routed_grouped_gemm_routing_gb300.workloads import CONFIGS
+
+    out = {}
+    for key, cname, backward, steps, n_tok, n_exp in OTHER_CONFIGS:
+        shape = CONFIGS[cname]
+        lb = LayerBench(shape, dev, args.seed + rank, backward=backward)
+        ms, trace, clk = lb.timed(steps, max(3, args.warmup), world, dev, dev.index if world == 1 else
+                                  int(os.environ.get("LOCAL_RANK", "0")))
+        r = lb.summary(ms, trace, steps, world, peaks, peaks_src, cname)
+        r.pop("kernels")
+        r.update({"config": config_dict(shape, world), "steps": steps, "clocks": clk,
+                  "step": "prologue + forward + backward" if backward else "prologue + forward (forward only)"})
+        counts = np.bincount(lb.inp["topk_idx"].flatten().cpu().numpy(), minlength=shape.E)
+        r["expert_load"] = {"min": int(counts.min()), "mean": float(counts.mean()), "max": int(counts.max()),
+                            "below_block_m": int(((counts > 0) & (counts < 128)).sum()),
+                            "empty": int((counts == 0).sum()), "top5": sorted(counts.tolist())[-5:][::-1]}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and backward:
+            whole = n_exp == 0
+            r["cpu_baseline"] = time_oracle(shape, lb.inp, n_tok=shape.T if whole else n_tok,
+                                            n_exp=max(1, n_exp), seconds=2.0, seed=args.seed)
+        out[key] = r
+        del lb, trace
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     from routed_grouped_gemm_routing_gb300 import binding as B
     from routed_grouped_gemm_routing_gb300 import build
-    from routed_grouped_gemm_routing_gb300.layer import HostPipeline, MoEWorkspace
-    from routed_grouped_gemm_routing_gb300.workloads import CONFIGS, make_layer_inputs
+    from routed_grouped_gemm_routing_gb300.layer import HostPipeline
+    from routed_grouped_gemm_routing_gb300.workloads import CONFIGS
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -282,98 +514,11 @@ def run_ours(args):
 
     shape = CONFIGS[args.config]
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
-    inp = make_layer_inputs(shape, seed=args.seed + rank, device=dev)
-    ws = MoEWorkspace(T, H, I, E, k, device=dev, activation_clamp=args.activation_clamp)
-    s = ws.shape
-    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    dx = torch.empty_like(y)
-    dW1 = torch.empty_like(inp["W1"])
-    dW2 = torch.empty_like(inp["W2"])
-    dw = torch.empty(T, k, dtype=torch.float32, device=dev)
-
-    def step():
-        B.moe_route_prologue(s, inp["topk_idx"], ws.route)
-        B.moe_forward(s, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
-        B.moe_backward(s, inp["dY"], inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, ws.bwd,
-                       dx, dW1, dW2, dw)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    status = B.moe_read_status(s, ws.route)
-    if status[B.STATUS_FLAGS] != 0:
-        raise RuntimeError(f"kernel status flags {status[B.STATUS_FLAGS]:#x} after warm-up")
-
-    # timed region: K steps, every kernel bracketed by events for per-kernel times
-    trace = B.KernelTrace(max_launches=16 * args.steps)
-    clocks = ClockSampler(dev.index if world == 1 else local)
-    clocks.start()
-    time.sleep(0.3)
-    stream = torch.cuda.current_stream()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    with trace:
-        for _ in range(args.steps):
-            step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    status = B.moe_read_status(s, ws.route)
-    if status[B.STATUS_FLAGS] != 0:
-        raise RuntimeError(f"kernel status flags {status[B.STATUS_FLAGS]:#x} in the timed region")
-
+    lb = LayerBench(shape, dev, args.seed + rank, activation_clamp=args.activation_clamp)
+    ms, trace, clk = lb.timed(args.steps, args.warmup, world, dev, dev.index if world == 1 else local)
+    head = lb.summary(ms, trace, args.steps, world, peaks, peaks_src, args.config)
+    inp, ws, y = lb.inp, lb.ws, lb.y
     flops_step = shape.flops_forward() + shape.flops_backward()
-    value = job_rate(flops_step, args.steps, world, ms) / 1e12
-    tok_s = job_rate(shape.slots, args.steps, world, ms)
-
-    # per-kernel device times (rank-local)
-    per = {}
-    for name, d in trace.durations_ms():
-        per.setdefault(name, []).append(d)
-    launches_per_step = trace.count / args.steps
-    kernels = {n: {"launches": len(v), "avg_ms": statistics.mean(v), "total_ms": sum(v),
-                   "share": sum(v) / ms} for n, v in per.items()}
-    fwd_names = ("route_hist", "route_scan", "route_place", "gemm_l1_fwd", "gemm_l2_fwd", "combine_fwd")
-    forward_ms = sum(v["avg_ms"] for n, v in kernels.items() if n in fwd_names)
-    backward_ms = sum(v["avg_ms"] for n, v in kernels.items() if n not in fwd_names)
-    gemms = {n: v for n, v in kernels.items() if n in GEMM_FLOP_FACTOR}
-    dom = max(gemms, key=lambda n: gemms[n]["total_ms"])
-    dom_flops = GEMM_FLOP_FACTOR[dom] * H * I * shape.slots
-    dom_bytes = gemm_alg_bytes(dom, T, H, I, E, k)
-    dom_s = gemms[dom]["avg_ms"] / 1e3
-    # the kernel's roof: HBM below the ridge point of the measured peaks, tensor above it
-    ridge = float(peaks["bf16_tflops_sustained"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-    hbm_bound = dom_flops / dom_bytes < ridge
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            tj = json.load(f)
-        ent = tj.get(args.config, {}).get(dom)
-        if ent and ent.get("source_hash") == kernel_source_hash():
-            traffic = ent["bytes_per_launch"]
-    if hbm_bound:
-        achieved = dom_bytes / dom_s / 1e9
-        peak = float(peaks["hbm_gbs"])
-        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": traffic,
-                    "peak_source": f"hbm_gbs ({peaks_src}, copy bandwidth)"}
-    else:
-        achieved = dom_flops / dom_s / 1e12
-        peak = float(peaks["bf16_tflops_sustained"])
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": traffic,
-                    "peak_source": f"bf16_tflops_sustained ({peaks_src}); burst {float(peaks['bf16_tflops']):.1f}"}
-    roofline.update({"algorithmic_bytes_per_launch": dom_bytes, "algorithmic_flops_per_launch": dom_flops,
-                     "arithmetic_intensity": dom_flops / dom_bytes, "ridge_flop_per_byte": ridge,
-                     "achieved_tflops": dom_flops / dom_s / 1e12, "achieved_gbs": dom_bytes / dom_s / 1e9})
 
     # the same step captured once in a CUDA graph and replayed (every launch
     # of the step is capturable: no host synchronisation, no allocation)
@@ -382,12 +527,12 @@ def run_ours(args):
         gs = torch.cuda.Stream()
         gs.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(gs):
-            step()
+            lb.step()
         torch.cuda.current_stream().wait_stream(gs)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            step()
+            lb.step()
         for _ in range(2):
             g.replay()
         torch.cuda.synchronize()
@@ -409,7 +554,7 @@ def run_ours(args):
         outs = {"y_h": torch.empty(T, H, dtype=torch.bfloat16).pin_memory(),
                 "dx_h": torch.empty(T, H, dtype=torch.bfloat16).pin_memory(),
                 "dw_h": torch.empty(T, k, dtype=torch.float32).pin_memory()}
-        pipe = HostPipeline(ws, inp["W1"], inp["W2"], dW1, dW2)
+        pipe = HostPipeline(ws, inp["W1"], inp["W2"], lb.dW1, lb.dW2)
 
         def e2e_step():
             pipe.submit(host["x"], host["topk_idx"], host["topk_w"], host["dY"], outs["y_h"], outs["dx_h"],
@@ -437,6 +582,7 @@ def run_ours(args):
                "note": "x, topk_idx, topk_weights, dY copied in from pinned host memory and y, dx, "
                        "d topk_weights copied out every step (HostPipeline: uploads of step n+1 and downloads "
                        "of step n overlap the kernels); dW1/dW2 stay on the device"}
+        del pipe
 
     # the router stage in front of the layer (logits -> top-k ids and weights
     # -> routing tables), timed on its own: it is not part of the layer step
@@ -508,48 +654,39 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
+        cpu = time_oracle(shape, inp, n_tok=args.cpu_tokens, n_exp=args.cpu_experts, seconds=args.cpu_seconds,
+                          seed=args.seed, clamp=args.activation_clamp)
 
-        oracle.build()
-        run, flops, desc = oracle_sample(shape, inp, n_tok=args.cpu_tokens, seed=args.seed,
-                                         clamp=args.activation_clamp)
-        reps, t0 = 0, time.perf_counter()
-        while True:
-            run()
-            reps += 1
-            if time.perf_counter() - t0 >= args.cpu_seconds:
-                break
-        dt = time.perf_counter() - t0
-        cpu = {"value": flops * reps / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-               "host_cores_available": cpu_cores(), "kind": "oracle", "sample": f"{reps} x ({desc})",
-               "seconds": dt,
-               "extrapolated_full_step_s": flops_step / (flops * reps / dt),
-               "extrapolated_note": "the whole layer step at the sample's FLOP rate (extrapolated, not run)"}
+    del lb, inp, ws, y
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    others = None if args.no_configs else run_other_configs(args, dev, world, rank, peaks, peaks_src)
 
     if rank != 0:
         dist.destroy_process_group()
         return 0
     line = {
         "metric": METRIC,
-        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms / args.steps, "forward_ms": forward_ms, "backward_ms": backward_ms,
+        "value": head["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "forward_ms": head["forward_ms"], "backward_ms": head["backward_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded Gaussian inputs and weights, Gaussian-logit top-k routing)",
         "config": config_dict(shape, world, args.activation_clamp),
-        "routed_tokens_per_s": tok_s,
-        "pct_bf16_peak_burst": 100.0 * value / world / float(peaks["bf16_tflops"]),
-        "pct_bf16_peak_sustained": 100.0 * value / world / float(peaks["bf16_tflops_sustained"]),
+        "routed_tokens_per_s": head["routed_tokens_per_s"],
+        "pct_bf16_peak_burst": head["pct_bf16_peak_burst"],
+        "pct_bf16_peak_sustained": head["pct_bf16_peak_sustained"],
         "peaks_source": peaks_src,
         "clocks": clk,
-        "gpu_launches": int(trace.count),
-        "launches_per_step": launches_per_step,
-        "kernels": kernels,
-        "roofline": roofline,
+        "gpu_launches": head["gpu_launches"],
+        "launches_per_step": head["launches_per_step"],
+        "kernels": head["kernels"],
+        "roofline": head["roofline"],
         "e2e": e2e,
         "graph": graph,
         "cpu_baseline": cpu,
         "router": router,
         "fp8_forward": fp8,
+        "configs": others,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -572,8 +709,10 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--activation-clamp", type=float, default=0.0,
                     help="SwiGLU input clamp c > 0 (0: none, the default workload)")
-    ap.add_argument("--cpu-tokens", type=int, default=4)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--cpu-experts", type=int, default=2)
+    ap.add_argument("--cpu-seconds", type=float, default=5.0)
     ap.add_argument("--ref-tokens", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
