@@ -472,7 +472,7 @@ def run_other_configs(args, dev, world, rank, peaks, peaks_src):
         ms, trace, clk = lb.timed(steps, max(3, args.warmup), world, dev, dev.index if world == 1 else
                                   int(os.environ.get("LOCAL_RANK", "0")))
         r = lb.summary(ms, trace, steps, world, peaks, peaks_src, cname)
-        r.pop("kernels")
+        r["kernels_ms"] = {n: v["avg_ms"] for n, v in r.pop("kernels").items()}
         r.update({"config": config_dict(shape, world), "steps": steps, "clocks": clk,
                   "step": "prologue + forward + backward" if backward else "prologue + forward (forward only)"})
         counts = np.bincount(lb.inp["topk_idx"].flatten().cpu().numpy(), minlength=shape.E)

@@ -9,9 +9,9 @@
 // A work unit is (expert e, stationary tile s): 256 features of H, 128 in
 // each CTA of a 2-CTA cluster.  Each CTA gathers its 128 features of the
 // token operand (x for dW1, dY for dW2) for all of the expert's routed rows
-// ONCE into a shared-memory slab (up to kWSlabKb 64-row K blocks), and then
+// ONCE into a shared-memory slab (up to S 64-row K blocks), and then
 // streams the other operand (dh for dW1, aw for dW2) by TMA, 128 of its
-// features per CTA at a time, through a kWStages ring.  For every streamed
+// features per CTA at a time, through an 11 - S stage ring.  For every streamed
 // tile t the pair issues M=256 x N=256 MMAs over the expert's rows:
 //   dW1: A = slab (M = H features), B = dh (N = 2I features)
 //   dW2: A = aw   (M = I features), B = slab (N = H features)
@@ -21,8 +21,8 @@
 // tile (16x fewer gathered bytes for dW1, 8x for dW2), and each SM streams
 // 16 KiB per K block instead of 48 KiB.
 //
-// Experts with more rows than the slab holds run K in chunks of kWSlabKb
-// blocks, the slab gathered again for every (tile, chunk).  An expert
+// Experts with more rows than the slab holds run K in chunks of S blocks,
+// the slab gathered again for every round of tiles (w_group).  An expert
 // without routed rows gets zeros.
 //
 // The streamed tiles of a unit start at tile (s mod T) so that the clusters
@@ -44,38 +44,49 @@
 
 namespace moe {
 
-constexpr int kWSlabKb = 5;                  // slab capacity in 64-row K blocks (320 routed rows)
-constexpr int kWStages = 6;                  // streamed-operand ring
+// Eleven 16 KiB operand blocks per CTA, S of them for the slab (S 64-row K
+// blocks: 64 S routed rows) and 11 - S for the streamed ring.  S = 5 (320
+// rows, 6 ring stages) unless the shape's mean rows per expert, T k / E,
+// exceed 320; then S = 7 (448 rows, 4 stages), so that such experts fit the
+// slab (a 4-stage ring starves the 256-row experts of the V3-shaped layer,
+// measured: dW1 3.2 -> 4.0 ms; 7 slab blocks cut the V2-Lite-shaped
+// layer's dW1 0.30 -> 0.24 ms and dW2 0.17 -> 0.12 ms).
+constexpr int kWBlocks = 11;
 constexpr int kWBlockBytes = 128 * kBK * 2;  // 16 KiB: 128 features x 64 rows, MN-major, 128B swizzle
-constexpr int kWNumBars = 3 * kWSlabKb + 2 * kWStages + 5;
+constexpr int kWSlabSmall = 5, kWSlabLarge = 7;
 constexpr int kWTailBytes = 512;
-static_assert(8 * kWNumBars + 8 <= kWTailBytes, "barrier area");
-constexpr int kWSmemBytes = 1024 + (kWSlabKb + kWStages) * kWBlockBytes + kEpiWarps * kStageEpiBytes + kWTailBytes;
+static_assert(8 * (3 * kWSlabLarge + 2 * (kWBlocks - kWSlabLarge) + 5) + 8 <= kWTailBytes &&
+                  8 * (3 * kWSlabSmall + 2 * (kWBlocks - kWSlabSmall) + 5) + 8 <= kWTailBytes,
+              "barrier area");
+constexpr int kWSmemBytes = 1024 + kWBlocks * kWBlockBytes + kEpiWarps * kStageEpiBytes + kWTailBytes;
 static_assert(kWSmemBytes <= 232448, "shared memory per CTA");
 
+template <int S>
 struct WBars {
+    static constexpr int kSlab = S, kStages = kWBlocks - S;
+    static constexpr int kNum = 3 * kSlab + 2 * kStages + 5;  // barriers
     uint32_t base;
     __device__ __forceinline__ uint32_t slab_full(int i) const { return base + 8u * i; }
-    __device__ __forceinline__ uint32_t peer_slab_full(int i) const { return base + 8u * (kWSlabKb + i); }
-    __device__ __forceinline__ uint32_t slab_empty(int i) const { return base + 8u * (2 * kWSlabKb + i); }
+    __device__ __forceinline__ uint32_t peer_slab_full(int i) const { return base + 8u * (kSlab + i); }
+    __device__ __forceinline__ uint32_t slab_empty(int i) const { return base + 8u * (2 * kSlab + i); }
     // full: the even CTA's barrier counts both CTAs' bytes of a stage
-    __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * (3 * kWSlabKb + s); }
-    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (3 * kWSlabKb + kWStages + s); }
-    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kWSlabKb + 2 * kWStages + a); }
+    __device__ __forceinline__ uint32_t full(int s) const { return base + 8u * (3 * kSlab + s); }
+    __device__ __forceinline__ uint32_t empty(int s) const { return base + 8u * (3 * kSlab + kStages + s); }
+    __device__ __forceinline__ uint32_t tfull(int a) const { return base + 8u * (3 * kSlab + 2 * kStages + a); }
     __device__ __forceinline__ uint32_t tempty(int a) const {
-        return base + 8u * (3 * kWSlabKb + 2 * kWStages + 2 + a);
+        return base + 8u * (3 * kSlab + 2 * kStages + 2 + a);
     }
-    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kWSlabKb + 2 * kWStages + 4); }
+    __device__ __forceinline__ uint32_t drain() const { return base + 8u * (3 * kSlab + 2 * kStages + 4); }
 };
 
-// Shape of one unit.  S = stationary tiles per expert (over H), T = streamed
-// tiles (over 2I for dW1, over I for dW2).
+// Shape of one unit (an expert's stationary tile; its streamed tiles run over
+// 2I for dW1, over I for dW2).
 struct WUnit {
     int e, s;
     int off;  // first routed row of the expert
     int cnt;  // routed rows of the expert
     int nkb;  // 64-row K blocks
-    int nch;  // K chunks of at most kWSlabKb blocks
+    int nch;  // K chunks of at most S blocks (the slab)
 };
 
 // Experts in decreasing order of routed rows (ties by id), built in shared
@@ -95,6 +106,7 @@ __device__ __forceinline__ const int32_t* w_order_smem() {
 // routing every cluster gets a similar share of the rows; all roles of a
 // CTA walk the same sequence.  The next unit's count and offset are read
 // while the current one runs.
+template <int S>
 struct WWalk {
     const GemmArgs& p;
     const int32_t* order;  // experts by decreasing count
@@ -125,7 +137,7 @@ struct WWalk {
         w.cnt = cnt;
         w.off = off;
         w.nkb = (cnt + kBK - 1) / kBK;
-        w.nch = (w.nkb + kWSlabKb - 1) / kWSlabKb;
+        w.nch = (w.nkb + S - 1) / S;
         const int nxt = map(n + 1);
         if (nxt < total) load(nxt);
         return w;
@@ -136,39 +148,76 @@ struct WWalk {
     }
 };
 
+// Streamed tiles per slab round.  An expert whose rows fit the slab gathers
+// it once for all its tiles.  A longer one gathers each chunk of its rows
+// again for every round: per tile when it has two chunks (groups of one
+// tile keep the two TMEM accumulators double-buffered), per pair of tiles
+// from three chunks on (the pair accumulates in both accumulators side by
+// side, so the gathered bytes halve while the epilogue no longer overlaps
+// the pair's MMAs, which then take long anyway).  Measured with skewed
+// routing (top expert 5649 rows): dW1 4.75 -> 4.42 ms, dW2 2.34 -> 2.22 ms.
+__device__ __forceinline__ int w_group(const WUnit& u) { return u.nch > 2 ? 2 : 1; }
+
 // K blocks [kb0, kb1) of chunk c.
-__device__ __forceinline__ int w_kb0(int c) { return c * kWSlabKb; }
-__device__ __forceinline__ int w_kb1(const WUnit& u, int c) { return min(u.nkb, (c + 1) * kWSlabKb); }
+template <int S>
+__device__ __forceinline__ int w_kb0(int c) { return c * S; }
+template <int S>
+__device__ __forceinline__ int w_kb1(const WUnit& u, int c) { return min(u.nkb, (c + 1) * S); }
 
 // ------------------------------------------------------------ TMA producer
 // Streamed operand: 128 features (this CTA's half of the tile's 256) x 64 rows
 // per K block, two 64 x 64 boxes, completing the even CTA's full barrier
 // (which the even CTA's producer arms with both CTAs' bytes).
-template <int F>
-__device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS, WBars bars, volatile int* abort,
+template <int F, int S>
+__device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS, WBars<S> bars, volatile int* abort,
                            int rank) {
     int stage = 0;
     uint32_t phase = 0;
     const int T = p.n_tiles;
-    for (WWalk w(p); w.valid(); w.next()) {
+    for (WWalk<S> w(p); w.valid(); w.next()) {
         const WUnit u = w.take();
-        for (int t = 0; t < T; ++t) {
-            const int tt = (t + u.s) % T;  // streamed tiles rotated per stationary tile
-            const int f0 = tt * 256 + 128 * rank;
+        const int G = w_group(u);
+        if (G == 1) {
+            for (int t = 0; t < T; ++t) {
+                const int tt = (t + u.s) % T;  // streamed tiles rotated per stationary tile
+                const int f0 = tt * 256 + 128 * rank;
+                for (int kb = 0; kb < u.nkb; ++kb) {
+                    if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                    if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * kWBlockBytes);
+                    const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
+                    const uint32_t dst = sS + stage * kWBlockBytes;
+                    // the expert's streamed rows are read again by the other
+                    // stationary tiles' clusters: keep them in L2 against the
+                    // stream of weight-gradient stores (stored evict-first)
+                    const uint64_t pol = l2_policy_evict_last();
+                    tma_load_2d_pair_hint(dst, mS, f0, u.off + kb * kBK, fb, pol);
+                    tma_load_2d_pair_hint(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb, pol);
+                    if (++stage == WBars<S>::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            continue;
+        }
+        // paired tiles: for each K block, the block of both tiles in turn
+        for (int t0 = 0; t0 < T; t0 += G) {
+            const int nt = min(G, T - t0);
             for (int kb = 0; kb < u.nkb; ++kb) {
-                if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
-                if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * kWBlockBytes);
-                const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
-                const uint32_t dst = sS + stage * kWBlockBytes;
-                // the expert's streamed rows are read again by the other
-                // stationary tiles' clusters: keep them in L2 against the
-                // stream of weight-gradient stores (stored evict-first)
-                const uint64_t pol = l2_policy_evict_last();
-                tma_load_2d_pair_hint(dst, mS, f0, u.off + kb * kBK, fb, pol);
-                tma_load_2d_pair_hint(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb, pol);
-                if (++stage == kWStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                for (int j = 0; j < nt; ++j) {
+                    const int tt = (t0 + j + u.s) % T;
+                    const int f0 = tt * 256 + 128 * rank;
+                    if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+                    if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * kWBlockBytes);
+                    const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
+                    const uint32_t dst = sS + stage * kWBlockBytes;
+                    const uint64_t pol = l2_policy_evict_last();
+                    tma_load_2d_pair_hint(dst, mS, f0, u.off + kb * kBK, fb, pol);
+                    tma_load_2d_pair_hint(dst + 8192, mS, f0 + 64, u.off + kb * kBK, fb, pol);
+                    if (++stage == WBars<S>::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
@@ -181,8 +230,9 @@ __device__ void w_role_tma(const CUtensorMap* mS, const GemmArgs& p, uint32_t sS
 // the 128-byte-swizzled MN-major layout (row r of a 64-feature region at
 // r*128, chunk c at (c ^ (r & 7)) * 16); padding rows (perm = -1) and
 // features past H are zero-filled.
+template <int S>
 __device__ __forceinline__ void w_gather_round(const GemmArgs& p, const WUnit& u, int kb0, int kb1, uint32_t sL,
-                                               WBars bars, uint32_t& sphase, volatile int* abort, int gw, int lane,
+                                               WBars<S> bars, uint32_t& sphase, volatile int* abort, int gw, int lane,
                                                int rank, bool& ok) {
     constexpr int kRowsPerWarp = kBK / kGatherWarps;  // 8
     const int c = lane & 7;
@@ -191,12 +241,12 @@ __device__ __forceinline__ void w_gather_round(const GemmArgs& p, const WUnit& u
     const int rw0 = gw * kRowsPerWarp;
     const int col0 = u.s * 256 + 128 * rank;
     // permutation entries of this warp's rows in every block of the round
-    int ent[kWSlabKb];
+    int ent[S];
 #pragma unroll
-    for (int i = 0; i < kWSlabKb; ++i)
+    for (int i = 0; i < S; ++i)
         ent[i] = (kb0 + i < kb1) ? __ldg(p.perm + u.off + (kb0 + i) * kBK + rw0 + (lane & (kRowsPerWarp - 1))) : -1;
 #pragma unroll
-    for (int i = 0; i < kWSlabKb; ++i) {
+    for (int i = 0; i < S; ++i) {
         if (kb0 + i >= kb1) break;
         if (!warp_wait(bars.slab_empty(i), ((sphase >> i) & 1u) ^ 1u, abort)) {
             ok = false;
@@ -224,19 +274,20 @@ __device__ __forceinline__ void w_gather_round(const GemmArgs& p, const WUnit& u
     }
 }
 
-__device__ void w_role_gather(const GemmArgs& p, uint32_t sL, WBars bars, volatile int* abort, int gw, int lane,
+template <int S>
+__device__ void w_role_gather(const GemmArgs& p, uint32_t sL, WBars<S> bars, volatile int* abort, int gw, int lane,
                               int rank) {
     uint32_t sphase = 0;
     bool ok = true;
     const int T = p.n_tiles;
-    for (WWalk w(p); w.valid() && ok; w.next()) {
+    for (WWalk<S> w(p); w.valid() && ok; w.next()) {
         const WUnit u = w.take();
         if (u.nch == 1) {
-            w_gather_round(p, u, 0, u.nkb, sL, bars, sphase, abort, gw, lane, rank, ok);
+            w_gather_round<S>(p, u, 0, u.nkb, sL, bars, sphase, abort, gw, lane, rank, ok);
         } else {
-            for (int t = 0; t < T && ok; ++t)
+            for (int t0 = 0; t0 < T && ok; t0 += w_group(u))
                 for (int c = 0; c < u.nch && ok; ++c)
-                    w_gather_round(p, u, w_kb0(c), w_kb1(u, c), sL, bars, sphase, abort, gw, lane, rank, ok);
+                    w_gather_round<S>(p, u, w_kb0<S>(c), w_kb1<S>(u, c), sL, bars, sphase, abort, gw, lane, rank, ok);
         }
     }
 }
@@ -244,80 +295,143 @@ __device__ void w_role_gather(const GemmArgs& p, uint32_t sL, WBars bars, volati
 // -------------------------------------------------------------- MMA issuer
 // The whole MMA warp runs this loop: it waits warp-uniformly and one elected
 // lane issues the MMAs and their commits (see warp_wait_uniform).
-template <int F>
-__device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars bars, uint32_t tmem_base,
+template <int F, int S>
+__device__ void w_role_mma(const GemmArgs& p, uint32_t sL, uint32_t sS, WBars<S> bars, uint32_t tmem_base,
                            volatile int* abort) {
     constexpr uint32_t idesc = make_idesc_bf16(2 * kBM, 256, true, true);
     int stage = 0;
     uint32_t phase = 0, sphase = 0;
     int it = 0;
     const int T = p.n_tiles;
-    for (WWalk w(p); w.valid(); w.next()) {
+    for (WWalk<S> w(p); w.valid(); w.next()) {
         const WUnit u = w.take();
-        for (int t = 0; t < T; ++t, ++it) {
-            const int acc = it & 1;
-            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            if (!warp_wait_uniform<true>(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+        if (w_group(u) == 1) {
+            for (int t = 0; t < T; ++t, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+                if (!warp_wait_uniform<true>(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * 256);
+                for (int c = 0; c < u.nch; ++c) {
+                    const int kb0 = w_kb0<S>(c), kb1 = w_kb1<S>(u, c);
+                    // the slab blocks of this round are waited for on their first
+                    // use and released after their last one
+                    const bool first = u.nch > 1 || t == 0;
+                    const bool last = u.nch > 1 || t == T - 1;
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        const int i = kb - kb0;
+                        if (first) {
+                            if (!warp_wait_uniform<false>(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
+                            if (!warp_wait_uniform<true>(bars.peer_slab_full(i), (sphase >> i) & 1u, abort)) return;
+                        }
+                        if (!warp_wait_uniform<true>(bars.full(stage), phase, abort)) return;
+                        tc_fence_after();
+                        const uint32_t sl = sL + i * kWBlockBytes;
+                        const uint32_t st = sS + stage * kWBlockBytes;
+                        // descriptors of the block's first 16 rows; the next 16 rows
+                        // start 2048 bytes (128 descriptor units) further on
+                        const uint64_t ad = make_sdesc_sw128((F == DW1) ? sl : st, 8192, 1024);
+                        const uint64_t bd = make_sdesc_sw128((F == DW1) ? st : sl, 8192, 1024);
+                        // stop at the 16-row step that holds the expert's last row
+                        const int ksteps = min(kBK / 16, (u.cnt - kb * kBK + 15) / 16);
+                        if (elect_one()) {
+                            if (first) fence_proxy_async_smem();  // a slab block freshly written by cp.async
+    #pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                if (kk >= ksteps) break;
+                                tc_mma_bf16_pair(d, ad + 128u * kk, bd + 128u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            }
+                            tc_commit_pair(bars.empty(stage));
+                            if (last) tc_commit_pair(bars.slab_empty(i));
+                        }
+                        __syncwarp();
+                        if (last) sphase ^= 1u << i;
+                        if (++stage == WBars<S>::kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (elect_one()) tc_commit_pair(bars.tfull(acc));
+                __syncwarp();
+            }
+            continue;
+        }
+        // an expert of three or more slab chunks: its tiles go in pairs (see w_group)
+        const int G = 2;
+        for (int t0 = 0; t0 < T; t0 += G) {
+            const int nt = min(G, T - t0);
+            // tiles it .. it + nt - 1 accumulate side by side (acc = it & 1)
+            for (int j = 0; j < nt; ++j)
+                if (!warp_wait_uniform<true>(bars.tempty((it + j) & 1), ((uint32_t)((it + j) >> 1) & 1u) ^ 1u, abort))
+                    return;
             tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)(acc * 256);
             for (int c = 0; c < u.nch; ++c) {
-                const int kb0 = w_kb0(c), kb1 = w_kb1(u, c);
+                const int kb0 = w_kb0<S>(c), kb1 = w_kb1<S>(u, c);
                 // the slab blocks of this round are waited for on their first
                 // use and released after their last one
-                const bool first = u.nch > 1 || t == 0;
-                const bool last = u.nch > 1 || t == T - 1;
+                const bool first = u.nch > 1 || t0 == 0;
+                const bool last = u.nch > 1 || t0 + nt == T;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     const int i = kb - kb0;
                     if (first) {
                         if (!warp_wait_uniform<false>(bars.slab_full(i), (sphase >> i) & 1u, abort)) return;
                         if (!warp_wait_uniform<true>(bars.peer_slab_full(i), (sphase >> i) & 1u, abort)) return;
                     }
-                    if (!warp_wait_uniform<true>(bars.full(stage), phase, abort)) return;
-                    tc_fence_after();
-                    const uint32_t sl = sL + i * kWBlockBytes;
-                    const uint32_t st = sS + stage * kWBlockBytes;
-                    // descriptors of the block's first 16 rows; the next 16 rows
-                    // start 2048 bytes (128 descriptor units) further on
-                    const uint64_t ad = make_sdesc_sw128((F == DW1) ? sl : st, 8192, 1024);
-                    const uint64_t bd = make_sdesc_sw128((F == DW1) ? st : sl, 8192, 1024);
                     // stop at the 16-row step that holds the expert's last row
                     const int ksteps = min(kBK / 16, (u.cnt - kb * kBK + 15) / 16);
-                    if (elect_one()) {
-                        if (first) fence_proxy_async_smem();  // a slab block freshly written by cp.async
+                    const uint32_t sl = sL + i * kWBlockBytes;
+                    for (int j = 0; j < nt; ++j) {
+                        if (!warp_wait_uniform<true>(bars.full(stage), phase, abort)) return;
+                        tc_fence_after();
+                        const uint32_t st = sS + stage * kWBlockBytes;
+                        const uint32_t d = tmem_base + (uint32_t)(((it + j) & 1) * 256);
+                        // descriptors of the block's first 16 rows; the next 16 rows
+                        // start 2048 bytes (128 descriptor units) further on
+                        const uint64_t ad = make_sdesc_sw128((F == DW1) ? sl : st, 8192, 1024);
+                        const uint64_t bd = make_sdesc_sw128((F == DW1) ? st : sl, 8192, 1024);
+                        if (elect_one()) {
+                            if (first && j == 0) fence_proxy_async_smem();  // a slab block freshly written by cp.async
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            if (kk >= ksteps) break;
-                            tc_mma_bf16_pair(d, ad + 128u * kk, bd + 128u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                if (kk >= ksteps) break;
+                                tc_mma_bf16_pair(d, ad + 128u * kk, bd + 128u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            }
+                            tc_commit_pair(bars.empty(stage));
+                            if (last && j == nt - 1) tc_commit_pair(bars.slab_empty(i));
                         }
-                        tc_commit_pair(bars.empty(stage));
-                        if (last) tc_commit_pair(bars.slab_empty(i));
+                        __syncwarp();
+                        if (++stage == WBars<S>::kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    __syncwarp();
                     if (last) sphase ^= 1u << i;
-                    if (++stage == kWStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
             }
-            if (elect_one()) tc_commit_pair(bars.tfull(acc));
+            for (int j = 0; j < nt; ++j)
+                if (elect_one()) tc_commit_pair(bars.tfull((it + j) & 1));
             __syncwarp();
+            it += nt;
         }
     }
 }
 
 // The odd CTA's MMA thread: tells the even CTA that this CTA's half of a
 // slab block is in shared memory, in the order the MMA uses the blocks.
-__device__ void w_role_relay(const GemmArgs& p, WBars bars, volatile int* abort) {
+template <int S>
+__device__ void w_role_relay(const GemmArgs& p, WBars<S> bars, volatile int* abort) {
     uint32_t sphase = 0;
     const int T = p.n_tiles;
-    for (WWalk w(p); w.valid(); w.next()) {
+    for (WWalk<S> w(p); w.valid(); w.next()) {
         const WUnit u = w.take();
-        for (int t = 0; t < T; ++t) {
+        const int G = w_group(u);
+        for (int t0 = 0; t0 < T; t0 += G) {
+            const int nt = min(G, T - t0);
             for (int c = 0; c < u.nch; ++c) {
-                const int kb0 = w_kb0(c), kb1 = w_kb1(u, c);
-                const bool first = u.nch > 1 || t == 0;
-                const bool last = u.nch > 1 || t == T - 1;
+                const int kb0 = w_kb0<S>(c), kb1 = w_kb1<S>(u, c);
+                const bool first = u.nch > 1 || t0 == 0;
+                const bool last = u.nch > 1 || t0 + nt == T;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     const int i = kb - kb0;
                     if (first) {
@@ -338,8 +452,8 @@ __device__ void w_role_relay(const GemmArgs& p, WBars bars, volatile int* abort)
 // kMG (FP32 main-grad accumulation): eight 32 x 32 FP32 boxes instead, each
 // added element-wise to the caller's FP32 gradient by a TMA reduce-add; an
 // expert without routed rows adds nothing.
-template <int F, bool kMG>
-__device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars bars, uint32_t tmem_base,
+template <int F, bool kMG, int S>
+__device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars<S> bars, uint32_t tmem_base,
                                 uint32_t stage, volatile int* abort, int warp, int lane, int rank) {
     const uint32_t tempty_leader[2] = {cluster_addr_of(bars.tempty(0), 0), cluster_addr_of(bars.tempty(1), 0)};
     const int T = p.n_tiles;
@@ -348,7 +462,7 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars 
     const int cols_out = (F == DW1) ? 2 * p.I : p.H;
     int it = 0;
     uint32_t nstore = 0;
-    for (WWalk w(p); w.valid(); w.next()) {
+    for (WWalk<S> w(p); w.valid(); w.next()) {
         const WUnit u = w.take();
         for (int t = 0; t < T; ++t, ++it) {
             const int acc = it & 1;
@@ -430,7 +544,7 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars 
 // mapS: the streamed operand (dh for dW1, aw for dW2), box 64 x 64;
 // mapC: the weight gradient [E][rows][cols], bf16 box 64 x 32 (kMG: the FP32
 // main gradient, box 32 x 32).
-template <int F, bool kMG>
+template <int F, bool kMG, int S>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_wgrad_pair_kernel(const __grid_constant__ CUtensorMap mapS, const __grid_constant__ CUtensorMap mapC,
                           const GemmArgs p) {
@@ -438,25 +552,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const uint32_t sL = base;                               // slab: kWSlabKb blocks
-    const uint32_t sS = sL + kWSlabKb * kWBlockBytes;       // streamed ring: kWStages blocks
-    const uint32_t sE = sS + kWStages * kWBlockBytes;       // epilogue staging
+    const uint32_t sL = base;                               // slab: S blocks
+    const uint32_t sS = sL + S * kWBlockBytes;              // streamed ring: 11 - S blocks
+    const uint32_t sE = base + kWBlocks * kWBlockBytes;     // epilogue staging
     const uint32_t bar_base = sE + kEpiWarps * kStageEpiBytes;
     uint8_t* tail = base_ptr + (bar_base - base);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * kWNumBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * WBars<S>::kNum);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const WBars bars{bar_base};
+    const WBars<S> bars{bar_base};
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rank = (int)cluster_ctarank();
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kWSlabKb; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(bars.slab_full(i), 32u * kGatherWarps);
             mbar_init(bars.peer_slab_full(i), 1);
             mbar_init(bars.slab_empty(i), 1);
         }
-        for (int s = 0; s < kWStages; ++s) {
+        for (int s = 0; s < WBars<S>::kStages; ++s) {
             mbar_init(bars.full(s), 1);
             mbar_init(bars.empty(s), 1);
         }
@@ -500,13 +614,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == kWarpTma) {
-        if (lane == 0) w_role_tma<F>(&mapS, p, sS, bars, abort, rank);
+        if (lane == 0) w_role_tma<F, S>(&mapS, p, sS, bars, abort, rank);
     } else if (warp >= kWarpGather0) {
-        w_role_gather(p, sL, bars, abort, warp - kWarpGather0, lane, rank);
+        w_role_gather<S>(p, sL, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
         if (rank == 0) {
-            w_role_mma<F>(p, sL, sS, bars, tmem_base, abort);
+            w_role_mma<F, S>(p, sL, sS, bars, tmem_base, abort);
             const bool aborted = __any_sync(0xffffffffu, *abort != 0);
             if (elect_one() && aborted) {
                 // let every MMA already issued (by this same elected lane)
@@ -518,10 +632,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             __syncwarp();
         } else if (lane == 0) {
-            w_role_relay(p, bars, abort);
+            w_role_relay<S>(p, bars, abort);
         }
     } else {
-        w_role_epilogue<F, kMG>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
+        w_role_epilogue<F, kMG, S>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
     }
     if (warp == kWarpTma && lane == 0 && *abort) {
         const uint64_t t0 = global_timer_ns();
@@ -542,8 +656,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // (persistent, static unit stride).  a.m_tiles = stationary tiles per expert
 // (ceil(H / 256)), a.n_tiles = streamed tiles (ceil(2I / 256) for dW1,
 // ceil(I / 256) for dW2).
-template <int F, bool kMG = false>
-int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensorMap& mapC, cudaStream_t st) {
+template <int F, bool kMG, int S>
+int launch_wgrad_pair_s(const GemmArgs& a, const CUtensorMap& mapS, const CUtensorMap& mapC, cudaStream_t st) {
     // filled on the first call per device; host threads may race to fill it
     // with the same value
     static std::atomic<int> clusters_fit[kMaxDevices] = {};
@@ -567,7 +681,7 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
     int fit = clusters_fit[dev].load(std::memory_order_relaxed);
     if (fit == 0) {
         // set once per device, outside any stream capture (on the first call)
-        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F, kMG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(moe_wgrad_pair_kernel<F, kMG, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kWSmemBytes + 8 * kMaxExperts);
         if (e != cudaSuccess) return (int)e;
         int sms = 0;
@@ -575,7 +689,7 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
         if (e != cudaSuccess) return (int)e;
         cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, moe_wgrad_pair_kernel<F, kMG>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, moe_wgrad_pair_kernel<F, kMG, S>, &cfg);
         if (e != cudaSuccess) return (int)e;
         if (n < 1) return (int)cudaErrorInvalidConfiguration;
         fit = n;
@@ -585,9 +699,18 @@ int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensor
     if (units <= 0) return 0;
     const int clusters = units < fit ? (int)units : fit;
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
-    e = cudaLaunchKernelEx(&cfg, moe_wgrad_pair_kernel<F, kMG>, mapS, mapC, a);
+    e = cudaLaunchKernelEx(&cfg, moe_wgrad_pair_kernel<F, kMG, S>, mapS, mapC, a);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
+}
+
+// The slab / ring split from the shape (no routing statistic is read on the
+// host): the large slab when the mean rows per expert exceed the small one.
+template <int F, bool kMG = false>
+int launch_wgrad_pair(const GemmArgs& a, const CUtensorMap& mapS, const CUtensorMap& mapC, cudaStream_t st) {
+    const long long mean_rows = a.E > 0 ? (long long)a.T * a.k / a.E : 0;
+    if (mean_rows > (long long)kWSlabSmall * kBK) return launch_wgrad_pair_s<F, kMG, kWSlabLarge>(a, mapS, mapC, st);
+    return launch_wgrad_pair_s<F, kMG, kWSlabSmall>(a, mapS, mapC, st);
 }
 
 }  // namespace moe

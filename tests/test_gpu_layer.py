@@ -99,14 +99,23 @@ def test_one_hot_expert_long_k():
     _full_check(shape, _inputs(shape, 7, mutate))
 
 
+# Expert sizes around the weight-gradient slab.  Mean rows per expert 280:
+# the 5-block slab (320 rows): 320 fits, 321 needs a second K chunk of one
+# row, 700 needs three chunks (its tiles then go in pairs).  Mean 392: the
+# 7-block slab (448 rows): 448 fits, 449 needs two chunks, 1000 three.
+SLAB_CASES = {"slab5": [320, 321, 700, 0, 59], "slab7": [448, 449, 1000, 0, 59, 400]}
+
+
 @pytest.mark.parametrize("main_grad", [False, True])
-def test_experts_around_the_weight_gradient_slab(main_grad):
-    """Experts with 320 routed rows (the most the weight-gradient slab holds),
-    321 (one row past it: a second K chunk of one row) and 700, and one empty
-    expert, with H = 320 (the last 256-feature tile half past H) and I = 192,
-    the workspaces starting as NaN bytes; also through the FP32 main-gradient
+@pytest.mark.parametrize("case", sorted(SLAB_CASES))
+def test_experts_around_the_weight_gradient_slab(case, main_grad):
+    """Experts at, one row past, and several chunks past the weight-gradient
+    slab's capacity (both slab sizes, chosen by the shape), and one empty
+    expert, with H = 320 (the last 256-feature tile half past H) and I = 192
+    (two streamed dW1 tiles: one pair; one dW2 tile: a pair's lone tile), the
+    workspaces starting as NaN bytes; also through the FP32 main-gradient
     entry point."""
-    sizes = [320, 321, 700, 0, 59]
+    sizes = SLAB_CASES[case]
     T, H, I, E, k = sum(sizes), 320, 192, len(sizes), 1
     shape = LayerShape("slab_edges", T=T, H=H, I=I, E=E, k=k)
 
