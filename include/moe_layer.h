@@ -182,20 +182,35 @@ int moe_backward(const moe_shape* shape, const void* dY, const void* x, const vo
  * Errors as for moe_route_prologue. */
 int moe_quantize_fp8(const moe_shape* shape, const void* x, uint8_t* x_fp8, uint8_t* x_sf, void* stream);
 
-/* moe_forward with the input given as moe_quantize_fp8's x_fp8 / x_sf: the
- * L1 GEMM gathers the E4M3 rows and their scales and widens them to bf16 in
- * shared memory (exactly: an E4M3 value times a power of two is a bf16
- * value), so the result equals moe_forward on the dequantized input
- * decode(x_fp8) * 2^(x_sf - 127); gathered bytes are halved.  Everything
- * else (saved, y, route_ws, errors) as for moe_forward; moe_backward may
- * follow with x = the dequantized input. */
-int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const void* W1,
-                    const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream);
+/* FP8 weights for moe_forward_fp8 (DeepGEMM Mega-MoE article, usage example:
+ * the weights are transformed once for the FP8 kernel): W1 bf16[E,H,2I] ->
+ * W1_fp8 = E4M3 bytes, K-major [E][2I][H] (column f of W1 as a row: gate
+ * columns 0..I-1, then up), and W1_sf = UE8M0 scales, one per 32 consecutive
+ * h of a column (the same rule as moe_quantize_fp8, along H), E * 2I * H/32
+ * bytes in the layout the L1 kernel loads: for column f, group g = (f mod I)
+ * / 64 and row r = 64 [f >= I] + (f mod I) mod 64; for the 32-group j32 of
+ * h, block kb = j32 / 4 and step j = j32 mod 4; byte
+ *   ((e (I/64) + g) (H/128) + kb) 512 + 16 (r mod 32) + 4 floor(r / 32) + j.
+ * Needs H a multiple of 128 (MOE_EUNSUPPORTED otherwise).  Kernels on
+ * `stream`; other errors as for moe_route_prologue. */
+int moe_quantize_weights_fp8(const moe_shape* shape, const void* W1, uint8_t* W1_fp8, uint8_t* W1_sf, void* stream);
+
+/* FP8 forward: moe_forward with the input given as moe_quantize_fp8's
+ * x_fp8 / x_sf and W1 as moe_quantize_weights_fp8's W1_fp8 / W1_sf; W2 stays
+ * bf16.  The L1 GEMM multiplies the E4M3 operands on the tensor cores with
+ * their UE8M0 scales applied per 32 elements of K (block-scaled MMA), FP32
+ * accumulation, so the result is moe_forward on the dequantized input and
+ * the dequantized W1 (up to the order of the FP32 sums); it reads half the
+ * bytes of W1 and of the gathered rows.  Needs H a multiple of 128.
+ * Everything else (saved, y, route_ws, errors) as for moe_forward.  An
+ * inference path: the pages' FP8 operator is a forward; training steps use
+ * moe_forward / moe_backward. */
+int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const uint8_t* W1_fp8,
+                    const uint8_t* W1_sf, const void* W2, const float* topk_w, void* route_ws, void* saved, void* y,
+                    void* stream);
 
 /* The inverse of moe_quantize_fp8: x_out bf16[T,H] = decode(x_fp8) *
- * 2^(x_sf - 127), exactly (every such value is a bf16 value).  The backward
- * of an FP8-dispatched forward is moe_backward with x = this dequantized
- * input (the input the forward actually multiplied).  Errors as for
+ * 2^(x_sf - 127), exactly (every such value is a bf16 value).  Errors as for
  * moe_quantize_fp8. */
 int moe_dequantize_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, void* x_out, void* stream);
 

@@ -135,6 +135,19 @@ def quantize_fp8(x_bits: np.ndarray, gran: int = 32):
     return q[:T], sf[:T]
 
 
+def quantize_weights_fp8(W1_bits: np.ndarray, gran: int = 32):
+    """FP8 weights for the L1 GEMM (DeepGEMM Mega-MoE article, usage example:
+    the weights are transformed once for the low-precision kernel).  W1_bits:
+    bf16 bit patterns [E, H, 2I].  Each column W1[e, :, f] is quantized like
+    a token of quantize_fp8 (groups of `gran` consecutive h, the contraction
+    index of the L1 GEMM).  Returns q uint8 [E, 2I, H] and sf uint8
+    [E, 2I, H // gran]."""
+    wb = np.ascontiguousarray(W1_bits, dtype=np.uint16)
+    E, H, I2 = wb.shape
+    q, sf = quantize_fp8(np.ascontiguousarray(wb.transpose(0, 2, 1)).reshape(E * I2, H), gran)
+    return q.reshape(E, I2, H), sf.reshape(E, I2, H // gran)
+
+
 def dequantize_fp8(q: np.ndarray, sf: np.ndarray, gran: int = 32) -> np.ndarray:
     """decode(q) * 2^(sf - 127), float64 [T, H]."""
     table = np.array([e4m3_decode(c) for c in range(256)], np.float64)

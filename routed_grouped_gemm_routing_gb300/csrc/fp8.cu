@@ -1,8 +1,9 @@
-// FP8 dispatch of the layer input (DeepGEMM Mega-MoE article, usage example:
+// FP8 forward of the layer (DeepGEMM Mega-MoE article, usage example:
 // activations cast per token to FP8 with UE8M0 scale factors at a
-// granularity of 32 elements before they are dispatched): the quantization
-// kernel, and the instantiation of the L1 GEMM whose gather reads the E4M3
-// rows.
+// granularity of 32 elements before they are dispatched, and the weights
+// transformed once for its low-precision kernel): the quantization kernels
+// of the input and of W1, and the instantiation of the L1 GEMM on E4M3
+// operands.
 #include "grouped_gemm_2sm.cuh"
 
 namespace moe {
@@ -80,7 +81,77 @@ __global__ void __launch_bounds__(256) dequantize_fp8_kernel(const uint8_t* __re
     }
 }
 
+// W1 [E][H][2I] bf16 to E4M3, one scale per 32 consecutive h of a column
+// (the K of the L1 GEMM), written K-major as q[E][2I][H] (gate columns, then
+// up) with the scale bytes in the L1 GEMM's atom layout: for column f (gate
+// f < I, up I + f'), group g = (f mod I) / 64 and atom row r = 64 (f >= I) +
+// (f mod I) % 64; for K group j32 = h / 32, block kb = j32 / 4 and step j =
+// j32 % 4; byte ((e (I/64) + g) (H/128) + kb) 512 + 16 (r % 32) + 4 (r / 32)
+// + j.  One block of 128 threads per 32 rows of h x 128 columns: the tile
+// comes in coalesced through shared memory and each thread quantizes one
+// column's group.  The same rule as the input (smallest power of two with
+// 448 2^e >= max|group|, round to nearest even, saturate).
+__global__ void __launch_bounds__(128) quantize_w1_fp8_kernel(const __nv_bfloat16* __restrict__ W1, int E, int H,
+                                                              int I, uint8_t* __restrict__ q,
+                                                              uint8_t* __restrict__ atoms) {
+    __shared__ __align__(16) __nv_bfloat16 tile[32][128];
+    const int ncol = 2 * I / 128, nrow = H / 32, nkb = H / 128;
+    const long long ntiles = (long long)E * nrow * ncol;
+    const int tid = threadIdx.x;
+    for (long long ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
+        const int cb = (int)(ti % ncol);
+        const int hb = (int)((ti / ncol) % nrow);
+        const int e = (int)(ti / ((long long)ncol * nrow));
+        const int f0 = cb * 128, h0 = hb * 32;
+        __syncthreads();  // the previous tile has been read
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int ch = tid + 128 * i;  // 16-byte chunk: row ch / 16, columns 8 (ch % 16)
+            const int hr = ch >> 4, cc = (ch & 15) * 8;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + ((size_t)e * H + h0 + hr) * (size_t)(2 * I) + f0 + cc));
+            *reinterpret_cast<uint4*>(&tile[hr][cc]) = v;
+        }
+        __syncthreads();
+        float v[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            v[j] = __bfloat162float(tile[j][tid]);
+            amax = fmaxf(amax, fabsf(v[j]));
+        }
+        const int ex = fp8_group_exponent(amax);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const float2 f = make_float2(ldexpf(v[4 * j + 2 * m], -ex), ldexpf(v[4 * j + 2 * m + 1], -ex));
+                acc |= (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3) << (16 * m);
+            }
+            w[j] = acc;
+        }
+        const int f = f0 + tid;
+        uint8_t* dst = q + ((size_t)e * (size_t)(2 * I) + f) * (size_t)H + h0;
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        const int fi = f < I ? f : f - I;
+        const int g = fi >> 6, r = (f < I ? 0 : 64) + (fi & 63);
+        const int kb = hb >> 2, js = hb & 3;
+        atoms[(((size_t)e * (I / 64) + g) * nkb + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5) + js] = (uint8_t)(ex + 127);
+    }
+}
+
 }  // namespace
+
+int launch_quantize_w1_fp8(const __nv_bfloat16* W1, int E, int H, int I, uint8_t* q, uint8_t* atoms, int num_sms,
+                           cudaStream_t st) {
+    const long long ntiles = (long long)E * (H / 32) * (2 * I / 128);
+    if (ntiles <= 0) return 0;
+    const long long cap = (long long)num_sms * 16;
+    quantize_w1_fp8_kernel<<<(unsigned)(ntiles < cap ? ntiles : cap), 128, 0, st>>>(W1, E, H, I, q, atoms);
+    return (int)cudaGetLastError();
+}
 
 int launch_dequantize_fp8(const uint8_t* q, const uint8_t* sf, long long n, __nv_bfloat16* out, int num_sms,
                           cudaStream_t st) {
@@ -102,9 +173,9 @@ int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t
     return (int)cudaGetLastError();
 }
 
-// L1 GEMM + SwiGLU with the gathered rows read as E4M3 + UE8M0 scales
-int launch_gemm_l1_fwd_fp8(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
-    return launch_gemm_pair<L1_FWD_FP8>(a, m, max_units, st);
+// L1 GEMM + SwiGLU on E4M3 weights and gathered E4M3 rows (block-scaled MMA)
+int launch_gemm_l1_fwd_mx(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
+    return launch_gemm_pair<L1_FWD_MX>(a, m, max_units, st);
 }
 
 }  // namespace moe

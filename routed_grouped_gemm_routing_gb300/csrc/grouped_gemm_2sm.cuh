@@ -206,6 +206,49 @@ __device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// ---------------------------------------------- block-scaled FP8 (MX) MMA
+// D[tmem] (+)= sum over one 32-deep K step of (A 2^sa) (B 2^sb): E4M3 A and
+// B, one UE8M0 scale per operand row and K step, FP32 accumulation
+// (kind::mxf8f6f4, block_scale, one scale per 32 elements).  The scales are
+// read from TMEM at sfa / sfb; the instruction descriptor picks the byte of
+// each lane's word (the K step).
+__device__ __forceinline__ void tc_mma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+// Copies 32 rows x 16 bytes of shared memory (described by sdesc) into TMEM
+// columns [taddr, taddr + 4) of each of the four 32-lane quadrants (row i to
+// lane 32 q + i), in both CTAs of the pair from their own shared memory.
+// Ordered before the MMAs the same thread issues after it.
+__device__ __forceinline__ void tc_cp_rows16_x4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Shared-memory descriptor of 32 rows x 16 bytes, no swizzle (8-row core
+// matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t make_sdesc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;             // leading byte offset 16 (one column of 16 bytes)
+    d |= static_cast<uint64_t>(128 >> 4) << 32;      // stride byte offset 128
+    d |= static_cast<uint64_t>(1) << 46;             // version 1, no swizzle
+    return d;
+}
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B (K-major), UE8M0
+// scales, scale byte `sf` (the K step) of both A's and B's scale words.
+__host__ __device__ constexpr uint32_t make_idesc_mx_e4m3(int M, int N, int sf) {
+    return ((uint32_t)sf << 4)                       // B scale byte
+           | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+           | (1u << 23)                              // scale type: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24)   // M / 16
+           | ((uint32_t)sf << 29);                   // A scale byte
+}
+
 // Column l of a 32-row x 32-column bf16 box in the 64-byte swizzle (row j
 // at byte 64 j, its 16-byte chunk q stored at chunk q ^ ((j / 2) % 4)):
 // v[j] is the value of row j.
@@ -261,19 +304,51 @@ struct T2<L1_FWD> {
     static constexpr int kEpiHalves = 1;  // epilogue warps per TMEM lane quadrant
     static constexpr int kInBytes = 0;
 };
-// FP8 dispatch: the same GEMM, its gathered rows read as E4M3 bytes with
-// one UE8M0 scale per 32 elements and widened to bf16 on the way into
-// shared memory (exact: an E4M3 value times a power of two fits bf16).
+// FP8 forward: the same GEMM on E4M3 weights (pre-quantized, K-major,
+// [E][2][I][H]) and gathered E4M3 rows, each with one UE8M0 scale per 32
+// elements of K, by the block-scaled tcgen05.mma (kind::mxf8f6f4).  A stage
+// is 128 deep in K (128 bytes per row, like a 64-deep bf16 stage).  Its
+// scales sit in 512-byte atoms of 128 operand rows x 4 K steps (row r, step
+// j at byte 16 (r % 32) + 4 (r / 32) + j, the order in which TMEM holds
+// them: lane r % 32 of every 32-lane quadrant, column r / 32, byte j): one
+// atom for this CTA's weights (by TMA, stored in that layout) and two for
+// the unit's up to 256 rows (gathered; both CTAs hold all of them), copied
+// into TMEM by the MMA thread before the stage's four MMAs.
 template <>
-struct T2<L1_FWD_FP8> : T2<L1_FWD> {
-    static constexpr int kStages = 4;
-    static constexpr int kFp8Slots = 4;  // staging ring of raw E4M3 blocks
-    static constexpr int kInBytes = kFp8Slots * (128 * 64 + 128 * 4);
+struct T2<L1_FWD_MX> : T2<L1_FWD> {
+    static constexpr bool kAMN = false;
+    static constexpr int kStages = 5;
+    static constexpr int kSfBytes = 512 + 1024;  // per stage: the weights' atom, the rows' two atoms
+    static constexpr int kInBytes = kStages * kSfBytes;
 };
 template <int F>
 __host__ __device__ constexpr bool t2_is_l1() {
-    return F == L1_FWD || F == L1_FWD_FP8;
+    return F == L1_FWD || F == L1_FWD_MX;
 }
+// K per stage: 64 bf16 or 128 E4M3 elements (128 bytes per operand row)
+template <int F>
+__host__ __device__ constexpr int t2_kblock() {
+    return F == L1_FWD_MX ? 128 : kBK;
+}
+// TMEM of the FP8 flavour: accumulator 0 at column 0 (up to 256 columns),
+// accumulator 1 at column 256 (up to 224: a unit of more rows always takes
+// accumulator 0), and two slots of scale factors, the rows' two atoms at
+// columns 480 + 8 s, the weights' atom at 496 + 4 s.
+constexpr uint32_t kMxAcc1MaxN = 224, kMxSfb = 480, kMxSfa = 496;
+// Accumulator of each unit in turn (the MMA warp and the epilogue warps walk
+// the same units): the other one than the previous unit's when the unit
+// fits accumulator 1, so that the epilogue of one overlaps the next one's
+// MMAs; the phase of an accumulator counts its own uses.
+struct MxAcc {
+    int prev = 1;
+    uint32_t uses[2] = {0u, 0u};
+    __device__ __forceinline__ int pick(int n, uint32_t* phase) {
+        const int a = n > (int)kMxAcc1MaxN ? 0 : prev ^ 1;
+        prev = a;
+        *phase = uses[a]++ & 1u;
+        return a;
+    }
+};
 
 template <>
 struct T2<L2_FWD> {
@@ -311,7 +386,7 @@ constexpr int t2_smem_bytes() {
            kT2TailBytes;
 }
 static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448 &&
-                  t2_smem_bytes<L1_FWD_FP8>() <= 232448,
+                  t2_smem_bytes<L1_FWD_MX>() <= 232448,
               "shared memory per CTA");
 static_assert(T2<L2_FWD>::kProducers - 1 + kEpiWarps * (T2<L2_FWD>::kEpiHalves - 1) <= kGatherWarps &&
                   T2<L1_DGRAD>::kEpiHalves == 1 && T2<L1_FWD>::kEpiHalves == 1 && T2<L2_DGRAD>::kEpiHalves == 1,
@@ -325,7 +400,7 @@ constexpr bool t2_producers_ok() {
     return T2<F>::kProducers <= T2<F>::kStages;
 }
 static_assert(t2_producers_ok<L1_FWD>() && t2_producers_ok<L2_FWD>() && t2_producers_ok<L2_DGRAD>() &&
-                  t2_producers_ok<L1_DGRAD>() && t2_producers_ok<L1_FWD_FP8>(),
+                  t2_producers_ok<L1_DGRAD>() && t2_producers_ok<L1_FWD_MX>(),
               "round-robin producers within the ring depth");
 static_assert(T2<L1_FWD>::kProducers == 1 && T2<L2_DGRAD>::kProducers == 1 && T2<L2_FWD>::kProducers <= 1 + kGatherWarps &&
                   T2<L1_DGRAD>::kProducers <= 1 + kGatherWarps,
@@ -531,9 +606,10 @@ __device__ void t2_role_sched(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
 // threads proceed side by side.
 template <int F>
 __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, uint32_t ring,
-                            uint32_t sA, uint32_t sB, T2Bars bars, volatile int* abort, int rank, int pid) {
+                            uint32_t sA, uint32_t sB, uint32_t sIn, T2Bars bars, volatile int* abort, int rank,
+                            int pid) {
     constexpr int NP = T2<F>::kProducers;
-    const int nkb = p.K / kBK;
+    const int nkb = p.K / t2_kblock<F>();
     int stage = 0;
     uint32_t phase = 0;
     uint32_t g = 0;
@@ -542,7 +618,8 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
         const int nh = t.n >> 1;           // this CTA's rows of the unit
         const int nbox = (nh + 31) >> 5;   // 32-row boxes of a non-gathered B
         const int rb = t.r0 + nh * rank;
-        const uint32_t tx = (uint32_t)kT2ABytes + (T2<F>::kGather ? 0u : (uint32_t)nbox * 4096u);
+        const uint32_t tx = (uint32_t)kT2ABytes + (T2<F>::kGather ? 0u : (uint32_t)nbox * 4096u) +
+                            (F == L1_FWD_MX ? 512u : 0u);
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             if (NP > 1 && (int)(g % (uint32_t)NP) != pid) {
                 if (++stage == T2<F>::kStages) {
@@ -554,12 +631,21 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
             if (!mbar_wait(bars.empty(stage), phase ^ 1u, abort)) return;
             const uint32_t a = sA + stage * kT2ABytes;
             const uint32_t b = sB + stage * kT2BBytes;
-            const int k0 = kb * kBK;
+            const int k0 = kb * t2_kblock<F>();
             // both CTAs' TMA loads complete the even CTA's full barrier, armed
             // there with both halves' bytes
             if (rank == 0) mbar_arrive_expect_tx(bars.full(stage), 2u * tx);
             const uint32_t fb = cluster_addr_of(bars.full(stage), 0);
-            if constexpr (t2_is_l1<F>()) {
+            if constexpr (F == L1_FWD_MX) {
+                // E4M3 W1 viewed as [E][2][I][H] (K-major): the 64 gate rows,
+                // then the same 64 up rows, 128 bytes of K each; then their
+                // scale atom, atoms stored [E][I / 64][H / 128] (512 bytes,
+                // two 256-byte rows of the atoms' tensor map)
+                tma_load_4d_pair(a, mA, k0, t.f0, 0, t.e, fb);
+                tma_load_4d_pair(a + 8192, mA, k0, t.f0, 1, t.e, fb);
+                const int atom = (t.e * (p.I / 64) + t.fcol) * nkb + kb;
+                tma_load_2d_pair(sIn + (uint32_t)stage * (uint32_t)T2<L1_FWD_MX>::kSfBytes, mB, 0, 2 * atom, fb);
+            } else if constexpr (t2_is_l1<F>()) {
                 // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
                 tma_load_4d_pair(a, mA, t.f0, 0, k0, t.e, fb);
                 tma_load_4d_pair(a + 8192, mA, t.f0, 1, k0, t.e, fb);
@@ -593,7 +679,7 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, ui
     const int rb = lane >> 3;
     const int H = p.H;
     const int k = p.k;
-    const int nkb = p.K / kBK;
+    const int nkb = p.K / t2_kblock<F>();
     const __nv_bfloat16* src = p.gsrc;
     int stage = 0;
     uint32_t phase = 0;
@@ -609,89 +695,42 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, ui
             if (r < nh) s = __ldg(p.perm + rbase + r);
             tok[q] = r < nh ? (s >= 0 ? s / k : -1) : -2;  // -2: row not in this unit
         }
-        if constexpr (F == L1_FWD_FP8) {
-            // Raw E4M3 blocks (64 bytes per row) and the row's aligned scale
-            // word come into a staging ring by cp.async, kFp8Slots - 1 blocks
-            // ahead; each thread widens the chunks it copied itself (its own
-            // cp.async.wait_group makes them visible) and the quad of a row
-            // shares the scale word after a warp barrier.  Thread (row pair,
-            // c4): rows gw*16 + (lane >> 2) + 8 q, 16-element chunk c4.
-            constexpr int S = T2<F>::kFp8Slots;
-            constexpr uint32_t kSlot = 128 * 64 + 128 * 4;
-            const int c4 = lane & 3;
-            const int G = H >> 5;
-            int tq[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int r = gw * 16 + (lane >> 2) + 8 * q;
-                int sl = -1;
-                if (r < nh) sl = __ldg(p.perm + rbase + r);
-                tq[q] = r < nh ? (sl >= 0 ? sl / k : -1) : -2;
+        if constexpr (F == L1_FWD_MX) {
+            // This CTA's rows as E4M3 bytes (128 per row and K block, the same
+            // 16-byte chunks as a bf16 block), and the 4 scale bytes of the
+            // block of one unit row per thread (every row of the unit: both
+            // CTAs' MMA columns) into the rows' atoms: unit row u at byte
+            // 512 (u / 128) + 16 (u % 32) + 4 ((u % 128) / 32) of them.
+            const int G = H >> 5;  // scale bytes per row of x_sf
+            const int us = gw * 32 + lane;
+            int stok = -2;  // -2: past the unit's N, not read by the MMA
+            if (us < t.n) {
+                const int sl = __ldg(p.perm + t.r0 + us);
+                stok = sl >= 0 ? sl / k : -1;
             }
-            auto issue = [&](int kb) {
-                const uint32_t slot = stg + (uint32_t)(kb % S) * kSlot;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int tk = tq[q];
-                    if (tk == -2) continue;
-                    const int r = gw * 16 + (lane >> 2) + 8 * q;
-                    const size_t t0 = (size_t)(tk < 0 ? 0 : tk);
-                    cp_async_16(slot + r * 64 + c4 * 16, p.gsrc8 + t0 * (size_t)H + kb * kBK + c4 * 16,
-                                tk < 0 ? 0u : 16u);
-                    if (c4 == 0) {
-                        // the aligned 4-byte word holding the row's two scales of
-                        // this block (at byte a & 3 = 0 or 2 of it); when they are
-                        // its low half only those 2 bytes are read, so the copy
-                        // never runs past the end of x_sf
-                        const size_t a = t0 * (size_t)G + (size_t)kb * 2;
-                        cp_async_4(slot + 128 * 64 + r * 4, p.gsf + (a & ~(size_t)3),
-                                   tk < 0 ? 0u : ((a & 3) ? 4u : 2u));
-                    }
-                }
-            };
-#pragma unroll 1
-            for (int j = 0; j < S - 1; ++j) {
-                if (j < nkb) issue(j);
-                cp_async_commit();
-            }
+            const uint32_t soff =
+                512u + (uint32_t)(us >> 7) * 512u + (uint32_t)(us & 31) * 16u + (uint32_t)((us >> 5) & 3) * 4u;
             for (int kb = 0; kb < nkb; ++kb) {
-                if (kb + S - 1 < nkb) issue(kb + S - 1);
-                cp_async_commit();
-                cp_async_wait_group<S - 1>();
-                __syncwarp();
                 if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
                 const uint32_t b = sB + stage * kT2BBytes;
-                const uint32_t slot = stg + (uint32_t)(kb % S) * kSlot;
+                const int colb = kb * 128 + c * 16;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int tk = tq[q];
+                for (int q = 0; q < 4; ++q) {
+                    const int tk = tok[q];
                     if (tk == -2) continue;
-                    const int r = gw * 16 + (lane >> 2) + 8 * q;
-                    const int4 raw = ld_shared_v4s(slot + r * 64 + c4 * 16);
-                    uint32_t word;
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(word) : "r"(slot + 128 * 64 + r * 4) : "memory");
-                    // this chunk's group is kb * 2 + c4 / 2: its byte inside the aligned word
-                    const size_t a = (size_t)(tk < 0 ? 0 : tk) * (size_t)G + (size_t)kb * 2 + (size_t)(c4 >> 1);
-                    const float sc = fp8_scale((word >> (8 * (uint32_t)(a & 3))) & 0xffu);
-                    const uint32_t w0 = (uint32_t)raw.x, w1 = (uint32_t)raw.y, w2 = (uint32_t)raw.z, w3 = (uint32_t)raw.w;
-                    const uint32_t row = b + r * 128;
-                    const uint32_t sw = (uint32_t)(r & 7);
-                    st_shared_v4(row + (((uint32_t)(2 * c4) ^ sw) << 4), e4m3x2_to_bf16x2(w0 & 0xffffu, sc),
-                                 e4m3x2_to_bf16x2(w0 >> 16, sc), e4m3x2_to_bf16x2(w1 & 0xffffu, sc),
-                                 e4m3x2_to_bf16x2(w1 >> 16, sc));
-                    st_shared_v4(row + (((uint32_t)(2 * c4 + 1) ^ sw) << 4), e4m3x2_to_bf16x2(w2 & 0xffffu, sc),
-                                 e4m3x2_to_bf16x2(w2 >> 16, sc), e4m3x2_to_bf16x2(w3 & 0xffffu, sc),
-                                 e4m3x2_to_bf16x2(w3 >> 16, sc));
+                    const int r = gw * 16 + rb + 4 * q;
+                    const uint8_t* g = p.gsrc8 + (size_t)(tk < 0 ? 0 : tk) * (size_t)H + colb;
+                    cp_async_16(b + r * 128 + ((c ^ (r & 7)) << 4), g, tk < 0 ? 0u : 16u);
                 }
-                fence_proxy_async_smem();  // generic-proxy stores, read by the tensor core
-                mbar_arrive(bars.full(stage));
-                __syncwarp();  // the slot's scale words are read before it is refilled
+                if (stok != -2)
+                    cp_async_4(stg + (uint32_t)stage * (uint32_t)T2<L1_FWD_MX>::kSfBytes + soff,
+                               p.gsf + (size_t)(stok < 0 ? 0 : stok) * (size_t)G + (size_t)kb * 4, stok < 0 ? 0u : 4u);
+                cp_async_arrive_noinc(bars.full(stage));
                 if (++stage == T2<F>::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
-            cp_async_wait_group<0>();
         } else {
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
@@ -721,7 +760,7 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, ui
 template <int F>
 __device__ void t2_role_mma(const GemmArgs& p, uint32_t ring, uint32_t sA, uint32_t sB, T2Bars bars,
                             uint32_t tmem_base, volatile int* abort, int lane) {
-    const int nkb = p.K / kBK;
+    const int nkb = p.K / t2_kblock<F>();
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
@@ -760,11 +799,64 @@ __device__ void t2_role_mma(const GemmArgs& p, uint32_t ring, uint32_t sA, uint3
     }
 }
 
+// The MMA warp of the FP8 flavour: per stage, the elected lane copies the
+// stage's three scale atoms into the next of the two TMEM scale slots and
+// issues the four block-scaled MMAs of the 128-deep block (one per 32-deep
+// K step, each reading byte kk of the scale words); a copy and the MMAs
+// after it run in issue order, and the slot a copy overwrites was last read
+// by MMAs issued before it.
+template <int F>
+__device__ void t2_role_mma_mx(const GemmArgs& p, uint32_t ring, uint32_t sA, uint32_t sB, uint32_t sIn, T2Bars bars,
+                               uint32_t tmem_base, volatile int* abort, int lane) {
+    const int nkb = p.K / t2_kblock<F>();
+    int stage = 0;
+    uint32_t phase = 0, nblk = 0;
+    MxAcc accs;
+    T2Feed<F> feed(ring, bars, 0);
+    for (T2Unit t; feed.template next<true>(t, abort, lane);) {
+        uint32_t acc_phase;
+        const int acc = accs.pick(t.n, &acc_phase);
+        if (!warp_wait_uniform<true>(bars.tempty(acc), acc_phase ^ 1u, abort)) return;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < nkb; ++kb, ++nblk) {
+            if (!warp_wait_uniform<true>(bars.full(stage), phase, abort)) return;
+            tc_fence_after();
+            const uint32_t a = sA + stage * kT2ABytes;
+            const uint32_t b = sB + stage * kT2BBytes;
+            const uint32_t sf = sIn + (uint32_t)stage * (uint32_t)T2<L1_FWD_MX>::kSfBytes;
+            const uint32_t tsfa = tmem_base + kMxSfa + 4u * (nblk & 1u);
+            const uint32_t tsfb = tmem_base + kMxSfb + 8u * (nblk & 1u);
+            if (elect_one()) {
+                fence_proxy_async_smem();  // rows and row scales written by cp.async
+                tc_cp_rows16_x4_pair(tsfa, make_sdesc_rows16(sf));
+                tc_cp_rows16_x4_pair(tsfb, make_sdesc_rows16(sf + 512));
+                tc_cp_rows16_x4_pair(tsfb + 4, make_sdesc_rows16(sf + 1024));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = make_sdesc_sw128(a + kk * 32, 16, 1024);
+                    const uint64_t bd = make_sdesc_sw128(b + kk * 32, 16, 1024);
+                    tc_mma_mx_pair(d, ad, bd, make_idesc_mx_e4m3(2 * kBM, t.n, kk), tsfa, tsfb,
+                                   (kb | kk) != 0 ? 1u : 0u);
+                }
+                tc_commit_pair(bars.empty(stage));
+            }
+            __syncwarp();
+            if (++stage == T2<F>::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (elect_one()) tc_commit_pair(bars.tfull(acc));
+        __syncwarp();
+    }
+}
+
 // The odd CTA's MMA thread: tells the even CTA that this CTA's half of a
 // stage is in shared memory.
 template <int F>
 __device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, volatile int* abort) {
-    const int nkb = p.K / kBK;
+    const int nkb = p.K / t2_kblock<F>();
     int stage = 0;
     uint32_t phase = 0;
     T2Feed<F> feed(ring, bars, 1);
@@ -803,10 +895,12 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
     uint32_t nstore = 0;
     uint32_t xchunk = 0;  // L1: chunks handed over between warp i and warp 2 + i
     uint32_t nin = 0;     // L2 dgrad: input boxes waited for
+    MxAcc accs;
     T2Feed<F> feed(ring, bars, rank);
     for (T2Unit t; feed.template next<true>(t, abort, lane); ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        int acc = it & 1;
+        uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if constexpr (F == L1_FWD_MX) acc = accs.pick(t.n, &acc_phase);
         if constexpr (F == L2_DGRAD) {
             if (lane == 0 && t.f0 + 32 * warp < p.I) {
                 // the unit's first chunk, into buffer nin & 1, whose last
@@ -1064,7 +1158,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     }
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_map(&mapA);
-        if constexpr (!T2<F>::kGather || F == L2_DGRAD) tma_prefetch_map(&mapB);
+        if constexpr (!T2<F>::kGather || F == L2_DGRAD || F == L1_FWD_MX) tma_prefetch_map(&mapB);
         if constexpr (F == L2_DGRAD) tma_prefetch_map(&mapD);
         tma_prefetch_map(&mapC0);
         if constexpr (t2_is_l1<F>() || F == L2_DGRAD) tma_prefetch_map(&mapC1);
@@ -1081,7 +1175,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         if (warp >= kWarpGather0 && warp < kWarpGather0 + T2<F>::kProducers - 1) pid = 1 + warp - kWarpGather0;
     }
     if (pid >= 0) {
-        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, bars, abort, rank, pid);
+        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, sIn, bars, abort, rank, pid);
     } else if (warp == kWarpSched) {
         if (lane == 0 && rank == 0) t2_role_sched<F>(p, ring, bars, abort);
     } else if (T2<F>::kEpiHalves > 1 && warp >= kWarpGather0 + T2<F>::kProducers - 1 &&
@@ -1096,7 +1190,10 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
         if (rank == 0) {
-            t2_role_mma<F>(p, ring, sA, sB, bars, tmem_base, abort, lane);
+            if constexpr (F == L1_FWD_MX)
+                t2_role_mma_mx<F>(p, ring, sA, sB, sIn, bars, tmem_base, abort, lane);
+            else
+                t2_role_mma<F>(p, ring, sA, sB, bars, tmem_base, abort, lane);
             const bool aborted = __any_sync(0xffffffffu, *abort != 0);
             if (elect_one() && aborted) {
                 // let every MMA already issued (by this same elected lane)

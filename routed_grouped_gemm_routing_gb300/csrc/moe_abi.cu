@@ -21,7 +21,7 @@ int launch_gemm_dw1(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw2(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw1_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw2_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
-int launch_gemm_l1_fwd_fp8(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_l1_fwd_mx(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 
 int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     switch (f) {
@@ -33,7 +33,7 @@ int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaS
         case DW2: return launch_gemm_dw2(a, m, grid, st);
         case DW1_MG: return launch_gemm_dw1_mg(a, m, grid, st);
         case DW2_MG: return launch_gemm_dw2_mg(a, m, grid, st);
-        case L1_FWD_FP8: return launch_gemm_l1_fwd_fp8(a, m, grid, st);
+        case L1_FWD_MX: return launch_gemm_l1_fwd_mx(a, m, grid, st);
         default: return (int)cudaErrorInvalidValue;
     }
 }
@@ -212,6 +212,26 @@ int map_w1_halves(CUtensorMap* m, const void* p, int E, int H, int I) {
     return make_map(m, p, 4, dims, str, box, "W1 (gate/up halves)");
 }
 
+// E4M3 W1, K-major [E][2][I][H] bytes: a box is 128 bytes of K of 64 rows
+// (columns) of one half, 128-byte swizzle.
+int map_w1_fp8(CUtensorMap* m, const void* p, int E, int H, int I) {
+    cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
+    cuuint64_t str[3] = {(cuuint64_t)H, (cuuint64_t)H * I, (cuuint64_t)H * I * 2};
+    cuuint32_t box[4] = {128, 64, 1, 1};
+    return make_map(m, p, 4, dims, str, box, "W1 (E4M3, K-major)", CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+// W1's scale atoms, E (I / 64) (H / 128) atoms of 512 bytes, as rows of 256
+// bytes: a box is one atom (2 rows), no swizzle.
+int map_w1_atoms(CUtensorMap* m, const void* p, int E, int H, int I) {
+    cuuint64_t dims[2] = {256, (cuuint64_t)E * (I / 64) * (H / 128) * 2};
+    cuuint64_t str[1] = {256};
+    cuuint32_t box[2] = {256, 2};
+    return make_map(m, p, 2, dims, str, box, "W1 scale atoms", CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
 struct Ctx {
     moe_layout L;
     int sms;
@@ -351,18 +371,19 @@ int moe_router_topk(const moe_shape* shape, const float* logits, int32_t* topk_i
     return MOE_OK;
 }
 
-// Body of moe_forward (x bf16) and of moe_forward_fp8 (x8 E4M3 bytes and
-// xsf UE8M0 scales instead of x).
+// Body of moe_forward (x, W1 bf16) and of moe_forward_fp8 (x8 / xsf the E4M3
+// input and its scales, W1 / w1sf the E4M3 W1 and its scale atoms).
 static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8, const uint8_t* xsf, const void* W1,
-                        const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream) {
+                        const uint8_t* w1sf, const void* W2, const float* topk_w, void* route_ws, void* saved,
+                        void* y, void* stream, bool fp8) {
     Ctx c;
     int rc = prepare(shape, &c);
     if (rc) return rc;
-    const bool fp8 = x8 != nullptr || xsf != nullptr;
-    if (!W1 || !W2 || !route_ws || !saved ||
+    if (!W1 || !W2 || !route_ws || !saved || (fp8 && !w1sf) ||
         (shape->T > 0 && (!topk_w || !y || (fp8 ? (!x8 || !xsf) : !x))))
         return fail(MOE_EINVAL, "NULL pointer argument");
-    const void* ptrs[] = {x, x8, xsf, W1, W2, topk_w, route_ws, saved, y};
+    if (fp8 && shape->H % 128) return fail(MOE_EUNSUPPORTED, "the FP8 forward needs H to be a multiple of 128");
+    const void* ptrs[] = {x, x8, xsf, W1, w1sf, W2, topk_w, route_ws, saved, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
     if ((rc = query_device(&c, route_ws))) return rc;
@@ -380,7 +401,12 @@ static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8
     // 128 up features x one row chunk of one expert
     GemmMaps m1;
     memset(&m1, 0, sizeof m1);
-    if ((rc = map_w1_halves(&m1.a, W1, E, H, I))) return rc;
+    if (fp8) {
+        if ((rc = map_w1_fp8(&m1.a, W1, E, H, I))) return rc;
+        if ((rc = map_w1_atoms(&m1.b, w1sf, E, H, I))) return rc;
+    } else if ((rc = map_w1_halves(&m1.a, W1, E, H, I))) {
+        return rc;
+    }
     if ((rc = map_2d(&m1.c0, h, L.rows_cap, 2 * I, 32, 32, "h (store)"))) return rc;
     if ((rc = map_2d(&m1.c1, a, L.rows_cap, I, 32, 32, "a (store)"))) return rc;
     GemmArgs g1 = base_args(shape, L, route);
@@ -390,7 +416,7 @@ static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8
     g1.gsrc8 = x8;
     g1.gsf = xsf;
     g1.cmask = cmask;
-    int e = launch_gemm(fp8 ? L1_FWD_FP8 : L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
+    int e = launch_gemm(fp8 ? L1_FWD_MX : L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
     if (e) return cuda_fail(e, "L1 grouped GEMM launch");
 
     // L2 grouped GEMM + routing-weight epilogue -> o; units of 256 features
@@ -417,15 +443,32 @@ static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8
 
 int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2, const float* topk_w,
                 void* route_ws, void* saved, void* y, void* stream) {
-    return forward_impl(shape, x, nullptr, nullptr, W1, W2, topk_w, route_ws, saved, y, stream);
+    return forward_impl(shape, x, nullptr, nullptr, W1, nullptr, W2, topk_w, route_ws, saved, y, stream, false);
 }
 
-int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const void* W1,
-                    const void* W2, const float* topk_w, void* route_ws, void* saved, void* y, void* stream) {
-    if (!x_fp8 || !x_sf) {
-        if (shape && shape->T > 0) return fail(MOE_EINVAL, "NULL pointer argument");
-    }
-    return forward_impl(shape, nullptr, x_fp8, x_sf, W1, W2, topk_w, route_ws, saved, y, stream);
+int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const uint8_t* W1_fp8,
+                    const uint8_t* W1_sf, const void* W2, const float* topk_w, void* route_ws, void* saved, void* y,
+                    void* stream) {
+    return forward_impl(shape, nullptr, x_fp8, x_sf, W1_fp8, W1_sf, W2, topk_w, route_ws, saved, y, stream, true);
+}
+
+int moe_quantize_weights_fp8(const moe_shape* shape, const void* W1, uint8_t* W1_fp8, uint8_t* W1_sf, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!W1 || !W1_fp8 || !W1_sf) return fail(MOE_EINVAL, "NULL pointer argument");
+    if (shape->H % 128) return fail(MOE_EUNSUPPORTED, "FP8 weights need H to be a multiple of 128");
+    const void* ptrs[] = {W1, W1_fp8, W1_sf};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if ((rc = query_device(&c, W1))) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    trace_pre(st);
+    const int e = launch_quantize_w1_fp8(static_cast<const __nv_bfloat16*>(W1), shape->E, shape->H, shape->I, W1_fp8,
+                                         W1_sf, c.sms, st);
+    trace_post(st, "quantize_w1_fp8");
+    if (e) return cuda_fail(e, "W1 FP8 quantization launch");
+    return MOE_OK;
 }
 
 int moe_dequantize_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, void* x_out, void* stream) {

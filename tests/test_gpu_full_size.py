@@ -10,8 +10,8 @@ skewed routing sharp enough to leave experts empty.  Properties that hold at any
 tables bit-exact over the whole routing, every output finite, the combine
 equal to the slot-ordered FP32 sum of the weighted rows for every token, and
 zero weight gradients for experts that got no slot.  At the V3 shape the FP8
-dispatch forward and the FP32 main-gradient backward are also checked bit
-for bit against the bf16 path."""
+forward is checked against the bf16 path on the dequantized operands and
+the FP32 main-gradient backward bit for bit against the bf16 path."""
 import numpy as np
 import pytest
 import torch
@@ -120,11 +120,29 @@ def test_full_size_tiny_every_output():
     compare("tiny dtopk_w", f32(run.dw), ref["dtopk_w"], bf16_output=False)
 
 
-def test_full_size_fp8_dispatch_and_main_grad():
-    """The V3-shaped layer through the two variants, against the bf16 path
-    on the same GPU: the FP8-dispatch forward equals the bf16 forward on the
-    dequantized input bit for bit, and the FP32 main-gradient backward from
-    zero main gradients rounds to the bf16 weight gradients bit for bit."""
+def _dequantize_w1_on_gpu(wq, atoms, E, H, I):
+    """bf16 W1 [E, H, 2I] from E4M3 bytes [E, 2I, H] and the scale atoms, one
+    expert at a time (torch's float8 conversion, exact powers of two)."""
+    f = torch.arange(2 * I, device="cuda")
+    fi = torch.where(f < I, f, f - I)
+    g, r = fi // 64, torch.where(f < I, 0, 64) + fi % 64
+    j = torch.arange(H // 32, device="cuda")
+    idx = (g[:, None] * (H // 128) + (j // 4)[None, :]) * 512 + (16 * (r % 32) + 4 * (r // 32))[:, None] + (j % 4)[None, :]
+    per = (I // 64) * (H // 128) * 512
+    out = torch.empty(E, H, 2 * I, dtype=torch.bfloat16, device="cuda")
+    for e in range(E):
+        sf = atoms[e * per:(e + 1) * per][idx].to(torch.int32) - 127
+        scale = torch.ldexp(torch.ones_like(sf, dtype=torch.float32), sf).repeat_interleave(32, dim=1)
+        out[e] = (wq[e].view(torch.float8_e4m3fn).float() * scale).t().to(torch.bfloat16)
+    return out
+
+
+def test_full_size_fp8_forward_and_main_grad():
+    """The V3-shaped layer through the two variants, against the bf16 path on
+    the same GPU: the FP8 forward (E4M3 input and W1, block-scaled MMA)
+    within the comparison bar of the bf16 forward on the dequantized input
+    and W1, and the FP32 main-gradient backward from zero main gradients
+    rounding to the bf16 weight gradients bit for bit."""
     shape = CONFIGS["v3"]
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     inp = make_layer_inputs(shape, seed=5, device="cuda")
@@ -134,20 +152,27 @@ def test_full_size_fp8_dispatch_and_main_grad():
     B.moe_quantize_fp8(s, inp["x"], q, sf)
     xd = torch.empty_like(inp["x"])
     B.moe_dequantize_fp8(s, q, sf, xd)
+    wq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
+    wsf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_weights_fp8(s, inp["W1"], wq, wsf)
+    W1d = _dequantize_w1_on_gpu(wq, wsf, E, H, I)
     ref = GpuRun(T, H, I, E, k)
-    ref.run(dict(inp, x=xd))
+    ref.run(dict(inp, x=xd, W1=W1d), backward=False)
     y8 = torch.empty_like(ref.y)
-    B.moe_forward_fp8(ref.shape, q, sf, inp["W1"], inp["W2"], inp["topk_w"], ref.route, ref.saved, y8)
+    B.moe_forward_fp8(ref.shape, q, sf, wq, wsf, inp["W2"], inp["topk_w"], ref.route, ref.saved, y8)
     torch.cuda.synchronize()
-    assert torch.equal(y8, ref.y)
-    # the saved activations are again those of the dequantized input: main-grad backward
+    compare("v3 y (fp8) vs bf16 path on the dequantized operands", f32(y8), f32(ref.y))
+    del W1d, wq, wsf, y8
+    # FP32 main gradients from the bf16 forward's saved activations
+    run = GpuRun(T, H, I, E, k)
+    run.run(inp)
     mg1 = torch.zeros(E, H, 2 * I, dtype=torch.float32, device="cuda")
     mg2 = torch.zeros(E, I, H, dtype=torch.float32, device="cuda")
-    dx = torch.empty_like(ref.dx)
-    dw = torch.empty_like(ref.dw)
-    B.moe_backward_main_grad(ref.shape, inp["dY"], xd, inp["W1"], inp["W2"], inp["topk_w"], ref.route, ref.saved,
-                             ref.bwd, dx, mg1, mg2, dw)
+    dx = torch.empty_like(run.dx)
+    dw = torch.empty_like(run.dw)
+    B.moe_backward_main_grad(run.shape, inp["dY"], inp["x"], inp["W1"], inp["W2"], inp["topk_w"], run.route,
+                             run.saved, run.bwd, dx, mg1, mg2, dw)
     torch.cuda.synchronize()
-    assert torch.equal(dx, ref.dx) and torch.equal(dw, ref.dw)
-    assert torch.equal(mg1.to(torch.bfloat16), ref.dW1)
-    assert torch.equal(mg2.to(torch.bfloat16), ref.dW2)
+    assert torch.equal(dx, run.dx) and torch.equal(dw, run.dw)
+    assert torch.equal(mg1.to(torch.bfloat16), run.dW1)
+    assert torch.equal(mg2.to(torch.bfloat16), run.dW2)

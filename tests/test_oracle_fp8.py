@@ -94,3 +94,31 @@ def test_quantize_properties_random():
     err = np.abs(deq - xf)
     tol = np.maximum(np.abs(xf) * 2.0 ** -4, scale * 2.0 ** -10)
     assert np.all(err <= tol)
+
+
+def test_weight_quantization_is_the_per_column_rule():
+    """quantize_weights_fp8 quantizes each column W1[e, :, f] on its own:
+    brute force over the columns of a small W1 with the per-token quantizer
+    and the scales' closed form (448 * 2^(sf - 127) >= max|group| > 224 *
+    2^(sf - 127) for nonzero groups)."""
+    rng = np.random.default_rng(11)
+    E, H, I2 = 2, 96, 6
+    w = (rng.standard_normal((E, H, I2)) * np.logspace(-3, 2, I2)).astype(np.float32)
+    w[0, :32, 1] = 0.0
+    bits = bf16_bits(torch.from_numpy(w).to(torch.bfloat16))
+    q, sf = oracle.quantize_weights_fp8(bits)
+    assert q.shape == (E, I2, H) and sf.shape == (E, I2, H // 32)
+    for e in range(E):
+        for f in range(I2):
+            cq, csf = oracle.quantize_fp8(bits[e, :, f][None, :])
+            assert np.array_equal(q[e, f], cq[0]) and np.array_equal(sf[e, f], csf[0])
+    vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    for e in range(E):
+        for f in range(I2):
+            for g in range(H // 32):
+                amax = np.abs(vals[e, 32 * g:32 * g + 32, f]).max()
+                s = np.ldexp(1.0, int(sf[e, f, g]) - 127)
+                if amax == 0:
+                    assert sf[e, f, g] == 127
+                else:
+                    assert 448 * s >= amax > 224 * s
