@@ -565,6 +565,19 @@ __device__ __forceinline__ int t2_total_units(const GemmArgs& p) {
     return np * p.n_tiles;
 }
 
+// The pair of status words (work counter, clusters done) of a flavour's unit
+// feed: words MOE_STATUS_SCHED + 2 slot, + 1 of the eight the prologue
+// zeroes.  The FP8 L1 shares the bf16 L1's pair (the two are never in flight
+// on one route_ws at once, like any two calls on it).
+template <int F>
+__host__ __device__ constexpr int t2_sched_slot() {
+    return F == L1_FWD_MX ? (int)L1_FWD : F;
+}
+static_assert(t2_sched_slot<L1_FWD>() < 4 && t2_sched_slot<L2_FWD>() < 4 && t2_sched_slot<L2_DGRAD>() < 4 &&
+                  t2_sched_slot<L1_DGRAD>() < 4 && t2_sched_slot<L1_FWD_MX>() < 4 &&
+                  MOE_STATUS_SCHED + 2 * 4 <= MOE_STATUS_WORDS,
+              "unit-feed counters inside the status words the prologue zeroes");
+
 // The even CTA's unit scheduler (one thread).  The work counter and the
 // count of clusters done are status words of route_ws (zeroed by the routing
 // prologue); the last cluster to finish puts both back to zero for the next
@@ -573,7 +586,7 @@ template <int F>
 __device__ void t2_role_sched(const GemmArgs& p, uint32_t ring, T2Bars bars, volatile int* abort) {
     const int total = t2_total_units(p);
     const int ncl = (int)gridDim.x >> 1;
-    int* ctr = reinterpret_cast<int*>(p.status + MOE_STATUS_SCHED + 2 * F);
+    int* ctr = reinterpret_cast<int*>(p.status + MOE_STATUS_SCHED + 2 * t2_sched_slot<F>());
     int* fin = ctr + 1;
     const uint32_t ring1 = cluster_addr_of(ring, 1);
     int u = (int)blockIdx.x >> 1;

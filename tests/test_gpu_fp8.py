@@ -133,6 +133,12 @@ def test_forward_fp8_parity(T, H, I, E, k, seed):
     B.moe_forward_fp8(run.shape, q, sf, wq, wsf, inp["W2"], inp["topk_w"], run.route, run.saved, run.y)
     torch.cuda.synchronize()
     check_tables(run, oracle_route(inp, E))
+    # a second launch on the same tables (its unit feed must start from the
+    # counters the first one left at zero) gives the same bytes
+    y2 = torch.full_like(run.y, float("nan"))
+    B.moe_forward_fp8(run.shape, q, sf, wq, wsf, inp["W2"], inp["topk_w"], run.route, run.saved, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, run.y), "a second FP8 forward on the same routing tables differs"
     # every E4M3 x E4M3 x 2^k product is exact in FP32; the two MMA kinds may
     # still round their FP32 partial sums differently over a long K
     compare("y (fp8) vs bf16 path on the dequantized operands", f32(run.y), f32(ref_run.y))
