@@ -5,8 +5,9 @@ The oracle cannot cover every output at these sizes, so it checks what it
 can compute one by one: y, dx and d(topk_weights) of sampled tokens (from a
 sub-problem holding those tokens and their experts) and the full dW1 / dW2
 of sampled experts (most and least loaded, one below block M and one empty
-when present, two random others); 512 sampled tokens per workload, and a
-skewed routing sharp enough to leave experts empty.  Properties that hold at any size cover the rest: routing
+when present, two random others); every token of the V2-Lite-shaped layer,
+512 sampled tokens of the larger ones, and a skewed routing sharp enough to
+leave experts empty.  Properties that hold at any size cover the rest: routing
 tables bit-exact over the whole routing, every output finite, the combine
 equal to the slot-ordered FP32 sum of the weighted rows for every token, and
 zero weight gradients for experts that got no slot.  At the V3 shape the FP8
@@ -50,7 +51,7 @@ def _pick_experts(counts, rng, heaviest=True, n_random=2):
 
 
 # (workload, sampled tokens, weight-gradient experts include the most loaded)
-CASES = [("v2lite", 512, True), ("v3", 512, True), ("skew", 512, True), ("wide", 512, True),
+CASES = [("v2lite", 4096, True), ("v3", 512, True), ("skew", 512, True), ("wide", 512, True),
          ("skew_c1", 128, False)]
 
 
