@@ -89,10 +89,15 @@ enum {
  *    tiles   int32[tiles_cap]  expert owning rows [m*block_m, (m+1)*block_m);
  *                              -1 for m >= Mpad/block_m
  *    status  int32[16]         MOE_STATUS_* words
- *    pair_offs  int32[E+1]     exclusive prefix sum of ceil(tiles_e / 2), where
- *                              tiles_e = (offs[e+1]-offs[e]) / block_m: the GEMMs
- *                              take an expert's M tiles two at a time
- *    pair_owner int32[tiles_cap] expert of tile pair q; -1 past pair_offs[E]
+ *    pair_offs  int32[E+1]     the GEMMs take an expert's M tiles two at a time
+ *                              (ceil(tiles_e / 2) pairs, tiles_e =
+ *                              (offs[e+1]-offs[e]) / block_m) and walk the
+ *                              experts in decreasing order of counts[e] (ties:
+ *                              smaller e first); pair_offs[e] = pairs of the
+ *                              experts before e in that walk, pair_offs[E] =
+ *                              all pairs
+ *    pair_owner int32[tiles_cap] expert of tile pair q of the walk; -1 past
+ *                              pair_offs[E]
  *    blk_counts int32[route_blocks*(E+1) (at least 1)] prologue scratch: the
  *                              slots are cut into route_blocks blocks of whole
  *                              1024-slot rounds; per block and expert the

@@ -53,8 +53,8 @@ struct GemmArgs {
     const int32_t* offs;
     const int32_t* counts;
     const int32_t* tiles;
-    const int32_t* pair_offs;   // exclusive prefix sum of ceil(tiles_e / 2)
-    const int32_t* pair_owner;  // expert of each tile pair
+    const int32_t* pair_offs;   // first tile pair of each expert in the walk (decreasing count)
+    const int32_t* pair_owner;  // expert of each tile pair of the walk
     int32_t* status;
     const __nv_bfloat16* gsrc;  // gathered source rows [T, H] (x or dY)
     const float* topk_w;

@@ -17,9 +17,12 @@
 //      the block counts (in place) and the total count; block-M padded sizes
 //      and their exclusive prefix sum (warp-shuffle scan) -> offs, Mpad, the
 //      tile-owner table, the status words, and the two scheduling tables of
-//      the SM-pair GEMMs: pair_offs = exclusive prefix sum of
-//      ceil(tiles_e / 2), pair_owner[q] = expert of tile pair q (-1 past the
-//      last pair).
+//      the SM-pair GEMMs, which walk the experts in decreasing order of
+//      routed rows (ties: smaller id first; a bitonic sort of (count, id)):
+//      pair_offs[e] = first tile pair of expert e in that walk (the
+//      exclusive prefix sum of ceil(tiles / 2) over the experts before it),
+//      pair_offs[E] = the number of pairs, pair_owner[q] = expert of tile
+//      pair q of the walk (-1 past the last pair).
 //   3. route_place (grid over slots): row = offs[e] + (slots of e in earlier
 //      blocks) + (rank inside the block); perm[row] = s, inv[s] = row, and
 //      inv[s] = -1 for a dropped slot.
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ int sm[];
     int* cnt = sm;       // [E]
     int* base = sm + E;  // [E]
+    __shared__ unsigned long long walk_key[kMaxExperts];  // (count descending, id) sort keys
     __shared__ int warp_tot[kWarps];
     __shared__ int warp_tot2[kWarps];
     __shared__ int s_invalid;
@@ -132,17 +136,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (lane == 0 && bad) atomicAdd(&s_invalid, bad);
 
-    // padded exclusive scan over experts; each thread owns a contiguous run
-    // (and the same scan of the per-expert tile-pair counts)
+    // the GEMMs' walk order: ascending bitonic sort of ((2^31-1 - count) << 32
+    // | id) over the next power of two >= E (padding keys sort last), one key
+    // per thread; partners closer than a warp are exchanged by shuffles,
+    // farther ones through shared memory
+    static_assert(kThreads >= kMaxExperts, "one sort key per thread");
+    int np2 = 1;
+    while (np2 < E) np2 <<= 1;
+    unsigned long long key = tid < E ? ((unsigned long long)(0x7fffffff - cnt[tid]) << 32) | (unsigned)tid : ~0ull;
+    for (int len = 2; len <= np2; len <<= 1) {
+        for (int j = len >> 1; j > 0; j >>= 1) {
+            unsigned long long other;
+            if (j >= 32) {
+                if (tid < np2) walk_key[tid] = key;
+                __syncthreads();
+                other = walk_key[(tid ^ j) & (kMaxExperts - 1)];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(0xffffffffu, key, j);
+            }
+            // the lower index of a pair keeps the smaller key in an ascending run
+            const bool keep_min = ((tid & j) == 0) == ((tid & len) == 0);
+            key = keep_min ? (key < other ? key : other) : (key > other ? key : other);
+        }
+    }
+    if (tid < np2) walk_key[tid] = key;
+    __syncthreads();
+
+    // padded exclusive scan over experts (by id) and the scan of the tile-pair
+    // counts over the walk (by rank); each thread owns a contiguous run of both
     const int per = (E + kThreads - 1) / kThreads;
     const int e0 = tid * per;
     int run = 0, run2 = 0;
     for (int q = 0; q < per; ++q) {
         const int e = e0 + q;
         if (e < E) {
-            const int t = (cnt[e] + bm - 1) / bm;
-            run += t * bm;
-            run2 += (t + 1) / 2;
+            run += ((cnt[e] + bm - 1) / bm) * bm;
+            const int w = (int)(walk_key[e] & 0xffffffffu);
+            run2 += ((cnt[w] + bm - 1) / bm + 1) / 2;
         }
     }
     const int incl = warp_incl_scan(run, lane);
@@ -168,10 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             offs[e] = acc;
             base[e] = acc;
             counts[e] = cnt[e];
-            pair_offs[e] = acc2;
-            for (int pq = acc2; pq < acc2 + (t + 1) / 2; ++pq) pair_owner[pq] = e;
             acc += t * bm;
-            acc2 += (t + 1) / 2;
+            const int w = (int)(walk_key[e] & 0xffffffffu);  // expert of rank e
+            const int np = ((cnt[w] + bm - 1) / bm + 1) / 2;
+            pair_offs[w] = acc2;
+            for (int pq = acc2; pq < acc2 + np; ++pq) pair_owner[pq] = w;
+            acc2 += np;
         }
     }
     if (tid == kThreads - 1) {

@@ -154,13 +154,26 @@ def check_tables(run: GpuRun, ref: dict):
     assert st[B.STATUS_NUM_TILES] == ref["num_tiles"]
     assert st[B.STATUS_N_INVALID] == ref["n_invalid"]
     assert st[B.STATUS_FLAGS] == 0, "a kernel reported a bounded-wait timeout"
-    # scheduling tables of the GEMM clusters, derived from the (bit-exact) offsets
-    tiles_e = np.diff(ref["offs"]) // 128
-    pairs_e = (tiles_e + 1) // 2
-    pair_offs = np.concatenate([[0], np.cumsum(pairs_e)]).astype(np.int32)
+    # scheduling tables of the GEMM clusters, derived from the (bit-exact)
+    # counts and offsets: experts walked by decreasing count, ties by id
+    pair_offs, owner = walk_tables(ref["counts"], ref["offs"], len(got["pair_owner"]))
     assert np.array_equal(got["pair_offs"], pair_offs)
-    owner = np.full(len(got["pair_owner"]), -1, np.int32)
-    for e in range(len(pairs_e)):
-        owner[pair_offs[e]: pair_offs[e + 1]] = e
     assert np.array_equal(got["pair_owner"], owner)
     assert st[B.STATUS_NUM_PAIRS] == pair_offs[-1]
+
+
+def walk_tables(counts, offs, cap):
+    """pair_offs and pair_owner (include/moe_layer.h) from the routing counts
+    and block-padded offsets: a stable sort of the experts by decreasing count."""
+    counts = np.asarray(counts, np.int64)
+    pairs_e = (np.diff(np.asarray(offs, np.int64)) // 128 + 1) // 2
+    walk = sorted(range(len(counts)), key=lambda e: (-counts[e], e))
+    pair_offs = np.zeros(len(counts) + 1, np.int32)
+    owner = np.full(cap, -1, np.int32)
+    q = 0
+    for e in walk:
+        pair_offs[e] = q
+        owner[q: q + pairs_e[e]] = e
+        q += pairs_e[e]
+    pair_offs[-1] = q
+    return pair_offs, owner
