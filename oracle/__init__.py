@@ -77,6 +77,10 @@ def _lib():
             L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_quantize_fp8.argtypes = [i32, i32, i32, vp, vp, vp]
             L.oracle_quantize_fp8.restype = None
+            L.oracle_quantize_fp8_f64.argtypes = [i32, i32, i32, vp, vp, vp]
+            L.oracle_quantize_fp8_f64.restype = None
+            L.oracle_forward_fp8.argtypes = [i32] * 5 + [vp] * 5 + [i32, vp, vp, vp, vp]
+            L.oracle_forward_fp8.restype = None
             _LIB = L
     return _LIB
 
@@ -146,6 +150,57 @@ def quantize_weights_fp8(W1_bits: np.ndarray, gran: int = 32):
     E, H, I2 = wb.shape
     q, sf = quantize_fp8(np.ascontiguousarray(wb.transpose(0, 2, 1)).reshape(E * I2, H), gran)
     return q.reshape(E, I2, H), sf.reshape(E, I2, H // gran)
+
+
+def quantize_fp8_values(v: np.ndarray, gran: int = 32):
+    """quantize_fp8's rule on float64 values [T, H] instead of bf16 bit
+    patterns (the activations between the FP8 forward's two GEMMs).  Returns
+    q uint8 [T, H] and sf uint8 [T, H // gran]."""
+    x = np.ascontiguousarray(v, dtype=np.float64)
+    T, H = x.shape
+    if H % gran:
+        raise ValueError("H must be a multiple of the granularity")
+    q = np.zeros((max(T, 1), H), np.uint8)
+    sf = np.zeros((max(T, 1), H // gran), np.uint8)
+    _lib().oracle_quantize_fp8_f64(T, H, gran, _p(x), _p(q), _p(sf))
+    return q[:T], sf[:T]
+
+
+def quantize_w2_fp8(W2_bits: np.ndarray, gran: int = 32):
+    """FP8 weights for the L2 GEMM, the counterpart of quantize_weights_fp8:
+    W2_bits: bf16 bit patterns [E, I, H]; each column W2[e, :, h] is quantized
+    like a token of quantize_fp8 (groups of `gran` consecutive i, the
+    contraction index of the L2 GEMM).  Returns q uint8 [E, H, I] and sf
+    uint8 [E, H, I // gran]."""
+    wb = np.ascontiguousarray(W2_bits, dtype=np.uint16)
+    E, I, H = wb.shape
+    q, sf = quantize_fp8(np.ascontiguousarray(wb.transpose(0, 2, 1)).reshape(E * H, I), gran)
+    return q.reshape(E, H, I), sf.reshape(E, H, I // gran)
+
+
+def forward_fp8(x, W1, W2, topk_idx, topk_w, tokens=None):
+    """FP8 forward for the listed tokens (all by default): x [T, H], W1
+    [E, H, 2I], W2 [E, I, H] as the float64 values the E4M3 operands stand
+    for; the SwiGLU output of every slot is quantized to E4M3 with UE8M0
+    scales per 32 consecutive features before the L2 contraction (see
+    oracle_forward_fp8).  Returns y [n, H] float64, aq uint8 [n, k, I] and
+    asf uint8 [n, k, I // 32]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    W1 = np.ascontiguousarray(W1, dtype=np.float64)
+    W2 = np.ascontiguousarray(W2, dtype=np.float64)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    T, H, I, E, k = _dims(x, W1, W2, idx)
+    if I % 32:
+        raise ValueError("I must be a multiple of 32")
+    toks = np.ascontiguousarray(np.arange(T) if tokens is None else tokens, dtype=np.int32)
+    n = len(toks)
+    y = np.zeros((max(n, 1), H), np.float64)
+    aq = np.zeros((max(n, 1), k, I), np.uint8)
+    asf = np.zeros((max(n, 1), k, I // 32), np.uint8)
+    _lib().oracle_forward_fp8(T, H, I, E, k, _p(x), _p(W1), _p(W2), _p(idx), _p(w), n, _p(toks), _p(y), _p(aq),
+                              _p(asf))
+    return y[:n], aq[:n], asf[:n]
 
 
 def dequantize_fp8(q: np.ndarray, sf: np.ndarray, gran: int = 32) -> np.ndarray:

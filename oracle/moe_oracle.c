@@ -118,6 +118,99 @@ void oracle_quantize_fp8(int T, int H, int gran, const uint16_t* x, uint8_t* q, 
     }
 }
 
+/*
+ * The same quantization of float64 values instead of bfloat16 bit patterns:
+ * used for the activations between the two GEMMs of the FP8 forward (below),
+ * which are computed, not stored as bf16.  One group of `gran` values.
+ */
+static void fp8_quantize_group_f64(const double* v, int gran, uint8_t* q, uint8_t* sf) {
+    double amax = 0.0;
+    for (int i = 0; i < gran; ++i)
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    const int e = fp8_group_exponent(amax);
+    *sf = (uint8_t)(e + 127);
+    for (int i = 0; i < gran; ++i) q[i] = oracle_e4m3_encode(ldexp(v[i], -e));
+}
+
+void oracle_quantize_fp8_f64(int T, int H, int gran, const double* x, uint8_t* q, uint8_t* sf) {
+    const int G = H / gran;
+    for (int t = 0; t < T; ++t)
+        for (int g = 0; g < G; ++g)
+            fp8_quantize_group_f64(x + (size_t)t * H + (size_t)g * gran, gran, q + (size_t)t * H + (size_t)g * gran,
+                                   sf + (size_t)t * G + g);
+}
+
+/*
+ * FP8 forward (DeepGEMM Mega-MoE article, "Code Example: Fused Overlap
+ * Path": the layer runs on FP8 activations and transformed low-precision
+ * weights).  The operands x, W1, W2 are given as the float64 values they
+ * stand for (the dequantized E4M3 inputs and weights).  For each token t and
+ * slot j with expert e, in float64:
+ *   hg, hu, a = silu(hg) * hu                    as in the forward below;
+ *   a is quantized like a token of the input: groups of 32 consecutive i,
+ *     scale 2^e with the smallest e such that 448 * 2^e >= max|group|,
+ *     aq[i] = E4M3(a[i] / 2^e), asf[g] = e + 127;
+ *   o[c] = sum_i decode(aq[i]) 2^(asf[i / 32] - 127) W2[e, i, c];
+ *   y[t, c] += w[t, j] o[c].
+ * aq_out [n_tok][k][I] and asf_out [n_tok][k][I / 32] receive each slot's
+ * quantized activations (zeros for a slot without a valid expert).  No
+ * activation clamp.
+ */
+void oracle_forward_fp8(int T, int H, int I, int E, int k, const double* x, const double* W1, const double* W2,
+                        const int32_t* topk_idx, const float* topk_w, int n_tok, const int32_t* tok_list,
+                        double* y_out, uint8_t* aq_out, uint8_t* asf_out) {
+    (void)T;
+    const int G = I / 32;
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double* hg = (double*)malloc(sizeof(double) * (size_t)I);
+        double* hu = (double*)malloc(sizeof(double) * (size_t)I);
+        double* a = (double*)malloc(sizeof(double) * (size_t)I);
+        double* o = (double*)malloc(sizeof(double) * (size_t)H);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int n = 0; n < n_tok; ++n) {
+            const int t = tok_list[n];
+            double* y = y_out + (size_t)n * H;
+            for (int c = 0; c < H; ++c) y[c] = 0.0;
+            for (int j = 0; j < k; ++j) {
+                uint8_t* aq = aq_out + ((size_t)n * k + j) * I;
+                uint8_t* asf = asf_out + ((size_t)n * k + j) * G;
+                memset(aq, 0, (size_t)I);
+                memset(asf, 0, (size_t)G);
+                const int e = topk_idx[(size_t)t * k + j];
+                if (e < 0 || e >= E) continue;
+                for (int i = 0; i < I; ++i) { hg[i] = 0.0; hu[i] = 0.0; }
+                for (int h = 0; h < H; ++h) {
+                    const double xv = x[(size_t)t * H + h];
+                    const double* row = W1 + ((size_t)e * H + h) * (size_t)(2 * I);
+                    for (int i = 0; i < I; ++i) {
+                        hg[i] += xv * row[i];
+                        hu[i] += xv * row[I + i];
+                    }
+                }
+                for (int i = 0; i < I; ++i) a[i] = hg[i] / (1.0 + exp(-hg[i])) * hu[i];
+                for (int g = 0; g < G; ++g) fp8_quantize_group_f64(a + 32 * g, 32, aq + 32 * g, asf + g);
+                for (int c = 0; c < H; ++c) o[c] = 0.0;
+                for (int i = 0; i < I; ++i) {
+                    const double ai = oracle_e4m3_decode(aq[i]) * ldexp(1.0, (int)asf[i / 32] - 127);
+                    const double* row = W2 + ((size_t)e * I + i) * (size_t)H;
+                    for (int c = 0; c < H; ++c) o[c] += ai * row[c];
+                }
+                const double wv = (double)topk_w[(size_t)t * k + j];
+                for (int c = 0; c < H; ++c) y[c] += wv * o[c];
+            }
+        }
+        free(hg);
+        free(hu);
+        free(a);
+        free(o);
+    }
+}
+
 /* ----------------------------------------------------------------- router */
 
 /*

@@ -2,6 +2,8 @@
 power-of-two scales per 32-element group), against things other than the
 oracle itself: PyTorch's float8_e4m3fn conversion, a brute-force nearest
 search over the 256 codes, and the closed-form properties of the scale."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -122,3 +124,119 @@ def test_weight_quantization_is_the_per_column_rule():
                     assert sf[e, f, g] == 127
                 else:
                     assert 448 * s >= amax > 224 * s
+
+
+def _nearest_code(x):
+    """E4M3 code nearest to x by search over the decoded values (ties: the
+    even mantissa), independent of oracle.e4m3_encode."""
+    codes = [c for c in range(256) if not np.isnan(oracle.e4m3_decode(c))]
+    vals = np.array([oracle.e4m3_decode(c) for c in codes])
+    d = np.abs(vals - x)
+    best = np.nonzero(d == d.min())[0]
+    cand = [codes[i] for i in best]
+    if len(set(vals[best])) > 1:
+        cand = [c for c in cand if (c & 1) == 0]
+    return cand[0]
+
+
+def _group_exponent(amax):
+    """The smallest e with 448 * 2^e >= amax, by search (0 for amax = 0)."""
+    if amax == 0:
+        return 0
+    e = -127
+    while 448.0 * 2.0 ** e < amax:
+        e += 1
+    return e
+
+
+def test_value_quantization_equals_the_bit_pattern_rule():
+    """quantize_fp8_values on bf16-representable float64 values gives the
+    bytes quantize_fp8 gives on their bit patterns."""
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(48, 256, generator=g) * torch.logspace(-5, 3, 48).unsqueeze(1)).to(torch.bfloat16)
+    x[0, :32] = 0.0
+    x[1, 40] = 448.0
+    q0, sf0 = oracle.quantize_fp8(bf16_bits(x))
+    q1, sf1 = oracle.quantize_fp8_values(x.double().numpy())
+    assert np.array_equal(q0, q1) and np.array_equal(sf0, sf1)
+
+
+def test_value_quantization_brute_force():
+    """Values that are not bf16 (the FP8 forward's activations): scale by
+    search for the smallest exponent, codes by nearest search."""
+    rng = np.random.default_rng(22)
+    v = rng.standard_normal((6, 64)) * np.logspace(-6, 4, 6)[:, None]
+    v[2, 32:] = 0.0
+    v[3, 7] = 448.0 * 2.0 ** 5  # amax on a scale boundary
+    q, sf = oracle.quantize_fp8_values(v)
+    for t in range(v.shape[0]):
+        for g in range(2):
+            grp = v[t, 32 * g:32 * g + 32]
+            e = _group_exponent(np.abs(grp).max())
+            assert sf[t, g] == e + 127, (t, g)
+            for i in range(32):
+                assert q[t, 32 * g + i] == _nearest_code(grp[i] / 2.0 ** e) or (
+                    oracle.e4m3_decode(q[t, 32 * g + i]) == oracle.e4m3_decode(_nearest_code(grp[i] / 2.0 ** e)))
+
+
+def test_w2_quantization_is_the_per_column_rule():
+    """quantize_w2_fp8 quantizes each column W2[e, :, h] (the L2 GEMM's
+    contraction index i) like a token."""
+    rng = np.random.default_rng(23)
+    E, I, H = 2, 64, 5
+    w = (rng.standard_normal((E, I, H)) * np.logspace(-2, 3, H)).astype(np.float32)
+    bits = bf16_bits(torch.from_numpy(w).to(torch.bfloat16))
+    q, sf = oracle.quantize_w2_fp8(bits)
+    assert q.shape == (E, H, I) and sf.shape == (E, H, I // 32)
+    vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for e in range(E):
+        for h in range(H):
+            for g in range(I // 32):
+                grp = vals[e, 32 * g:32 * g + 32, h]
+                ex = _group_exponent(np.abs(grp).max())
+                assert sf[e, h, g] == ex + 127
+                got = np.array([oracle.e4m3_decode(c) for c in q[e, h, 32 * g:32 * g + 32]])
+                ref = np.array([oracle.e4m3_decode(_nearest_code(x / 2.0 ** ex)) for x in grp])
+                assert np.array_equal(got, ref)
+
+
+def test_forward_fp8_brute_force():
+    """oracle.forward_fp8 against the definition written out in Python loops:
+    h and SwiGLU per slot, each 32-feature group of the activations scaled
+    by a searched exponent and rounded to the nearest code, the L2
+    contraction on the dequantized activations, the weighted sum; with an
+    invalid slot (-1) and an expert no slot uses."""
+    rng = np.random.default_rng(24)
+    T, H, I, E, k = 3, 8, 64, 3, 2
+    x = rng.standard_normal((T, H))
+    W1 = rng.standard_normal((E, H, 2 * I)) * 0.7
+    W2 = rng.standard_normal((E, I, H)) * 0.3
+    idx = np.array([[0, 2], [2, -1], [0, 0]], np.int32)
+    w = np.array([[0.7, 0.3], [1.0, 0.5], [0.25, 0.75]], np.float32)
+    y, aq, asf = oracle.forward_fp8(x, W1, W2, idx, w)
+    for t in range(T):
+        yr = np.zeros(H)
+        for j in range(k):
+            e = idx[t, j]
+            if e < 0:
+                assert not aq[t, j].any() and not asf[t, j].any()
+                continue
+            a = np.zeros(I)
+            for i in range(I):
+                g = u = 0.0
+                for h in range(H):
+                    g += x[t, h] * W1[e, h, i]
+                    u += x[t, h] * W1[e, h, I + i]
+                a[i] = g / (1.0 + math.exp(-g)) * u
+            deq = np.zeros(I)
+            for gi in range(I // 32):
+                grp = a[32 * gi:32 * gi + 32]
+                ex = _group_exponent(np.abs(grp).max())
+                assert asf[t, j, gi] == ex + 127
+                for i in range(32):
+                    c = _nearest_code(grp[i] / 2.0 ** ex)
+                    assert oracle.e4m3_decode(aq[t, j, 32 * gi + i]) == oracle.e4m3_decode(c)
+                    deq[32 * gi + i] = oracle.e4m3_decode(c) * 2.0 ** ex
+            o = np.array([sum(deq[i] * W2[e, i, c] for i in range(I)) for c in range(H)])
+            yr += float(w[t, j]) * o
+        np.testing.assert_allclose(y[t], yr, rtol=1e-12, atol=1e-12)
