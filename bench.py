@@ -614,28 +614,39 @@ def run_ours(args):
                   "note": "median of 20 runs of moe_router_topk (router kernel + routing prologue) on the "
                           "workload's logits; not part of the layer step"}
 
-    # the FP8 forward (E4M3 input per token and E4M3 W1 per column, UE8M0
-    # scales per 32 elements of K, block-scaled MMA in L1), timed beside the
-    # bf16 forward: an inference variant, not the layer step.  W1 is
-    # quantized once beforehand (a weight transform), timed on its own.
+    # the FP8 forward (E4M3 input per token, E4M3 W1 and W2 per column, UE8M0
+    # scales per 32 elements of K, block-scaled MMA in both GEMMs, a
+    # quantized between them), timed beside the bf16 forward: an inference
+    # variant, not the layer step.  The weights are quantized once
+    # beforehand (a weight transform), timed on their own.
     fp8 = None
-    if not args.no_fp8 and H % 128 == 0:
+    if not args.no_fp8 and H % 128 == 0 and I % 128 == 0:
         xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
         xsf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
-        wq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
-        wsf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
-        B.moe_quantize_weights_fp8(ws.shape, inp["W1"], wq, wsf)
+        w1q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        w1sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
+        w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        w2sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device=dev)
+
+        def quantize_weights():
+            B.moe_quantize_weights_fp8(ws.shape, inp["W1"], w1q, w1sf)
+            B.moe_quantize_w2_fp8(ws.shape, inp["W2"], w2q, w2sf)
+
+        quantize_weights()
         torch.cuda.synchronize()
         wtrace = B.KernelTrace(max_launches=2 * 3)
         with wtrace:
             for _ in range(3):
-                B.moe_quantize_weights_fp8(ws.shape, inp["W1"], wq, wsf)
+                quantize_weights()
         torch.cuda.synchronize()
-        wq_ms = statistics.median(d for _, d in wtrace.durations_ms())
+        wq = {}
+        for kn, d in wtrace.durations_ms():
+            wq.setdefault(kn, []).append(d)
+        wq_ms = {kn: statistics.median(v) for kn, v in wq.items()}
 
         def fwd_fp8():
             B.moe_quantize_fp8(ws.shape, inp["x"], xq, xsf)
-            B.moe_forward_fp8(ws.shape, xq, xsf, wq, wsf, inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
+            B.moe_forward_fp8(ws.shape, xq, xsf, w1q, w1sf, w2q, w2sf, inp["topk_w"], ws.route, ws.saved, y)
 
         def fwd_bf16():
             B.moe_forward(ws.shape, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
@@ -655,22 +666,32 @@ def run_ours(args):
             for kn, d in ftrace.durations_ms():
                 kk.setdefault(kn, []).append(d)
             per[name] = {kn: statistics.median(v) for kn, v in kk.items()}
+        tk = T * k
         q_bytes = T * H * 2 + T * H + T * H // 32
         l1_ms = per["fp8"]["gemm_l1_fwd_fp8"]
-        l1_bytes = E * 2 * I * H + E * 2 * I * H // 32 + T * H + T * H // 32 + 2.0 * T * k * 2 * I  # W1, x, h
+        l2_ms = per["fp8"]["gemm_l2_fwd_fp8"]
+        # W1 and its scales, x and its scales, h (bf16), a (E4M3) and its scales
+        l1_bytes = E * 2 * I * H * (1 + 1 / 32) + T * H * (1 + 1 / 32) + 2.0 * tk * 2 * I + tk * I * (1 + 1 / 32)
+        # W2 and its scales, a and its scales, o (bf16)
+        l2_bytes = E * H * I * (1 + 1 / 32) + tk * I * (1 + 1 / 32) + 2.0 * tk * H
+        hbm = float(peaks["hbm_gbs"])
         fp8 = {"forward_ms": sum(per["fp8"].values()), "bf16_forward_ms": sum(per["bf16"].values()),
                "kernels_ms": per["fp8"], "bf16_kernels_ms": per["bf16"],
                "quantize_gbs": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9,
-               "quantize_frac_of_hbm": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
+               "quantize_frac_of_hbm": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9 / hbm,
                "l1_fp8_gbs": l1_bytes / (l1_ms / 1e3) / 1e9,
-               "l1_fp8_frac_of_hbm": l1_bytes / (l1_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"]),
-               "l1_fp8_tflops": 4.0 * H * I * T * k / (l1_ms / 1e3) / 1e12,
-               "forward_tflops": 6.0 * H * I * T * k / (sum(per["fp8"].values()) / 1e3) / 1e12,
+               "l1_fp8_frac_of_hbm": l1_bytes / (l1_ms / 1e3) / 1e9 / hbm,
+               "l1_fp8_tflops": 4.0 * H * I * tk / (l1_ms / 1e3) / 1e12,
+               "l2_fp8_gbs": l2_bytes / (l2_ms / 1e3) / 1e9,
+               "l2_fp8_frac_of_hbm": l2_bytes / (l2_ms / 1e3) / 1e9 / hbm,
+               "l2_fp8_tflops": 2.0 * H * I * tk / (l2_ms / 1e3) / 1e12,
+               "forward_tflops": 6.0 * H * I * tk / (sum(per["fp8"].values()) / 1e3) / 1e12,
                "weight_quantize_ms": wq_ms,
                "note": "median of 10 runs of moe_quantize_fp8 + moe_forward_fp8 (and of moe_forward) on the "
-                       "workload; L1 multiplies E4M3 x and E4M3 W1 (quantized once beforehand, "
-                       "weight_quantize_ms) with block-scaled tcgen05.mma, L2 stays bf16; not part of the step"}
-        del wq, wsf
+                       "workload; both GEMMs multiply E4M3 operands (W1 and W2 quantized once beforehand, "
+                       "weight_quantize_ms) with block-scaled tcgen05.mma, a quantized to E4M3 in the L1 "
+                       "epilogue; not part of the step"}
+        del w1q, w1sf, w2q, w2sf
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -200,19 +200,41 @@ int moe_quantize_fp8(const moe_shape* shape, const void* x, uint8_t* x_fp8, uint
  * `stream`; other errors as for moe_route_prologue. */
 int moe_quantize_weights_fp8(const moe_shape* shape, const void* W1, uint8_t* W1_fp8, uint8_t* W1_sf, void* stream);
 
-/* FP8 forward: moe_forward with the input given as moe_quantize_fp8's
- * x_fp8 / x_sf and W1 as moe_quantize_weights_fp8's W1_fp8 / W1_sf; W2 stays
- * bf16.  The L1 GEMM multiplies the E4M3 operands on the tensor cores with
- * their UE8M0 scales applied per 32 elements of K (block-scaled MMA), FP32
- * accumulation, so the result is moe_forward on the dequantized input and
- * the dequantized W1 (up to the order of the FP32 sums); it reads half the
- * bytes of W1 and of the gathered rows.  Needs H a multiple of 128.
- * Everything else (saved, y, route_ws, errors) as for moe_forward.  An
- * inference path: the pages' FP8 operator is a forward; training steps use
- * moe_forward / moe_backward. */
+/* FP8 W2 for moe_forward_fp8, the counterpart of moe_quantize_weights_fp8:
+ * W2 bf16[E,I,H] -> W2_fp8 = E4M3 bytes, K-major [E][H][I] (column h of W2
+ * as a row), and W2_sf = UE8M0 scales, one per 32 consecutive i of a column
+ * (the same rule as moe_quantize_fp8, along I), E * H * I/32 bytes in the
+ * layout the L2 kernel loads: for column h, group g = h / 128 and row r =
+ * h mod 128; for the 32-group j32 of i, block kb = j32 / 4 and step j = j32
+ * mod 4; byte
+ *   ((e (H/128) + g) (I/128) + kb) 512 + 16 (r mod 32) + 4 floor(r / 32) + j.
+ * Needs H and I multiples of 128 (MOE_EUNSUPPORTED otherwise).  Kernels on
+ * `stream`; other errors as for moe_route_prologue. */
+int moe_quantize_w2_fp8(const moe_shape* shape, const void* W2, uint8_t* W2_fp8, uint8_t* W2_sf, void* stream);
+
+/* FP8 forward (DeepGEMM Mega-MoE article, "Code Example: Fused Overlap
+ * Path": the layer on FP8 activations and transformed FP8 weights):
+ * moe_forward with the input given as moe_quantize_fp8's x_fp8 / x_sf, W1 as
+ * moe_quantize_weights_fp8's W1_fp8 / W1_sf and W2 as moe_quantize_w2_fp8's
+ * W2_fp8 / W2_sf.  Both grouped GEMMs multiply E4M3 operands on the tensor
+ * cores with their UE8M0 scales applied per 32 elements of K (block-scaled
+ * MMA), FP32 accumulation.  Between them the SwiGLU output a of every routed
+ * row is quantized in the L1 kernel's epilogue with the rule of
+ * moe_quantize_fp8 (groups of 32 consecutive features of I, the scale's
+ * maximum taken over the FP32 values of a), so y is the FP8 layer: h and a
+ * from the dequantized x and W1, a rounded to E4M3 with its scales, o from
+ * that and the dequantized W2, the weighted sum.  It reads half the bytes of
+ * both weights and of the gathered rows.  saved receives h (bf16) and o as
+ * in moe_forward, and in a's region the E4M3 rows of a (u8[rows_cap, I] at
+ * offset a) followed by their scales (u8[rows_cap, I/32] at offset a +
+ * rows_cap * I); padding rows hold codes 0 with scale byte 127.  Needs H and
+ * I multiples of 128 and no activation clamp (MOE_EUNSUPPORTED otherwise).
+ * Everything else (route_ws, y, errors) as for moe_forward.  An inference
+ * path: the pages' FP8 operator is a forward; training steps use moe_forward
+ * / moe_backward. */
 int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const uint8_t* W1_fp8,
-                    const uint8_t* W1_sf, const void* W2, const float* topk_w, void* route_ws, void* saved, void* y,
-                    void* stream);
+                    const uint8_t* W1_sf, const uint8_t* W2_fp8, const uint8_t* W2_sf, const float* topk_w,
+                    void* route_ws, void* saved, void* y, void* stream);
 
 /* The inverse of moe_quantize_fp8: x_out bf16[T,H] = decode(x_fp8) *
  * 2^(x_sf - 127), exactly (every such value is a bf16 value).  Errors as for

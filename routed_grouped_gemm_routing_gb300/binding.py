@@ -70,12 +70,13 @@ def lib():
             L.moe_backward_main_grad.argtypes = [P(MoeShape)] + [vp] * 13
             L.moe_quantize_fp8.argtypes = [P(MoeShape)] + [vp] * 4
             L.moe_dequantize_fp8.argtypes = [P(MoeShape)] + [vp] * 4
-            L.moe_forward_fp8.argtypes = [P(MoeShape)] + [vp] * 10
+            L.moe_forward_fp8.argtypes = [P(MoeShape)] + [vp] * 11
             L.moe_quantize_weights_fp8.argtypes = [P(MoeShape)] + [vp] * 4
+            L.moe_quantize_w2_fp8.argtypes = [P(MoeShape)] + [vp] * 4
             L.moe_read_status.argtypes = [P(MoeShape), vp, vp, vp]
             for n in ("moe_workspace_layout", "moe_route_prologue", "moe_router_topk", "moe_forward", "moe_backward", "moe_backward_main_grad",
                       "moe_quantize_fp8", "moe_dequantize_fp8", "moe_forward_fp8", "moe_quantize_weights_fp8",
-                      "moe_read_status"):
+                      "moe_quantize_w2_fp8", "moe_read_status"):
                 getattr(L, n).restype = ctypes.c_int
             L.moe_trace_begin.argtypes = [vp, ctypes.c_int]
             L.moe_trace_begin.restype = ctypes.c_int
@@ -198,16 +199,30 @@ def moe_quantize_weights_fp8(shape: MoeShape, W1, W1_fp8, W1_sf, stream=None):
         _stream(stream)))
 
 
-def moe_forward_fp8(shape: MoeShape, x_fp8, x_sf, W1_fp8, W1_sf, W2, topk_w, route_ws, saved, y, stream=None):
-    """moe_forward on E4M3 operands: x_fp8 / x_sf from moe_quantize_fp8 and
-    W1_fp8 / W1_sf from moe_quantize_weights_fp8 (block-scaled MMA); W2 bf16."""
+def moe_quantize_w2_fp8(shape: MoeShape, W2, W2_fp8, W2_sf, stream=None):
+    """W2 bf16 [E, I, H] -> W2_fp8 uint8 [E, H, I] (E4M3, K-major) and W2_sf
+    uint8 [E * H * I // 32] (UE8M0 scales in the L2 kernel's atom layout)."""
+    H, I, E = shape.H, shape.I, shape.E
+    _check(lib().moe_quantize_w2_fp8(
+        ctypes.byref(shape), _ptr(W2, torch.bfloat16, E * I * H, "W2"),
+        _ptr(W2_fp8, torch.uint8, E * H * I, "W2_fp8"), _ptr(W2_sf, torch.uint8, E * H * I // 32, "W2_sf"),
+        _stream(stream)))
+
+
+def moe_forward_fp8(shape: MoeShape, x_fp8, x_sf, W1_fp8, W1_sf, W2_fp8, W2_sf, topk_w, route_ws, saved, y,
+                    stream=None):
+    """moe_forward on E4M3 operands (block-scaled MMA in both GEMMs): x_fp8 /
+    x_sf from moe_quantize_fp8, W1_fp8 / W1_sf from moe_quantize_weights_fp8,
+    W2_fp8 / W2_sf from moe_quantize_w2_fp8; a is quantized between the
+    GEMMs (saved's a region then holds its E4M3 rows and scales)."""
     L = moe_workspace_layout(shape)
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     bf = torch.bfloat16
     _check(lib().moe_forward_fp8(
         ctypes.byref(shape), _ptr(x_fp8, torch.uint8, T * H, "x_fp8"), _ptr(x_sf, torch.uint8, T * H // 32, "x_sf"),
         _ptr(W1_fp8, torch.uint8, E * 2 * I * H, "W1_fp8"), _ptr(W1_sf, torch.uint8, E * 2 * I * H // 32, "W1_sf"),
-        _ptr(W2, bf, E * I * H, "W2"), _ptr(topk_w, torch.float32, T * k, "topk_w"),
+        _ptr(W2_fp8, torch.uint8, E * H * I, "W2_fp8"), _ptr(W2_sf, torch.uint8, E * H * I // 32, "W2_sf"),
+        _ptr(topk_w, torch.float32, T * k, "topk_w"),
         _ptr(route_ws, torch.uint8, L.route_bytes, "route_ws"), _ptr(saved, torch.uint8, L.saved_bytes, "saved"),
         _ptr(y, bf, T * H, "y"), _stream(stream)))
 

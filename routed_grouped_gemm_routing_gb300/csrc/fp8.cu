@@ -2,23 +2,12 @@
 // activations cast per token to FP8 with UE8M0 scale factors at a
 // granularity of 32 elements before they are dispatched, and the weights
 // transformed once for its low-precision kernel): the quantization kernels
-// of the input and of W1, and the instantiation of the L1 GEMM on E4M3
-// operands.
+// of the input and of the weights, and the instantiations of the two GEMMs
+// on E4M3 operands.
 #include "grouped_gemm_2sm.cuh"
 
 namespace moe {
 namespace {
-
-// Exponent e of the group's scale 2^e: the smallest e with 448 * 2^e >= amax
-// (448 = 0.875 * 2^9 is the largest finite E4M3 value); 0 for an all-zero
-// group; clamped to the UE8M0 range [-127, 127].
-__device__ __forceinline__ int fp8_group_exponent(float amax) {
-    if (amax == 0.0f) return 0;
-    int p;
-    const float r = frexpf(amax, &p);  // amax = r 2^p, r in [0.5, 1)
-    const int e = r <= 0.875f ? p - 9 : p - 8;
-    return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
 
 // One warp per 256 consecutive elements of x (row-major [T, H], H a multiple
 // of 32, so no 32-element group straddles two rows): lane l takes elements
@@ -81,35 +70,40 @@ __global__ void __launch_bounds__(256) dequantize_fp8_kernel(const uint8_t* __re
     }
 }
 
-// W1 [E][H][2I] bf16 to E4M3, one scale per 32 consecutive h of a column
-// (the K of the L1 GEMM), written K-major as q[E][2I][H] (gate columns, then
-// up) with the scale bytes in the L1 GEMM's atom layout: for column f (gate
-// f < I, up I + f'), group g = (f mod I) / 64 and atom row r = 64 (f >= I) +
-// (f mod I) % 64; for K group j32 = h / 32, block kb = j32 / 4 and step j =
-// j32 % 4; byte ((e (I/64) + g) (H/128) + kb) 512 + 16 (r % 32) + 4 (r / 32)
-// + j.  One block of 128 threads per 32 rows of h x 128 columns: the tile
-// comes in coalesced through shared memory and each thread quantizes one
-// column's group.  The same rule as the input (smallest power of two with
-// 448 2^e >= max|group|, round to nearest even, saturate).
-__global__ void __launch_bounds__(128) quantize_w1_fp8_kernel(const __nv_bfloat16* __restrict__ W1, int E, int H,
-                                                              int I, uint8_t* __restrict__ q,
-                                                              uint8_t* __restrict__ atoms) {
+// A weight tensor W [E][K][C] bf16 (K the contraction index of its GEMM) to
+// E4M3, one scale per 32 consecutive k of a column, written K-major as
+// q[E][C][K] with the scale bytes in the GEMM's atom layout: for column c
+// in atom group g at atom row r, K group j32 = k / 32, block kb = j32 / 4
+// and step j = j32 % 4: byte ((e G + g) (K / 128) + kb) 512 + 16 (r % 32) +
+// 4 (r / 32) + j, G groups per expert.
+//   W1 [E][H][2I] (kW1): column f (gate f < I, up I + f') has g = (f mod I)
+//     / 64, r = 64 (f >= I) + (f mod I) % 64, G = I / 64 (a CTA of the L1
+//     GEMM holds 64 gate and the matching 64 up features);
+//   W2 [E][I][H]: column h has g = h / 128, r = h % 128, G = H / 128.
+// One block of 128 threads per 32 rows of k x 128 columns: the tile comes in
+// coalesced through shared memory and each thread quantizes one column's
+// group.  The same rule as the input (smallest power of two with 448 2^e >=
+// max|group|, round to nearest even, saturate).
+template <bool kW1>
+__global__ void __launch_bounds__(128) quantize_w_fp8_kernel(const __nv_bfloat16* __restrict__ W, int E, int K, int C,
+                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ atoms) {
     __shared__ __align__(16) __nv_bfloat16 tile[32][128];
-    const int ncol = 2 * I / 128, nrow = H / 32, nkb = H / 128;
+    const int ncol = C / 128, nrow = K / 32, nkb = K / 128;
+    const int I = C / 2;  // kW1 only
     const long long ntiles = (long long)E * nrow * ncol;
     const int tid = threadIdx.x;
     for (long long ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
         const int cb = (int)(ti % ncol);
-        const int hb = (int)((ti / ncol) % nrow);
+        const int kr = (int)((ti / ncol) % nrow);
         const int e = (int)(ti / ((long long)ncol * nrow));
-        const int f0 = cb * 128, h0 = hb * 32;
+        const int c0 = cb * 128, k0 = kr * 32;
         __syncthreads();  // the previous tile has been read
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int ch = tid + 128 * i;  // 16-byte chunk: row ch / 16, columns 8 (ch % 16)
-            const int hr = ch >> 4, cc = (ch & 15) * 8;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + ((size_t)e * H + h0 + hr) * (size_t)(2 * I) + f0 + cc));
-            *reinterpret_cast<uint4*>(&tile[hr][cc]) = v;
+            const int rr = ch >> 4, cc = (ch & 15) * 8;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(W + ((size_t)e * K + k0 + rr) * (size_t)C + c0 + cc));
+            *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
         }
         __syncthreads();
         float v[32];
@@ -131,14 +125,23 @@ __global__ void __launch_bounds__(128) quantize_w1_fp8_kernel(const __nv_bfloat1
             }
             w[j] = acc;
         }
-        const int f = f0 + tid;
-        uint8_t* dst = q + ((size_t)e * (size_t)(2 * I) + f) * (size_t)H + h0;
+        const int c = c0 + tid;
+        uint8_t* dst = q + ((size_t)e * (size_t)C + c) * (size_t)K + k0;
         reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
         reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        const int fi = f < I ? f : f - I;
-        const int g = fi >> 6, r = (f < I ? 0 : 64) + (fi & 63);
-        const int kb = hb >> 2, js = hb & 3;
-        atoms[(((size_t)e * (I / 64) + g) * nkb + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5) + js] = (uint8_t)(ex + 127);
+        int g, r, G;
+        if constexpr (kW1) {
+            const int fi = c < I ? c : c - I;
+            g = fi >> 6;
+            r = (c < I ? 0 : 64) + (fi & 63);
+            G = I / 64;
+        } else {
+            g = c >> 7;
+            r = c & 127;
+            G = C / 128;
+        }
+        const int kb = kr >> 2, js = kr & 3;
+        atoms[(((size_t)e * G + g) * nkb + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5) + js] = (uint8_t)(ex + 127);
     }
 }
 
@@ -149,7 +152,16 @@ int launch_quantize_w1_fp8(const __nv_bfloat16* W1, int E, int H, int I, uint8_t
     const long long ntiles = (long long)E * (H / 32) * (2 * I / 128);
     if (ntiles <= 0) return 0;
     const long long cap = (long long)num_sms * 16;
-    quantize_w1_fp8_kernel<<<(unsigned)(ntiles < cap ? ntiles : cap), 128, 0, st>>>(W1, E, H, I, q, atoms);
+    quantize_w_fp8_kernel<true><<<(unsigned)(ntiles < cap ? ntiles : cap), 128, 0, st>>>(W1, E, H, 2 * I, q, atoms);
+    return (int)cudaGetLastError();
+}
+
+int launch_quantize_w2_fp8(const __nv_bfloat16* W2, int E, int H, int I, uint8_t* q, uint8_t* atoms, int num_sms,
+                           cudaStream_t st) {
+    const long long ntiles = (long long)E * (I / 32) * (H / 128);
+    if (ntiles <= 0) return 0;
+    const long long cap = (long long)num_sms * 16;
+    quantize_w_fp8_kernel<false><<<(unsigned)(ntiles < cap ? ntiles : cap), 128, 0, st>>>(W2, E, I, H, q, atoms);
     return (int)cudaGetLastError();
 }
 
@@ -176,6 +188,11 @@ int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t
 // L1 GEMM + SwiGLU on E4M3 weights and gathered E4M3 rows (block-scaled MMA)
 int launch_gemm_l1_fwd_mx(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
     return launch_gemm_pair<L1_FWD_MX>(a, m, max_units, st);
+}
+
+// L2 GEMM + top-k weights on E4M3 W2 and the E4M3 rows of a (block-scaled MMA)
+int launch_gemm_l2_fwd_mx(const GemmArgs& a, const GemmMaps& m, int max_units, cudaStream_t st) {
+    return launch_gemm_pair<L2_FWD_MX>(a, m, max_units, st);
 }
 
 }  // namespace moe

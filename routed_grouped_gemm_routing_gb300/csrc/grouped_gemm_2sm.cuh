@@ -327,10 +327,20 @@ template <int F>
 __host__ __device__ constexpr bool t2_is_l1() {
     return F == L1_FWD || F == L1_FWD_MX;
 }
+// the block-scaled FP8 flavours
+template <int F>
+__host__ __device__ constexpr bool t2_is_mx() {
+    return F == L1_FWD_MX || F == L2_FWD_MX;
+}
+// flavours whose B rows come by TMA and their scales by one warp's cp.async
+template <int F>
+__host__ __device__ constexpr bool t2_sf_rows() {
+    return F == L2_FWD_MX;
+}
 // K per stage: 64 bf16 or 128 E4M3 elements (128 bytes per operand row)
 template <int F>
 __host__ __device__ constexpr int t2_kblock() {
-    return F == L1_FWD_MX ? 128 : kBK;
+    return t2_is_mx<F>() ? 128 : kBK;
 }
 // TMEM of the FP8 flavour: accumulator 0 at column 0 (up to 256 columns),
 // accumulator 1 at column 256 (up to 224: a unit of more rows always takes
@@ -363,6 +373,21 @@ struct T2<L2_FWD> {
     static constexpr int kEpiHalves = 2;
     static constexpr int kInBytes = 0;
 };
+// FP8 L2 forward: E4M3 W2 (pre-quantized, K-major [E][H][I], its scale
+// atoms [E][H / 128][I / 128]) and the E4M3 rows of a with one UE8M0 scale
+// per 32 features (written by the FP8 L1's epilogue), by the block-scaled
+// MMA, 128 deep per stage like the FP8 L1.  The weights and their atom come
+// by TMA, this CTA's rows of a by TMA, and the 4 scale bytes per row and
+// stage of every row of the unit (both CTAs' MMA columns) by one warp's
+// cp.async into the rows' two atoms; the odd CTA's relay forwards that
+// warp's arrival as in the gathering flavours.
+template <>
+struct T2<L2_FWD_MX> : T2<L2_FWD> {
+    static constexpr bool kAMN = false;
+    static constexpr int kStages = 5;
+    static constexpr int kSfBytes = 512 + 1024;  // per stage: the weights' atom, the rows' two atoms
+    static constexpr int kInBytes = kStages * kSfBytes;
+};
 template <>
 struct T2<L2_DGRAD> {
     static constexpr bool kGather = true, kAMN = false;
@@ -388,8 +413,15 @@ constexpr int t2_smem_bytes() {
            kT2TailBytes;
 }
 static_assert(t2_smem_bytes<L1_FWD>() <= 232448 && t2_smem_bytes<L2_DGRAD>() <= 232448 &&
-                  t2_smem_bytes<L1_FWD_MX>() <= 232448,
+                  t2_smem_bytes<L1_FWD_MX>() <= 232448 && t2_smem_bytes<L2_FWD_MX>() <= 232448,
               "shared memory per CTA");
+// the warp of a t2_sf_rows flavour that copies the rows' scales: the first
+// gather warp after its extra producers and second epilogue warps
+template <int F>
+__host__ __device__ constexpr int t2_sf_rows_warp() {
+    return kWarpGather0 + T2<F>::kProducers - 1 + kEpiWarps * (T2<F>::kEpiHalves - 1);
+}
+static_assert(t2_sf_rows_warp<L2_FWD_MX>() < kWarpGather0 + kGatherWarps, "free gather warp for the rows' scales");
 static_assert(T2<L2_FWD>::kProducers - 1 + kEpiWarps * (T2<L2_FWD>::kEpiHalves - 1) <= kGatherWarps &&
                   T2<L1_DGRAD>::kEpiHalves == 1 && T2<L1_FWD>::kEpiHalves == 1 && T2<L2_DGRAD>::kEpiHalves == 1,
               "free gather warps");
@@ -402,7 +434,7 @@ constexpr bool t2_producers_ok() {
     return T2<F>::kProducers <= T2<F>::kStages;
 }
 static_assert(t2_producers_ok<L1_FWD>() && t2_producers_ok<L2_FWD>() && t2_producers_ok<L2_DGRAD>() &&
-                  t2_producers_ok<L1_DGRAD>() && t2_producers_ok<L1_FWD_MX>(),
+                  t2_producers_ok<L1_DGRAD>() && t2_producers_ok<L1_FWD_MX>() && t2_producers_ok<L2_FWD_MX>(),
               "round-robin producers within the ring depth");
 static_assert(T2<L1_FWD>::kProducers == 1 && T2<L2_DGRAD>::kProducers == 1 && T2<L2_FWD>::kProducers <= 1 + kGatherWarps &&
                   T2<L1_DGRAD>::kProducers <= 1 + kGatherWarps,
@@ -573,10 +605,10 @@ __device__ __forceinline__ int t2_total_units(const GemmArgs& p) {
 // on one route_ws at once, like any two calls on it).
 template <int F>
 __host__ __device__ constexpr int t2_sched_slot() {
-    return F == L1_FWD_MX ? (int)L1_FWD : F;
+    return F == L1_FWD_MX ? (int)L1_FWD : (F == L2_FWD_MX ? (int)L2_FWD : F);
 }
 static_assert(t2_sched_slot<L1_FWD>() < 4 && t2_sched_slot<L2_FWD>() < 4 && t2_sched_slot<L2_DGRAD>() < 4 &&
-                  t2_sched_slot<L1_DGRAD>() < 4 && t2_sched_slot<L1_FWD_MX>() < 4 &&
+                  t2_sched_slot<L1_DGRAD>() < 4 && t2_sched_slot<L1_FWD_MX>() < 4 && t2_sched_slot<L2_FWD_MX>() < 4 &&
                   MOE_STATUS_SCHED + 2 * 4 <= MOE_STATUS_WORDS,
               "unit-feed counters inside the status words the prologue zeroes");
 
@@ -634,9 +666,9 @@ __device__ void t2_role_sched(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
 // on this GPU, whatever the number in flight, while copies from separate
 // threads proceed side by side.
 template <int F>
-__device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const GemmArgs& p, uint32_t ring,
-                            uint32_t sA, uint32_t sB, uint32_t sIn, T2Bars bars, volatile int* abort, int rank,
-                            int pid) {
+__device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const CUtensorMap* mD, const GemmArgs& p,
+                            uint32_t ring, uint32_t sA, uint32_t sB, uint32_t sIn, T2Bars bars, volatile int* abort,
+                            int rank, int pid) {
     constexpr int NP = T2<F>::kProducers;
     const int nkb = p.K / t2_kblock<F>();
     int stage = 0;
@@ -648,7 +680,7 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
         const int nbox = (nh + 31) >> 5;   // 32-row boxes of a non-gathered B
         const int rb = t.r0 + nh * rank;
         const uint32_t tx = (uint32_t)kT2ABytes + (T2<F>::kGather ? 0u : (uint32_t)nbox * 4096u) +
-                            (F == L1_FWD_MX ? 512u : 0u);
+                            (t2_is_mx<F>() ? 512u : 0u);
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             if (NP > 1 && (int)(g % (uint32_t)NP) != pid) {
                 if (++stage == T2<F>::kStages) {
@@ -673,7 +705,16 @@ __device__ void t2_role_tma(const CUtensorMap* mA, const CUtensorMap* mB, const 
                 tma_load_4d_pair(a, mA, k0, t.f0, 0, t.e, fb);
                 tma_load_4d_pair(a + 8192, mA, k0, t.f0, 1, t.e, fb);
                 const int atom = (t.e * (p.I / 64) + t.fcol) * nkb + kb;
-                tma_load_2d_pair(sIn + (uint32_t)stage * (uint32_t)T2<L1_FWD_MX>::kSfBytes, mB, 0, 2 * atom, fb);
+                tma_load_2d_pair(sIn + (uint32_t)stage * (uint32_t)T2<F>::kSfBytes, mB, 0, 2 * atom, fb);
+            } else if constexpr (F == L2_FWD_MX) {
+                // E4M3 W2 viewed as [E][H][I] (K-major): this CTA's 128 rows
+                // of H, 128 bytes of K each; their scale atom ([E][H / 128]
+                // [I / 128], two 256-byte rows of the atoms' tensor map);
+                // this CTA's rows of a (E4M3, 128 bytes of K per row)
+                tma_load_3d_pair(a, mA, k0, t.f0, t.e, fb);
+                const int atom = (t.e * (p.H / 128) + t.fcol) * nkb + kb;
+                tma_load_2d_pair(sIn + (uint32_t)stage * (uint32_t)T2<F>::kSfBytes, mD, 0, 2 * atom, fb);
+                for (int i = 0; i < nbox; ++i) tma_load_2d_pair(b + i * 4096, mB, k0, rb + 32 * i, fb);
             } else if constexpr (t2_is_l1<F>()) {
                 // W1 viewed as [E][H][2][I]: 64 gate columns, then the same 64 up columns
                 tma_load_4d_pair(a, mA, t.f0, 0, k0, t.e, fb);
@@ -783,6 +824,36 @@ __device__ void t2_role_gather(const GemmArgs& p, uint32_t ring, uint32_t sB, ui
     }
 }
 
+// The rows' scales of a t2_sf_rows flavour (one warp in each CTA): for each
+// 128-deep stage, the 4 scale bytes of every row of the unit (both CTAs'
+// MMA columns, so both CTAs hold all of them) into the rows' two atoms:
+// unit row u at byte 512 (u / 128) + 16 (u % 32) + 4 ((u % 128) / 32) past
+// the weights' atom.  The lanes arrive on this CTA's full barrier when
+// their copies land (the odd CTA's relay passes that on).
+template <int F>
+__device__ void t2_role_sf_rows(const GemmArgs& p, uint32_t ring, uint32_t sIn, T2Bars bars, volatile int* abort,
+                                int lane, int rank) {
+    const int nkb = p.K / t2_kblock<F>();
+    const int G = p.K >> 5;  // scale bytes per row
+    int stage = 0;
+    uint32_t phase = 0;
+    T2Feed<F> feed(ring, bars, rank);
+    for (T2Unit t; feed.template next<true>(t, abort, lane);) {
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!warp_wait(bars.empty(stage), phase ^ 1u, abort)) return;
+            const uint32_t sf = sIn + (uint32_t)stage * (uint32_t)T2<F>::kSfBytes + 512u;
+            for (int us = lane; us < t.n; us += 32)
+                cp_async_4(sf + (uint32_t)(us >> 7) * 512u + (uint32_t)(us & 31) * 16u + (uint32_t)((us >> 5) & 3) * 4u,
+                           p.gsf + (size_t)(t.r0 + us) * (size_t)G + (size_t)kb * 4, 4u);
+            cp_async_arrive_noinc(bars.full(stage));
+            if (++stage == T2<F>::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
 // -------------------------------------------- MMA issuer (even CTA) / relay
 // The whole MMA warp runs this loop: it waits warp-uniformly and one elected
 // lane issues the MMAs and their commits (see warp_wait_uniform).
@@ -853,7 +924,7 @@ __device__ void t2_role_mma_mx(const GemmArgs& p, uint32_t ring, uint32_t sA, ui
             tc_fence_after();
             const uint32_t a = sA + stage * kT2ABytes;
             const uint32_t b = sB + stage * kT2BBytes;
-            const uint32_t sf = sIn + (uint32_t)stage * (uint32_t)T2<L1_FWD_MX>::kSfBytes;
+            const uint32_t sf = sIn + (uint32_t)stage * (uint32_t)T2<F>::kSfBytes;
             const uint32_t tsfa = tmem_base + kMxSfa + 4u * (nblk & 1u);
             const uint32_t tsfb = tmem_base + kMxSfb + 8u * (nblk & 1u);
             if (elect_one()) {
@@ -892,7 +963,7 @@ __device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
     for (T2Unit t; feed.template next<false>(t, abort, 0);) {
         // flavours fed by TMA alone complete the even CTA's barrier directly;
         // the relay still takes every unit from the feed
-        if constexpr (!T2<F>::kGather) continue;
+        if constexpr (!T2<F>::kGather && !t2_sf_rows<F>()) continue;
         for (int kb = 0; kb < nkb; ++kb) {
             // this CTA's gathered rows of the stage have landed (its local
             // full barrier counts only the gather threads): make them visible
@@ -906,6 +977,61 @@ __device__ void t2_role_relay(const GemmArgs& p, uint32_t ring, T2Bars bars, vol
             }
         }
     }
+}
+
+// fp8_group_exponent from the bits m of a finite, non-negative maximum:
+// amax = 1.f 2^(E - 127) = r 2^p with p = E - 126 and r = 1.f / 2, and
+// r <= 0.875 exactly when the fraction bits are at most 0x600000 (1.f <=
+// 1.75), so e = E - 135 or E - 134; subnormal maxima clamp to -127.
+__device__ __forceinline__ int fp8_group_exponent_bits(uint32_t m) {
+    if (m == 0u) return 0;
+    const int e = (int)(m >> 23) - 135 + ((m & 0x7fffffu) > 0x600000u ? 1 : 0);
+    return e < -127 ? -127 : e;
+}
+
+// The FP8 L1's activations a of one 32-row chunk (v[j] = a of row row0 + j
+// at feature col + lane) as E4M3 rows with one UE8M0 scale per row and 32
+// features, the rule of the input's quantization: scale 2^e with the
+// smallest e such that 448 2^e >= max |a| over the warp's 32 features
+// (NaN left out of the maximum), codes rounded to nearest even and
+// saturating (a times 2^-e is exact, as in ldexpf).  Lane l writes byte
+// col + l of each row (32 consecutive bytes a row per warp) and the scale
+// byte of row row0 + l.
+__device__ __forceinline__ void store_a_e4m3(const GemmArgs& p, const float (&v)[32], int row0, int col, int lane) {
+    const int I = p.I;
+    // the maximum of row j over the warp's features, kept by lane j: a
+    // transposing reduction (at offset S the lanes with bit S set keep rows
+    // i + S, the others rows i, each taking the larger with its partner),
+    // 31 shuffles for the 32 rows instead of 32 warp reductions
+    uint32_t t[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t b = __float_as_uint(fabsf(v[j]));
+        t[j] = b > 0x7f800000u ? 0u : b;
+    }
+#pragma unroll
+    for (int S = 16; S > 0; S >>= 1) {
+        const bool upper = (lane & S) != 0;
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+            const uint32_t send = upper ? t[i] : t[i + S];
+            const uint32_t keep = upper ? t[i + S] : t[i];
+            t[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, S));
+        }
+    }
+    const uint32_t mine = t[0];
+    // lane j: the exponent of row j; each row's 2^-e comes back by shuffle
+    const int ex = fp8_group_exponent_bits(mine);
+    const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
+    uint8_t* q = p.q_out + (size_t)row0 * (size_t)I + (size_t)(col + lane);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float s0 = __shfl_sync(0xffffffffu, inv, j), s1 = __shfl_sync(0xffffffffu, inv, j + 1);
+        const uint32_t two = __nv_cvt_float2_to_fp8x2(make_float2(v[j] * s0, v[j + 1] * s1), __NV_SATFINITE, __NV_E4M3);
+        q[(size_t)j * (size_t)I] = (uint8_t)(two & 0xffu);
+        q[(size_t)(j + 1) * (size_t)I] = (uint8_t)(two >> 8);
+    }
+    p.sf_out[(size_t)(row0 + lane) * (size_t)(I >> 5) + (size_t)(col >> 5)] = (uint8_t)(ex + 127);
 }
 
 // ---------------------------------------------------------------- epilogue
@@ -929,7 +1055,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
     for (T2Unit t; feed.template next<true>(t, abort, lane); ++it) {
         int acc = it & 1;
         uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        if constexpr (F == L1_FWD_MX) acc = accs.pick(t.n, &acc_phase);
+        if constexpr (t2_is_mx<F>()) acc = accs.pick(t.n, &acc_phase);
         if constexpr (F == L2_DGRAD) {
             if (lane == 0 && t.f0 + 32 * warp < p.I) {
                 // the unit's first chunk, into buffer nin & 1, whose last
@@ -1023,12 +1149,17 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                             v[j] = __fdividef(g, 1.0f + __expf(-g)) * clamp_in(u[j], p.clamp);
                         }
                     }
-                    stage_col_sw64(buf + 2048, lane, v);
+                    const bool a8 = F == L1_FWD_MX && p.q_out != nullptr;
+                    if (a8) {
+                        if (col < I) store_a_e4m3(p, v, row0, col, lane);
+                    } else {
+                        stage_col_sw64(buf + 2048, lane, v);
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && col < I) {
                         tma_store_2d(om.c0, col, row0, buf);
-                        tma_store_2d(om.c1, col, row0, buf + 2048);
+                        if (!a8) tma_store_2d(om.c1, col, row0, buf + 2048);
                         bulk_commit();
                     }
                 }
@@ -1097,7 +1228,7 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                 }
             } else {
                 // one output: o = w (a . W2) (L2 forward) or dxp = dh . W1^T (L1 dgrad)
-                if constexpr (F == L2_FWD) {
+                if constexpr (F == L2_FWD || F == L2_FWD_MX) {
                     const int sl = __ldg(p.perm + row0 + lane);
                     const float wl = sl >= 0 ? __ldg(p.topk_w + sl) : 0.0f;
 #pragma unroll
@@ -1152,7 +1283,9 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     if (threadIdx.x == 0) {
         // even CTA: its producer's arrive (both CTAs' TMA bytes), its gather
         // threads and the odd CTA's relay; odd CTA: its gather threads only
-        const uint32_t full_count = !T2<F>::kGather ? 1u : (rank == 0 ? 2u + 32u * kGatherWarps : 32u * kGatherWarps);
+        // (t2_sf_rows flavours: the scale warp's lanes in place of the gather threads)
+        const uint32_t row_thr = T2<F>::kGather ? 32u * kGatherWarps : (t2_sf_rows<F>() ? 32u : 0u);
+        const uint32_t full_count = row_thr == 0u ? 1u : (rank == 0 ? 2u + row_thr : row_thr);
         for (int s = 0; s < kT2Stages; ++s) {
             mbar_init(bars.full(s), full_count);
             mbar_init(bars.empty(s), 1);
@@ -1169,10 +1302,11 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             mbar_init(bars.ein(w, 1), 1);
         }
         // consumers of a published unit: TMA producers, MMA or relay,
-        // epilogue warps and (gathering flavours) gather warps, in both CTAs
+        // epilogue warps, (gathering flavours) gather warps and (t2_sf_rows
+        // flavours) the scale warp, in both CTAs
         const uint32_t consumers =
             2u * (1u + (uint32_t)T2<F>::kProducers + kEpiWarps * (uint32_t)T2<F>::kEpiHalves +
-                  (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u));
+                  (T2<F>::kGather ? (uint32_t)kGatherWarps : 0u) + (t2_sf_rows<F>() ? 1u : 0u));
         for (int i = 0; i < kUR; ++i) {
             mbar_init(bars.ufull(i), 1);
             mbar_init(bars.uempty(i), consumers);
@@ -1188,7 +1322,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
     if (warp == kWarpTma && lane == 0) {
         tma_prefetch_map(&mapA);
         if constexpr (!T2<F>::kGather || F == L2_DGRAD || F == L1_FWD_MX) tma_prefetch_map(&mapB);
-        if constexpr (F == L2_DGRAD) tma_prefetch_map(&mapD);
+        if constexpr (F == L2_DGRAD || F == L2_FWD_MX) tma_prefetch_map(&mapD);
         tma_prefetch_map(&mapC0);
         if constexpr (t2_is_l1<F>() || F == L2_DGRAD) tma_prefetch_map(&mapC1);
     }
@@ -1204,7 +1338,7 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         if (warp >= kWarpGather0 && warp < kWarpGather0 + T2<F>::kProducers - 1) pid = 1 + warp - kWarpGather0;
     }
     if (pid >= 0) {
-        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, p, ring, sA, sB, sIn, bars, abort, rank, pid);
+        if (lane == 0) t2_role_tma<F>(&mapA, &mapB, &mapD, p, ring, sA, sB, sIn, bars, abort, rank, pid);
     } else if (warp == kWarpSched) {
         if (lane == 0 && rank == 0) t2_role_sched<F>(p, ring, bars, abort);
     } else if (T2<F>::kEpiHalves > 1 && warp >= kWarpGather0 + T2<F>::kProducers - 1 &&
@@ -1214,12 +1348,15 @@ __global__ void __launch_bounds__(kT2Threads, 1)
         const int q = warp & 3;
         t2_role_epilogue<F>(p, OutMaps{&mapC0, &mapC1}, &mapB, &mapD, ring, bars, tmem_base,
                             sStage + q * kStageEpiBytes + 4096, sStage, sIn + q * kT2InBytes, abort, q, lane, rank, 1);
+    } else if (t2_sf_rows<F>() && warp == t2_sf_rows_warp<F>()) {
+        if constexpr (t2_sf_rows<F>()) t2_role_sf_rows<F>(p, ring, sIn, bars, abort, lane, rank);
+        cp_async_wait_all();
     } else if (warp >= kWarpGather0) {
         if constexpr (T2<F>::kGather) t2_role_gather<F>(p, ring, sB, sIn, bars, abort, warp - kWarpGather0, lane, rank);
         cp_async_wait_all();
     } else if (warp == kWarpMma) {
         if (rank == 0) {
-            if constexpr (F == L1_FWD_MX)
+            if constexpr (t2_is_mx<F>())
                 t2_role_mma_mx<F>(p, ring, sA, sB, sIn, bars, tmem_base, abort, lane);
             else
                 t2_role_mma<F>(p, ring, sA, sB, bars, tmem_base, abort, lane);

@@ -22,6 +22,7 @@ int launch_gemm_dw2(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw1_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_dw2_mg(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 int launch_gemm_l1_fwd_mx(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
+int launch_gemm_l2_fwd_mx(const GemmArgs&, const GemmMaps&, int, cudaStream_t);
 
 int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
     switch (f) {
@@ -34,6 +35,7 @@ int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaS
         case DW1_MG: return launch_gemm_dw1_mg(a, m, grid, st);
         case DW2_MG: return launch_gemm_dw2_mg(a, m, grid, st);
         case L1_FWD_MX: return launch_gemm_l1_fwd_mx(a, m, grid, st);
+        case L2_FWD_MX: return launch_gemm_l2_fwd_mx(a, m, grid, st);
         default: return (int)cudaErrorInvalidValue;
     }
 }
@@ -41,7 +43,7 @@ int launch_gemm_raw(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaS
 namespace {
 const char* const kGemmNames[] = {"gemm_l1_fwd", "gemm_l2_fwd", "gemm_l2_dgrad", "gemm_l1_dgrad",
                                   "gemm_dw1",    "gemm_dw2",    "gemm_dw1_mg",   "gemm_dw2_mg",
-                                  "gemm_l1_fwd_fp8"};
+                                  "gemm_l1_fwd_fp8", "gemm_l2_fwd_fp8"};
 }  // namespace
 
 int launch_gemm(int f, const GemmArgs& a, const GemmMaps& m, int grid, cudaStream_t st) {
@@ -232,6 +234,35 @@ int map_w1_atoms(CUtensorMap* m, const void* p, int E, int H, int I) {
                     CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
+// E4M3 W2, K-major [E][H][I] bytes: a box is 128 bytes of K of 128 rows,
+// 128-byte swizzle.
+int map_w2_fp8(CUtensorMap* m, const void* p, int E, int H, int I) {
+    cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
+    cuuint64_t str[2] = {(cuuint64_t)I, (cuuint64_t)I * H};
+    cuuint32_t box[3] = {128, 128, 1};
+    return make_map(m, p, 3, dims, str, box, "W2 (E4M3, K-major)", CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+// W2's scale atoms, E (H / 128) (I / 128) atoms of 512 bytes, as rows of 256
+// bytes: a box is one atom (2 rows), no swizzle.
+int map_w2_atoms(CUtensorMap* m, const void* p, int E, int H, int I) {
+    cuuint64_t dims[2] = {256, (cuuint64_t)E * (H / 128) * (I / 128) * 2};
+    cuuint64_t str[1] = {256};
+    cuuint32_t box[2] = {256, 2};
+    return make_map(m, p, 2, dims, str, box, "W2 scale atoms", CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+// E4M3 rows [rows][K] bytes: a box is 128 bytes of K of 32 rows, 128-byte
+// swizzle.
+int map_rows_fp8(CUtensorMap* m, const void* p, long long rows, int K, const char* what) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t str[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {128, 32};
+    return make_map(m, p, 2, dims, str, box, what, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
 struct Ctx {
     moe_layout L;
     int sms;
@@ -371,19 +402,23 @@ int moe_router_topk(const moe_shape* shape, const float* logits, int32_t* topk_i
     return MOE_OK;
 }
 
-// Body of moe_forward (x, W1 bf16) and of moe_forward_fp8 (x8 / xsf the E4M3
-// input and its scales, W1 / w1sf the E4M3 W1 and its scale atoms).
+// Body of moe_forward (x, W1, W2 bf16) and of moe_forward_fp8 (x8 / xsf the
+// E4M3 input and its scales, W1 / w1sf and W2 / w2sf the E4M3 weights and
+// their scale atoms).
 static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8, const uint8_t* xsf, const void* W1,
-                        const uint8_t* w1sf, const void* W2, const float* topk_w, void* route_ws, void* saved,
-                        void* y, void* stream, bool fp8) {
+                        const uint8_t* w1sf, const void* W2, const uint8_t* w2sf, const float* topk_w, void* route_ws,
+                        void* saved, void* y, void* stream, bool fp8) {
     Ctx c;
     int rc = prepare(shape, &c);
     if (rc) return rc;
-    if (!W1 || !W2 || !route_ws || !saved || (fp8 && !w1sf) ||
+    if (!W1 || !W2 || !route_ws || !saved || (fp8 && (!w1sf || !w2sf)) ||
         (shape->T > 0 && (!topk_w || !y || (fp8 ? (!x8 || !xsf) : !x))))
         return fail(MOE_EINVAL, "NULL pointer argument");
-    if (fp8 && shape->H % 128) return fail(MOE_EUNSUPPORTED, "the FP8 forward needs H to be a multiple of 128");
-    const void* ptrs[] = {x, x8, xsf, W1, w1sf, W2, topk_w, route_ws, saved, y};
+    if (fp8 && (shape->H % 128 || shape->I % 128))
+        return fail(MOE_EUNSUPPORTED, "the FP8 forward needs H and I to be multiples of 128");
+    if (fp8 && shape->activation_clamp > 0.0f)
+        return fail(MOE_EUNSUPPORTED, "the FP8 forward has no activation clamp");
+    const void* ptrs[] = {x, x8, xsf, W1, w1sf, W2, w2sf, topk_w, route_ws, saved, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
     if ((rc = query_device(&c, route_ws))) return rc;
@@ -396,6 +431,10 @@ static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8
     auto* a = reinterpret_cast<__nv_bfloat16*>(sv + L.a);
     auto* o = reinterpret_cast<__nv_bfloat16*>(sv + L.o);
     auto* cmask = reinterpret_cast<uint32_t*>(sv + L.cmask);
+    // FP8: a as E4M3 rows [rows_cap, I] and their scales [rows_cap, I / 32]
+    // in a's region (which holds rows_cap I bf16)
+    uint8_t* a8 = sv + L.a;
+    uint8_t* asf = sv + L.a + (size_t)L.rows_cap * (size_t)I;
     cudaStream_t st = (cudaStream_t)stream;
     // L1 grouped GEMM (gathered x) + SwiGLU -> h, a; units of 128 gate and
     // 128 up features x one row chunk of one expert
@@ -416,20 +455,31 @@ static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8
     g1.gsrc8 = x8;
     g1.gsf = xsf;
     g1.cmask = cmask;
+    if (fp8) {
+        g1.q_out = a8;
+        g1.sf_out = asf;
+    }
     int e = launch_gemm(fp8 ? L1_FWD_MX : L1_FWD, g1, m1, (int)L.tiles_cap * g1.n_tiles, st);
     if (e) return cuda_fail(e, "L1 grouped GEMM launch");
 
     // L2 grouped GEMM + routing-weight epilogue -> o; units of 256 features
     GemmMaps m2;
     memset(&m2, 0, sizeof m2);
-    if ((rc = map_3d(&m2.a, W2, E, I, H, 64, 64, "W2"))) return rc;
-    if ((rc = map_2d(&m2.b, a, L.rows_cap, I, 64, 32, "a (rows)"))) return rc;
+    if (fp8) {
+        if ((rc = map_w2_fp8(&m2.a, W2, E, H, I))) return rc;
+        if ((rc = map_rows_fp8(&m2.b, a8, L.rows_cap, I, "a (E4M3 rows)"))) return rc;
+        if ((rc = map_w2_atoms(&m2.d, w2sf, E, H, I))) return rc;
+    } else {
+        if ((rc = map_3d(&m2.a, W2, E, I, H, 64, 64, "W2"))) return rc;
+        if ((rc = map_2d(&m2.b, a, L.rows_cap, I, 64, 32, "a (rows)"))) return rc;
+    }
     if ((rc = map_2d(&m2.c0, o, L.rows_cap, H, 32, 32, "o (store)"))) return rc;
     GemmArgs g2 = base_args(shape, L, route);
     g2.K = I;
     g2.n_tiles = cdiv(H, 2 * 128);
     g2.topk_w = topk_w;
-    e = launch_gemm(L2_FWD, g2, m2, (int)L.tiles_cap * g2.n_tiles, st);
+    if (fp8) g2.gsf = asf;
+    e = launch_gemm(fp8 ? L2_FWD_MX : L2_FWD, g2, m2, (int)L.tiles_cap * g2.n_tiles, st);
     if (e) return cuda_fail(e, "L2 grouped GEMM launch");
 
     // combine: y[t] = sum_j o[inv[t, j]]
@@ -443,13 +493,15 @@ static int forward_impl(const moe_shape* shape, const void* x, const uint8_t* x8
 
 int moe_forward(const moe_shape* shape, const void* x, const void* W1, const void* W2, const float* topk_w,
                 void* route_ws, void* saved, void* y, void* stream) {
-    return forward_impl(shape, x, nullptr, nullptr, W1, nullptr, W2, topk_w, route_ws, saved, y, stream, false);
+    return forward_impl(shape, x, nullptr, nullptr, W1, nullptr, W2, nullptr, topk_w, route_ws, saved, y, stream,
+                        false);
 }
 
 int moe_forward_fp8(const moe_shape* shape, const uint8_t* x_fp8, const uint8_t* x_sf, const uint8_t* W1_fp8,
-                    const uint8_t* W1_sf, const void* W2, const float* topk_w, void* route_ws, void* saved, void* y,
-                    void* stream) {
-    return forward_impl(shape, nullptr, x_fp8, x_sf, W1_fp8, W1_sf, W2, topk_w, route_ws, saved, y, stream, true);
+                    const uint8_t* W1_sf, const uint8_t* W2_fp8, const uint8_t* W2_sf, const float* topk_w,
+                    void* route_ws, void* saved, void* y, void* stream) {
+    return forward_impl(shape, nullptr, x_fp8, x_sf, W1_fp8, W1_sf, W2_fp8, W2_sf, topk_w, route_ws, saved, y, stream,
+                        true);
 }
 
 int moe_quantize_weights_fp8(const moe_shape* shape, const void* W1, uint8_t* W1_fp8, uint8_t* W1_sf, void* stream) {
@@ -468,6 +520,26 @@ int moe_quantize_weights_fp8(const moe_shape* shape, const void* W1, uint8_t* W1
                                          W1_sf, c.sms, st);
     trace_post(st, "quantize_w1_fp8");
     if (e) return cuda_fail(e, "W1 FP8 quantization launch");
+    return MOE_OK;
+}
+
+int moe_quantize_w2_fp8(const moe_shape* shape, const void* W2, uint8_t* W2_fp8, uint8_t* W2_sf, void* stream) {
+    Ctx c;
+    int rc = prepare(shape, &c);
+    if (rc) return rc;
+    if (!W2 || !W2_fp8 || !W2_sf) return fail(MOE_EINVAL, "NULL pointer argument");
+    if (shape->H % 128 || shape->I % 128)
+        return fail(MOE_EUNSUPPORTED, "FP8 W2 needs H and I to be multiples of 128");
+    const void* ptrs[] = {W2, W2_fp8, W2_sf};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(MOE_EUNSUPPORTED, "pointers must be 16-byte aligned");
+    if ((rc = query_device(&c, W2))) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    trace_pre(st);
+    const int e = launch_quantize_w2_fp8(static_cast<const __nv_bfloat16*>(W2), shape->E, shape->H, shape->I, W2_fp8,
+                                         W2_sf, c.sms, st);
+    trace_post(st, "quantize_w2_fp8");
+    if (e) return cuda_fail(e, "W2 FP8 quantization launch");
     return MOE_OK;
 }
 

@@ -35,9 +35,13 @@ constexpr int kStageEpiBytes = 8192;  // per epilogue warp: TMA-store staging
 //   DW2       dW2[e] = aw^T . gather(dY)       (K = the expert's rows)
 //   DW1_MG, DW2_MG  the same, added in FP32 to the caller's FP32 main gradient
 //   L1_FWD_MX   L1_FWD on E4M3 weights and gathered E4M3 rows with UE8M0
-//               scales per 32 elements of K (block-scaled MMA)
+//               scales per 32 elements of K (block-scaled MMA); with q_out
+//               set, a leaves as E4M3 rows with a UE8M0 scale per 32
+//               features instead of bf16
+//   L2_FWD_MX   L2_FWD on E4M3 W2 and those E4M3 rows of a
 enum Flavour : int {
-    L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5, DW1_MG = 6, DW2_MG = 7, L1_FWD_MX = 8
+    L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5, DW1_MG = 6, DW2_MG = 7, L1_FWD_MX = 8,
+    L2_FWD_MX = 9
 };
 
 struct GemmArgs {
@@ -62,7 +66,10 @@ struct GemmArgs {
     const __nv_bfloat16* a_in;  // saved a (L2_DGRAD epilogue)
     float* outf;                // dw_part (L2_DGRAD epilogue); bf16 outputs leave by TMA store
     const uint8_t* gsrc8;       // L1_FWD_MX: E4M3 rows [T, H]
-    const uint8_t* gsf;         // L1_FWD_MX: UE8M0 scales [T, H / 32]
+    const uint8_t* gsf;         // UE8M0 scales of the E4M3 B rows: L1_FWD_MX [T, H / 32],
+                                // L2_FWD_MX [rows_cap, I / 32] (those of a)
+    uint8_t* q_out;             // L1_FWD_MX: a as E4M3 [rows_cap, I] (null: a in bf16)
+    uint8_t* sf_out;            // L1_FWD_MX: the scales of q_out [rows_cap, I / 32]
 };
 
 // Tensor maps of one grouped-GEMM launch: operands A, B (loads), up to two
@@ -95,6 +102,8 @@ int launch_router_topk(const float* logits, int T, int E, int k, int32_t* topk_i
                        cudaStream_t st);
 int launch_quantize_fp8(const __nv_bfloat16* x, long long n, uint8_t* q, uint8_t* sf, int num_sms, cudaStream_t st);
 int launch_quantize_w1_fp8(const __nv_bfloat16* W1, int E, int H, int I, uint8_t* q, uint8_t* atoms, int num_sms,
+                           cudaStream_t st);
+int launch_quantize_w2_fp8(const __nv_bfloat16* W2, int E, int H, int I, uint8_t* q, uint8_t* atoms, int num_sms,
                            cudaStream_t st);
 int launch_dequantize_fp8(const uint8_t* q, const uint8_t* sf, long long n, __nv_bfloat16* out, int num_sms,
                           cudaStream_t st);

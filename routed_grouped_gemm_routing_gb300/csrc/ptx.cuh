@@ -236,6 +236,17 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t box, int r, const uint3
         st_shared_v4(box + r * 128 + ((c ^ (r & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
 }
 
+// Exponent e of a 32-element group's scale 2^e: the smallest e with
+// 448 * 2^e >= amax (448 = 0.875 * 2^9 is the largest finite E4M3 value); 0
+// for an all-zero group; clamped to the UE8M0 range [-127, 127].
+__device__ __forceinline__ int fp8_group_exponent(float amax) {
+    if (amax == 0.0f) return 0;
+    int p;
+    const float r = frexpf(amax, &p);  // amax = r 2^p, r in [0.5, 1)
+    const int e = r <= 0.875f ? p - 9 : p - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
 // 2^(s - 127) for a UE8M0 scale byte s (s = 0: the subnormal 2^-127).
 __device__ __forceinline__ float fp8_scale(uint32_t s) {
     return s == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);

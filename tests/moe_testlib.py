@@ -177,3 +177,70 @@ def walk_tables(counts, offs, cap):
         q += pairs_e[e]
     pair_offs[-1] = q
     return pair_offs, owner
+
+
+# ------------------------------------------------------------------ FP8
+
+def unpack_w1_atoms(atoms, E, H, I):
+    """The weights' scale bytes [E, 2I, H // 32] from the kernel's atom layout
+    (include/moe_layer.h, moe_quantize_weights_fp8)."""
+    a = np.asarray(atoms).reshape(E, I // 64, H // 128, 512)
+    f = np.arange(2 * I)
+    fi = np.where(f < I, f, f - I)
+    g, r = fi // 64, np.where(f < I, 0, 64) + fi % 64
+    out = np.zeros((E, 2 * I, H // 32), np.uint8)
+    for j32 in range(H // 32):
+        out[:, :, j32] = a[:, g, j32 // 4, 16 * (r % 32) + 4 * (r // 32) + j32 % 4]
+    return out
+
+
+def dequantized_w1(q, sf_atoms, E, H, I):
+    """bf16 W1 [E, H, 2I] from its E4M3 bytes (K-major) and scale atoms (exact)."""
+    deq = oracle.dequantize_fp8(np.asarray(q).reshape(E * 2 * I, H),
+                                unpack_w1_atoms(sf_atoms, E, H, I).reshape(E * 2 * I, H // 32))
+    return torch.from_numpy(np.ascontiguousarray(deq.reshape(E, 2 * I, H).transpose(0, 2, 1)).astype(np.float32)).to(torch.bfloat16)
+
+
+def unpack_w2_atoms(atoms, E, H, I):
+    """W2's scale bytes [E, H, I // 32] from the kernel's atom layout
+    (include/moe_layer.h, moe_quantize_w2_fp8)."""
+    a = np.asarray(atoms).reshape(E, H // 128, I // 128, 512)
+    h = np.arange(H)
+    r = h % 128
+    out = np.zeros((E, H, I // 32), np.uint8)
+    for j32 in range(I // 32):
+        out[:, :, j32] = a[:, h // 128, j32 // 4, 16 * (r % 32) + 4 * (r // 32) + j32 % 4]
+    return out
+
+
+def dequantized_w2(q, sf_atoms, E, H, I):
+    """bf16 W2 [E, I, H] from its E4M3 bytes (K-major) and scale atoms (exact)."""
+    deq = oracle.dequantize_fp8(np.asarray(q).reshape(E * H, I),
+                                unpack_w2_atoms(sf_atoms, E, H, I).reshape(E * H, I // 32))
+    return torch.from_numpy(np.ascontiguousarray(deq.reshape(E, H, I).transpose(0, 2, 1)).astype(np.float32)).to(torch.bfloat16)
+
+
+def check_a8_against_oracle(a8, asf, perm, aq, asf_ref, k):
+    """The GPU's E4M3 rows of a (quantized from its FP32 a) against the
+    oracle's (quantized from its float64 a), slot by slot: the scale bytes
+    equal but where a group's maximum sits within rounding of a power of
+    two, and codes at most one step apart where the two roundings of a value
+    straddle a midpoint (a handful in a thousand); padding rows hold codes 0
+    with scale byte 127."""
+    rows = np.nonzero(perm >= 0)[0]
+    slot = perm[rows]
+    g8, gsf = a8[rows], asf[rows]
+    r8, rsf = aq.reshape(-1, aq.shape[-1])[slot], asf_ref.reshape(-1, asf_ref.shape[-1])[slot]
+    sf_bad = np.mean(gsf != rsf)
+    assert sf_bad < 2e-3, f"{sf_bad:.2e} of the scale bytes of a differ from the oracle's"
+    same_sf = np.repeat(gsf == rsf, 32, axis=1)
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    gv, rv = table[g8], table[r8]
+    diff = (gv != rv) & same_sf
+    frac = diff.sum() / max(same_sf.sum(), 1)
+    assert frac < 5e-3, f"{frac:.2e} of the E4M3 codes of a differ from the oracle's"
+    # a differing code is the neighbouring one (same sign, one step apart)
+    gi, ri = g8[diff].astype(int), r8[diff].astype(int)
+    assert np.all((gi >> 7) == (ri >> 7)) and np.all(np.abs((gi & 0x7F) - (ri & 0x7F)) <= 1)
+    pad = np.nonzero(perm < 0)[0]
+    return sf_bad, frac, pad

@@ -100,13 +100,23 @@ def test_variant_entry_points_reject_bad_arguments_before_device_use(lib):
     # FP8 entry points
     assert lib.moe_quantize_fp8(ctypes.byref(s), None, None, None, None) == B.MOE_EINVAL
     assert lib.moe_dequantize_fp8(ctypes.byref(s), None, None, None, None) == B.MOE_EINVAL
-    assert lib.moe_forward_fp8(ctypes.byref(s), *([None] * 10)) == B.MOE_EINVAL
+    assert lib.moe_forward_fp8(ctypes.byref(s), *([None] * 11)) == B.MOE_EINVAL
     assert lib.moe_quantize_weights_fp8(ctypes.byref(s), None, None, None, None) == B.MOE_EINVAL
-    # FP8 weights and the FP8 forward need H % 128 == 0 (K blocks of 128 E4M3 bytes)
-    h64 = B.shape_of(64, 192, 64, 8, 2)
+    assert lib.moe_quantize_w2_fp8(ctypes.byref(s), None, None, None, None) == B.MOE_EINVAL
+    # FP8 weights and the FP8 forward need H (W1) and H and I (W2, the
+    # forward) multiples of 128: K blocks of 128 E4M3 bytes
+    h64 = B.shape_of(64, 192, 128, 8, 2)
+    i64 = B.shape_of(64, 256, 192, 8, 2)
     assert lib.moe_quantize_weights_fp8(ctypes.byref(h64), 4096, 8192, 16384, None) == B.MOE_EUNSUPPORTED
-    assert lib.moe_forward_fp8(ctypes.byref(h64), *[4096 * (i + 1) for i in range(9)], None) == B.MOE_EUNSUPPORTED
-    assert "128" in B.moe_last_error()
+    assert lib.moe_quantize_w2_fp8(ctypes.byref(h64), 4096, 8192, 16384, None) == B.MOE_EUNSUPPORTED
+    assert lib.moe_quantize_w2_fp8(ctypes.byref(i64), 4096, 8192, 16384, None) == B.MOE_EUNSUPPORTED
+    for sh in (h64, i64):
+        assert lib.moe_forward_fp8(ctypes.byref(sh), *[4096 * (i + 1) for i in range(10)], None) == B.MOE_EUNSUPPORTED
+        assert "128" in B.moe_last_error()
+    # no activation clamp in the FP8 forward
+    cl = B.MoeShape(64, 256, 128, 8, 2, 128, 10.0)
+    assert lib.moe_forward_fp8(ctypes.byref(cl), *[4096 * (i + 1) for i in range(10)], None) == B.MOE_EUNSUPPORTED
+    assert "clamp" in B.moe_last_error()
     assert lib.moe_quantize_fp8(ctypes.byref(s), 4096, 8192 + 4, 16384, None) == B.MOE_EUNSUPPORTED
     bad = B.MoeShape(64, 96, 64, 8, 2, 128)  # H not a multiple of 64
     assert lib.moe_quantize_fp8(ctypes.byref(bad), 4096, 8192, 16384, None) == B.MOE_EUNSUPPORTED

@@ -3,19 +3,21 @@
 * moe_quantize_fp8 and moe_quantize_weights_fp8: E4M3 bytes and UE8M0 scale
   bytes bit-exact against the oracle's quantization (integer output: exact
   bar; the weights' scales read back from the kernel's atom layout);
-* moe_forward_fp8 (block-scaled tensor-core MMA on the E4M3 operands): y
-  within the comparison bar of the oracle's forward on the dequantized input
-  and dequantized W1, and of moe_forward run on them in bf16 (every product
-  of two E4M3 values and two powers of two is exact in FP32, so the two
-  differ only in how the MMAs round FP32 partial sums: bit for bit on these
-  small shapes, one bf16 step in a few elements at the V3 shape);
+* moe_quantize_w2_fp8: the same for W2;
+* moe_forward_fp8 (block-scaled tensor-core MMA on E4M3 operands in both
+  GEMMs, the SwiGLU output quantized between them): its E4M3 activations
+  against the oracle's (a few codes one step apart, where the FP32 and the
+  float64 a round to different sides of a midpoint), y within the
+  comparison bar of the L2 contraction of its own E4M3 activations (exact
+  operands) and of oracle.forward_fp8 on the dequantized operands;
 * moe_dequantize_fp8 bit-exact against the oracle's dequantization."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from moe_testlib import GpuRun, compare, f32, oracle_route, check_tables
+from moe_testlib import (GpuRun, check_a8_against_oracle, check_tables, compare, dequantized_w1, dequantized_w2,
+                         f32, oracle_route, unpack_w1_atoms, unpack_w2_atoms)
 from routed_grouped_gemm_routing_gb300 import binding as B
 from routed_grouped_gemm_routing_gb300 import build
 from routed_grouped_gemm_routing_gb300.workloads import LayerShape, bf16_bits, make_layer_inputs
@@ -66,19 +68,6 @@ def _dequantized_bf16(q, sf):
     return torch.from_numpy(deq.astype(np.float32)).to(torch.bfloat16)
 
 
-def unpack_w1_atoms(atoms, E, H, I):
-    """The weights' scale bytes [E, 2I, H // 32] from the kernel's atom layout
-    (include/moe_layer.h, moe_quantize_weights_fp8)."""
-    a = np.asarray(atoms).reshape(E, I // 64, H // 128, 512)
-    f = np.arange(2 * I)
-    fi = np.where(f < I, f, f - I)
-    g, r = fi // 64, np.where(f < I, 0, 64) + fi % 64
-    out = np.zeros((E, 2 * I, H // 32), np.uint8)
-    for j32 in range(H // 32):
-        out[:, :, j32] = a[:, g, j32 // 4, 16 * (r % 32) + 4 * (r // 32) + j32 % 4]
-    return out
-
-
 def _quantize_w1_gpu(shape, W1):
     E, H, I2 = W1.shape
     q = torch.full((E, I2, H), 0xAA, dtype=torch.uint8, device="cuda")
@@ -102,55 +91,109 @@ def test_quantize_weights_bit_exact(E, H, I, seed):
     assert bad.size == 0, f"{len(bad)} E4M3 bytes of W1 differ, first at {bad[0]}"
 
 
-def dequantized_w1(q, sf_atoms, E, H, I):
-    """bf16 W1 [E, H, 2I] from its E4M3 bytes (K-major) and scale atoms (exact)."""
-    deq = oracle.dequantize_fp8(np.asarray(q).reshape(E * 2 * I, H),
-                                unpack_w1_atoms(sf_atoms, E, H, I).reshape(E * 2 * I, H // 32))
-    return torch.from_numpy(np.ascontiguousarray(deq.reshape(E, 2 * I, H).transpose(0, 2, 1)).astype(np.float32)).to(torch.bfloat16)
+def _quantize_w2_gpu(shape, W2):
+    E, I, H = W2.shape
+    q = torch.full((E, H, I), 0xAA, dtype=torch.uint8, device="cuda")
+    sf = torch.full((E * H * I // 32,), 0xAA, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_w2_fp8(shape, W2, q, sf)
+    torch.cuda.synchronize()
+    return q, sf
 
 
-@pytest.mark.parametrize("T,H,I,E,k,seed", [
-    (300, 256, 192, 6, 3, 40),    # ragged experts, I % 128 == 64
-    (64, 128, 64, 8, 2, 41),      # one K block
-    (513, 512, 256, 16, 4, 42),
-    (1000, 256, 128, 4, 1, 43),   # ~250 rows per expert: 256-row units (accumulator 0 twice in a row) and 2-chunk experts
-])
-def test_forward_fp8_parity(T, H, I, E, k, seed):
+@pytest.mark.parametrize("E,H,I,seed", [(3, 256, 128, 60), (2, 128, 256, 61), (1, 7168, 2048, 62)])
+def test_quantize_w2_bit_exact(E, H, I, seed):
+    g = torch.Generator().manual_seed(seed)
+    W2 = (torch.randn(E, I, H, generator=g) * torch.logspace(-3, 2, H)).to(torch.bfloat16)
+    W2[0, :32, 3] = 0.0  # an all-zero group
+    s = B.shape_of(4, H, I, E, 1)
+    q, sf = _quantize_w2_gpu(s, W2.cuda())
+    rq, rsf = oracle.quantize_w2_fp8(bf16_bits(W2))
+    assert np.array_equal(unpack_w2_atoms(sf.cpu().numpy(), E, H, I), rsf), "W2 scales differ from the oracle"
+    bad = np.argwhere(q.cpu().numpy() != rq)
+    assert bad.size == 0, f"{len(bad)} E4M3 bytes of W2 differ, first at {bad[0]}"
+
+
+def fp8_layer_inputs(T, H, I, E, k, seed):
+    """The layer's inputs, quantized on the GPU, and the float64 values the
+    E4M3 operands stand for."""
     shape = LayerShape("fp8", T=T, H=H, I=I, E=E, k=k)
     inp = {n: v.cuda() for n, v in make_layer_inputs(shape, seed=seed, device="cpu").items()}
     s = B.shape_of(T, H, I, E, k)
     q, sf = _quantize_gpu(s, inp["x"])
-    wq, wsf = _quantize_w1_gpu(s, inp["W1"])
-    xd = _dequantized_bf16(q.cpu().numpy(), sf.cpu().numpy()).cuda()
-    W1d = dequantized_w1(wq.cpu().numpy(), wsf.cpu().numpy(), E, H, I).cuda()
-    # the bf16 path on the dequantized operands
-    ref_run = GpuRun(T, H, I, E, k)
-    ref_run.run(dict(inp, x=xd, W1=W1d), backward=False)
-    # the FP8 path
+    w1q, w1sf = _quantize_w1_gpu(s, inp["W1"])
+    w2q, w2sf = _quantize_w2_gpu(s, inp["W2"])
+    deq = dict(x=oracle.dequantize_fp8(q.cpu().numpy(), sf.cpu().numpy()),
+               W1=dequantized_w1(w1q.cpu().numpy(), w1sf.cpu().numpy(), E, H, I).double().numpy(),
+               W2=dequantized_w2(w2q.cpu().numpy(), w2sf.cpu().numpy(), E, H, I).double().numpy())
+    return inp, (q, sf, w1q, w1sf, w2q, w2sf), deq
+
+
+def saved_a8(run, T, I, k):
+    """The E4M3 rows of a and their scales from saved's a region
+    (include/moe_layer.h, moe_forward_fp8)."""
+    L = B.moe_workspace_layout(run.shape)
+    R = L.rows_cap
+    sv = run.saved.cpu().numpy()
+    a8 = sv[L.a: L.a + R * I].reshape(R, I)
+    asf = sv[L.a + R * I: L.a + R * I + R * (I // 32)].reshape(R, I // 32)
+    return a8, asf
+
+
+@pytest.mark.parametrize("T,H,I,E,k,seed", [
+    (300, 256, 128, 6, 3, 40),    # ragged experts
+    (64, 128, 128, 8, 2, 41),     # one K block in each GEMM
+    (513, 512, 256, 16, 4, 42),
+    (1000, 256, 128, 4, 1, 43),   # ~250 rows per expert: 256-row units (accumulator 0 twice in a row) and 2-chunk experts
+    (40, 384, 384, 64, 2, 44),    # experts of 0-5 rows
+])
+def test_forward_fp8_parity(T, H, I, E, k, seed):
+    inp, (q, sf, w1q, w1sf, w2q, w2sf), deq = fp8_layer_inputs(T, H, I, E, k, seed)
     run = GpuRun(T, H, I, E, k)
     run.poison()
     B.moe_route_prologue(run.shape, inp["topk_idx"], run.route)
-    B.moe_forward_fp8(run.shape, q, sf, wq, wsf, inp["W2"], inp["topk_w"], run.route, run.saved, run.y)
+    B.moe_forward_fp8(run.shape, q, sf, w1q, w1sf, w2q, w2sf, inp["topk_w"], run.route, run.saved, run.y)
     torch.cuda.synchronize()
-    check_tables(run, oracle_route(inp, E))
-    # a second launch on the same tables (its unit feed must start from the
+    ref_tables = oracle_route(inp, E)
+    check_tables(run, ref_tables)
+    # a second launch on the same tables (its unit feeds must start from the
     # counters the first one left at zero) gives the same bytes
     y2 = torch.full_like(run.y, float("nan"))
-    B.moe_forward_fp8(run.shape, q, sf, wq, wsf, inp["W2"], inp["topk_w"], run.route, run.saved, y2)
+    B.moe_forward_fp8(run.shape, q, sf, w1q, w1sf, w2q, w2sf, inp["topk_w"], run.route, run.saved, y2)
     torch.cuda.synchronize()
     assert torch.equal(y2, run.y), "a second FP8 forward on the same routing tables differs"
-    # every E4M3 x E4M3 x 2^k product is exact in FP32; the two MMA kinds may
-    # still round their FP32 partial sums differently over a long K
-    compare("y (fp8) vs bf16 path on the dequantized operands", f32(run.y), f32(ref_run.y))
-    print("fp8 forward equal to the bf16 path bit for bit:", bool(torch.equal(run.y, ref_run.y)))
-    y_ref = oracle.forward(bf16_bits(xd.cpu()), bf16_bits(W1d.cpu()), bf16_bits(inp["W2"].cpu()),
-                           inp["topk_idx"].cpu().numpy().astype(np.int32), inp["topk_w"].cpu().numpy())
-    compare("y (fp8) vs oracle on the dequantized operands", f32(run.y), y_ref)
-    # the quantization error of the input stays within E4M3's half step
-    xf = inp["x"].float().cpu().numpy()
-    err = np.abs(xd.float().cpu().numpy() - xf)
-    assert np.all(err <= np.abs(xf) * 2.0 ** -4 + 1e-30 + np.repeat(
-        np.ldexp(1.0, sf.cpu().numpy().astype(np.int64) - 127), 32, axis=1) * 2.0 ** -10)
+    idx = inp["topk_idx"].cpu().numpy().astype(np.int32)
+    w = inp["topk_w"].cpu().numpy()
+    y_ref, aq, asf_ref = oracle.forward_fp8(deq["x"], deq["W1"], deq["W2"], idx, w)
+    # the quantized activations between the GEMMs
+    a8, asf = saved_a8(run, T, I, k)
+    perm = ref_tables["perm"]
+    _, _, pad = check_a8_against_oracle(a8, asf, perm, aq, asf_ref, k)
+    # the L2 GEMM alone, on the GPU's own E4M3 a (exact operands): y from
+    # the dequantized rows of a, the dequantized W2 and the weights, in
+    # float64, slot by slot
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    a_deq = table[a8] * np.repeat(np.ldexp(1.0, asf.astype(np.int64) - 127), 32, axis=1)
+    y_l2 = np.zeros((T, H))
+    rows = np.nonzero(perm >= 0)[0]
+    for r in rows:
+        s_ = perm[r]
+        t, j = divmod(int(s_), k)
+        y_l2[t] += float(w[t, j]) * (a_deq[r] @ deq["W2"][idx[t, j]])
+    compare("y (fp8) vs the L2 contraction of its own E4M3 a", f32(run.y), y_l2)
+    compare("y (fp8) vs oracle.forward_fp8", f32(run.y), y_ref)
+    # padding rows of the units (inside a 32-row chunk) hold zeros
+    written = np.zeros(len(perm), bool)
+    offs, counts = ref_tables["offs"], ref_tables["counts"]
+    for e in range(E):
+        c = int(counts[e])
+        if c:
+            nsub = (c + 255) // 256
+            nb = ((c + nsub - 1) // nsub + 31) // 32 * 32
+            for jj in range(nsub):
+                lo = offs[e] + jj * nb
+                written[lo: lo + ((min(nb, c - jj * nb) + 31) // 32) * 32] = True
+    padw = pad[written[pad]]
+    assert not a8[padw].any() and np.all(asf[padw] == 127), "padding rows of a are not zero"
 
 
 @pytest.mark.parametrize("T,H", [(257, 512), (64, 7168)])

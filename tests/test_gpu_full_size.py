@@ -11,14 +11,15 @@ leave experts empty.  Properties that hold at any size cover the rest: routing
 tables bit-exact over the whole routing, every output finite, the combine
 equal to the slot-ordered FP32 sum of the weighted rows for every token, and
 zero weight gradients for experts that got no slot.  At the V3 shape the FP8
-forward is checked against the bf16 path on the dequantized operands and
+forward is checked on whole experts against the oracle's FP8 forward and
 the FP32 main-gradient backward bit for bit against the bf16 path."""
 import numpy as np
 import pytest
 import torch
 
-from moe_testlib import (GpuRun, check_tables, compare, f32, oracle_all, oracle_experts, oracle_route,
-                         oracle_tokens)
+import oracle
+from moe_testlib import (GpuRun, check_a8_against_oracle, check_tables, compare, dequantized_w1, dequantized_w2, f32,
+                         oracle_all, oracle_experts, oracle_route, oracle_tokens)
 from routed_grouped_gemm_routing_gb300 import binding as B
 from routed_grouped_gemm_routing_gb300 import build
 from routed_grouped_gemm_routing_gb300.workloads import CONFIGS, make_layer_inputs
@@ -121,29 +122,15 @@ def test_full_size_tiny_every_output():
     compare("tiny dtopk_w", f32(run.dw), ref["dtopk_w"], bf16_output=False)
 
 
-def _dequantize_w1_on_gpu(wq, atoms, E, H, I):
-    """bf16 W1 [E, H, 2I] from E4M3 bytes [E, 2I, H] and the scale atoms, one
-    expert at a time (torch's float8 conversion, exact powers of two)."""
-    f = torch.arange(2 * I, device="cuda")
-    fi = torch.where(f < I, f, f - I)
-    g, r = fi // 64, torch.where(f < I, 0, 64) + fi % 64
-    j = torch.arange(H // 32, device="cuda")
-    idx = (g[:, None] * (H // 128) + (j // 4)[None, :]) * 512 + (16 * (r % 32) + 4 * (r // 32))[:, None] + (j % 4)[None, :]
-    per = (I // 64) * (H // 128) * 512
-    out = torch.empty(E, H, 2 * I, dtype=torch.bfloat16, device="cuda")
-    for e in range(E):
-        sf = atoms[e * per:(e + 1) * per][idx].to(torch.int32) - 127
-        scale = torch.ldexp(torch.ones_like(sf, dtype=torch.float32), sf).repeat_interleave(32, dim=1)
-        out[e] = (wq[e].view(torch.float8_e4m3fn).float() * scale).t().to(torch.bfloat16)
-    return out
-
-
 def test_full_size_fp8_forward_and_main_grad():
-    """The V3-shaped layer through the two variants, against the bf16 path on
-    the same GPU: the FP8 forward (E4M3 input and W1, block-scaled MMA)
-    within the comparison bar of the bf16 forward on the dequantized input
-    and W1, and the FP32 main-gradient backward from zero main gradients
-    rounding to the bf16 weight gradients bit for bit."""
+    """The V3-shaped layer through the two variants.  The FP8 forward (E4M3
+    input and weights, block-scaled MMA, a quantized between the GEMMs) on
+    whole experts (the most and the least loaded, one random): the E4M3
+    rows of a against oracle.forward_fp8 on a sub-problem of that expert's
+    slots and its dequantized weights, and the weighted L2 rows o within the
+    comparison bar of the oracle's slot outputs; y finite.  The FP32
+    main-gradient backward from zero main gradients rounds to the bf16
+    weight gradients bit for bit."""
     shape = CONFIGS["v3"]
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     inp = make_layer_inputs(shape, seed=5, device="cuda")
@@ -151,19 +138,49 @@ def test_full_size_fp8_forward_and_main_grad():
     q = torch.empty(T, H, dtype=torch.uint8, device="cuda")
     sf = torch.empty(T, H // 32, dtype=torch.uint8, device="cuda")
     B.moe_quantize_fp8(s, inp["x"], q, sf)
-    xd = torch.empty_like(inp["x"])
-    B.moe_dequantize_fp8(s, q, sf, xd)
-    wq = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
-    wsf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device="cuda")
-    B.moe_quantize_weights_fp8(s, inp["W1"], wq, wsf)
-    W1d = _dequantize_w1_on_gpu(wq, wsf, E, H, I)
-    ref = GpuRun(T, H, I, E, k)
-    ref.run(dict(inp, x=xd, W1=W1d), backward=False)
-    y8 = torch.empty_like(ref.y)
-    B.moe_forward_fp8(ref.shape, q, sf, wq, wsf, inp["W2"], inp["topk_w"], ref.route, ref.saved, y8)
+    w1q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
+    w1sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_weights_fp8(s, inp["W1"], w1q, w1sf)
+    w2q = torch.empty(E, H, I, dtype=torch.uint8, device="cuda")
+    w2sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_w2_fp8(s, inp["W2"], w2q, w2sf)
+    run8 = GpuRun(T, H, I, E, k)
+    B.moe_route_prologue(run8.shape, inp["topk_idx"], run8.route)
+    B.moe_forward_fp8(run8.shape, q, sf, w1q, w1sf, w2q, w2sf, inp["topk_w"], run8.route, run8.saved, run8.y)
     torch.cuda.synchronize()
-    compare("v3 y (fp8) vs bf16 path on the dequantized operands", f32(y8), f32(ref.y))
-    del W1d, wq, wsf, y8
+    assert torch.isfinite(run8.y).all()
+    tab = run8.tables()
+    counts, offs, perm = tab["counts"], tab["offs"], tab["perm"]
+    L = B.moe_workspace_layout(run8.shape)
+    sv = run8.saved
+    R = L.rows_cap
+    a8 = sv[L.a: L.a + R * I].view(R, I)
+    asf = sv[L.a + R * I: L.a + R * I + R * (I // 32)].view(R, I // 32)
+    o = sv[L.o: L.o + R * H * 2].view(torch.bfloat16).view(R, H)
+    xq, xsf = q.cpu().numpy(), sf.cpu().numpy()
+    w = inp["topk_w"].cpu().numpy()
+    rng = np.random.default_rng(7)
+    order = np.argsort(counts, kind="stable")
+    picks = [int(order[-1]), int(order[0]), int(rng.integers(E))]
+    per1, per2 = 2 * I * H // 32, H * I // 32
+    for e in dict.fromkeys(picks):
+        c = int(counts[e])
+        rows = np.arange(offs[e], offs[e] + c)
+        slots = perm[rows]
+        toks, js = slots // k, slots % k
+        x_sub = oracle.dequantize_fp8(xq[toks], xsf[toks])
+        W1_sub = dequantized_w1(w1q[e:e + 1].cpu().numpy(), w1sf[e * per1:(e + 1) * per1].cpu().numpy(), 1, H,
+                                I).double().numpy()
+        W2_sub = dequantized_w2(w2q[e:e + 1].cpu().numpy(), w2sf[e * per2:(e + 1) * per2].cpu().numpy(), 1, H,
+                                I).double().numpy()
+        y_sub, aq, asf_ref = oracle.forward_fp8(x_sub, W1_sub, W2_sub, np.zeros((c, 1), np.int32),
+                                                w[toks, js].reshape(c, 1))
+        trows = torch.from_numpy(rows).cuda()
+        sf_bad, frac, _ = check_a8_against_oracle(a8[trows].cpu().numpy(), asf[trows].cpu().numpy(),
+                                                  np.arange(c), aq, asf_ref, 1)
+        print(f"v3 fp8 expert {e} ({c} rows): scale bytes differing {sf_bad:.1e}, codes differing {frac:.1e}")
+        compare(f"v3 fp8 o rows of expert {e} ({c} rows)", f32(o[trows]), y_sub)
+    del w1q, w1sf, w2q, w2sf, run8
     # FP32 main gradients from the bf16 forward's saved activations
     run = GpuRun(T, H, I, E, k)
     run.run(inp)
