@@ -11,7 +11,8 @@
 // token operand (x for dW1, dY for dW2) for all of the expert's routed rows
 // ONCE into a shared-memory slab (up to S 64-row K blocks), and then
 // streams the other operand (dh for dW1, aw for dW2) by TMA, 128 of its
-// features per CTA at a time, through an 11 - S stage ring.  For every streamed
+// features per CTA at a time, through a ring of 6 (S = 5) or 5 (S = 7)
+// stages.  For every streamed
 // tile t the pair issues M=256 x N=256 MMAs over the expert's rows:
 //   dW1: A = slab (M = H features), B = dh (N = 2I features)
 //   dW2: A = aw   (M = I features), B = slab (N = H features)
@@ -44,26 +45,44 @@
 
 namespace moe {
 
-// Eleven 16 KiB operand blocks per CTA, S of them for the slab (S 64-row K
-// blocks: 64 S routed rows) and 11 - S for the streamed ring.  S = 5 (320
-// rows, 6 ring stages) unless the shape's mean rows per expert, T k / E,
-// exceed 320; then S = 7 (448 rows, 4 stages), so that such experts fit the
-// slab (a 4-stage ring starves the 256-row experts of the V3-shaped layer,
-// measured: dW1 3.2 -> 4.0 ms; 7 slab blocks cut the V2-Lite-shaped
-// layer's dW1 0.30 -> 0.24 ms and dW2 0.17 -> 0.12 ms).
+// Eleven 16 KiB operand blocks per CTA (twelve with S = 7, below), S of
+// them for the slab (S 64-row K blocks: 64 S routed rows) and the rest for
+// the streamed ring.  S = 5 (320 rows, 6 ring stages) unless the shape's
+// mean rows per expert, T k / E, exceed 320; then S = 7 (448 rows, 5
+// stages), so that such experts fit the slab (a 4-stage ring starves the
+// 256-row experts of the V3-shaped layer, measured: dW1 3.2 -> 4.0 ms; 7
+// slab blocks cut the V2-Lite-shaped layer's dW1 0.30 -> 0.24 ms and dW2
+// 0.17 -> 0.12 ms).
 constexpr int kWBlocks = 11;
 constexpr int kWBlockBytes = 128 * kBK * 2;  // 16 KiB: 128 features x 64 rows, MN-major, 128B swizzle
 constexpr int kWSlabSmall = 5, kWSlabLarge = 7;
 constexpr int kWTailBytes = 512;
-static_assert(8 * (3 * kWSlabLarge + 2 * (kWBlocks - kWSlabLarge) + 5) + 8 <= kWTailBytes &&
+static_assert(8 * (3 * kWSlabLarge + 2 * (kWBlocks + 1 - kWSlabLarge) + 5) + 8 <= kWTailBytes &&
                   8 * (3 * kWSlabSmall + 2 * (kWBlocks - kWSlabSmall) + 5) + 8 <= kWTailBytes,
               "barrier area");
 constexpr int kWSmemBytes = 1024 + kWBlocks * kWBlockBytes + kEpiWarps * kStageEpiBytes + kWTailBytes;
 static_assert(kWSmemBytes <= 232448, "shared memory per CTA");
+// With the 7-block slab the ring gets a fifth stage in place of the second
+// 4 KiB store buffer of each epilogue warp (the same shared memory): the
+// streamed operand's latency, not the epilogue, held the MMAs back there
+// (V2-Lite-shaped layer, per-role cycle counters: the MMA warp waited 35 %
+// of its time for streamed blocks with four stages; dW1 0.240 -> 0.226 ms).
+template <int S>
+__host__ __device__ constexpr int w_blocks() {
+    return S == kWSlabLarge ? kWBlocks + 1 : kWBlocks;
+}
+template <int S>
+__host__ __device__ constexpr int w_store_bufs() {  // 4 KiB store buffers per epilogue warp
+    return S == kWSlabLarge ? 1 : 2;
+}
+static_assert(1024 + w_blocks<kWSlabLarge>() * kWBlockBytes + kEpiWarps * 4096 * w_store_bufs<kWSlabLarge>() +
+                      kWTailBytes == kWSmemBytes &&
+                  4096 * w_store_bufs<kWSlabSmall>() == kStageEpiBytes,
+              "both slab sizes lay out the same shared memory");
 
 template <int S>
 struct WBars {
-    static constexpr int kSlab = S, kStages = kWBlocks - S;
+    static constexpr int kSlab = S, kStages = w_blocks<S>() - S;
     static constexpr int kNum = 3 * kSlab + 2 * kStages + 5;  // barriers
     uint32_t base;
     __device__ __forceinline__ uint32_t slab_full(int i) const { return base + 8u * i; }
@@ -485,8 +504,13 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars<
                     uint32_t r0[32];
                     tmem_ld32_nowait(tacc + 32 * c32, r0);
                     tmem_ld_wait();
-                    const uint32_t buf = stage + (nstore & 1u) * 4096u;
-                    if (lane == 0) bulk_wait_read<1>();
+                    const uint32_t buf = stage + (nstore % (uint32_t)w_store_bufs<S>()) * 4096u;
+                    if (lane == 0) {
+                        if constexpr (w_store_bufs<S>() == 1)
+                            bulk_wait_read<0>();
+                        else
+                            bulk_wait_read<1>();
+                    }
                     __syncwarp();
                     stage_row_sw128(buf, lane, r0);
                     fence_proxy_async_smem();
@@ -519,8 +543,13 @@ __device__ void w_role_epilogue(const GemmArgs& p, const CUtensorMap* mC, WBars<
                             pk[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
                         }
                     }
-                    const uint32_t buf = stage + (nstore & 1u) * 4096u;
-                    if (lane == 0) bulk_wait_read<1>();
+                    const uint32_t buf = stage + (nstore % (uint32_t)w_store_bufs<S>()) * 4096u;
+                    if (lane == 0) {
+                        if constexpr (w_store_bufs<S>() == 1)
+                            bulk_wait_read<0>();
+                        else
+                            bulk_wait_read<1>();
+                    }
                     __syncwarp();
                     stage_row_sw128(buf, lane, pk);
                     fence_proxy_async_smem();
@@ -553,9 +582,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t sL = base;                               // slab: S blocks
-    const uint32_t sS = sL + S * kWBlockBytes;              // streamed ring: 11 - S blocks
-    const uint32_t sE = base + kWBlocks * kWBlockBytes;     // epilogue staging
-    const uint32_t bar_base = sE + kEpiWarps * kStageEpiBytes;
+    const uint32_t sS = sL + S * kWBlockBytes;              // streamed ring: w_blocks<S>() - S blocks
+    const uint32_t sE = base + w_blocks<S>() * kWBlockBytes;     // epilogue staging
+    const uint32_t bar_base = sE + kEpiWarps * 4096u * (uint32_t)w_store_bufs<S>();
     uint8_t* tail = base_ptr + (bar_base - base);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tail + 8 * WBars<S>::kNum);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -635,7 +664,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             w_role_relay<S>(p, bars, abort);
         }
     } else {
-        w_role_epilogue<F, kMG, S>(p, &mapC, bars, tmem_base, sE + warp * kStageEpiBytes, abort, warp, lane, rank);
+        w_role_epilogue<F, kMG, S>(p, &mapC, bars, tmem_base, sE + warp * 4096u * (uint32_t)w_store_bufs<S>(), abort,
+                                   warp, lane, rank);
     }
     if (warp == kWarpTma && lane == 0 && *abort) {
         const uint64_t t0 = global_timer_ns();
