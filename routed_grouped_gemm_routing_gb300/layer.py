@@ -117,6 +117,59 @@ def moe_layer(x, W1, W2, topk_idx, topk_weights, workspace: MoEWorkspace | None 
                                  bool(accumulate_main_grad))
 
 
+class FP8Experts:
+    """The layer's expert weights in FP8 for inference (DeepGEMM Mega-MoE
+    article, "Code Example: Fused Overlap Path": the weights are transformed
+    once, the activations cast per token before each call).
+
+    Built once from bf16 W1 [E,H,2I] and W2 [E,I,H] (moe_quantize_weights_fp8,
+    moe_quantize_w2_fp8); ``forward`` casts x (moe_quantize_fp8), builds the
+    routing tables and runs moe_forward_fp8.  Needs H and I multiples of 128.
+    Not differentiable."""
+
+    def __init__(self, W1, W2):
+        E, H, I2 = W1.shape
+        I = I2 // 2
+        if I2 % 2 or tuple(W2.shape) != (E, I, H):
+            raise ValueError("expected W1 [E,H,2I], W2 [E,I,H]")
+        if H % 128 or I % 128:
+            raise ValueError("the FP8 path needs H and I to be multiples of 128")
+        self.E, self.H, self.I = E, H, I
+        dev = W1.device
+        s = B.shape_of(1, H, I, E, 1)
+        self.W1_fp8 = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        self.W1_sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
+        self.W2_fp8 = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        self.W2_sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device=dev)
+        with torch.cuda.device(dev):
+            B.moe_quantize_weights_fp8(s, W1.contiguous(), self.W1_fp8, self.W1_sf)
+            B.moe_quantize_w2_fp8(s, W2.contiguous(), self.W2_fp8, self.W2_sf)
+
+    def forward(self, x, topk_idx, topk_weights, workspace: MoEWorkspace | None = None):
+        """y bf16 [T,H] of the FP8 layer for x bf16 [T,H] and the routing."""
+        T, H = x.shape
+        k = topk_idx.shape[1]
+        if H != self.H:
+            raise ValueError("x's hidden size differs from the weights'")
+        ws = workspace
+        if ws is None or (ws.shape.T, ws.shape.H, ws.shape.I, ws.shape.E, ws.shape.k) != (T, H, self.I, self.E, k):
+            ws = MoEWorkspace(T, H, self.I, self.E, k, device=x.device)
+        ws.generation += 1  # the FP8 forward overwrites the saved activations
+        idx = (topk_idx if topk_idx.dtype == torch.int32 else topk_idx.to(torch.int32)).contiguous()
+        w = topk_weights.to(torch.float32).contiguous()
+        xq = torch.empty(T, H, dtype=torch.uint8, device=x.device)
+        xsf = torch.empty(T, H // 32, dtype=torch.uint8, device=x.device)
+        y = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+        with torch.cuda.device(x.device):
+            B.moe_quantize_fp8(ws.shape, x.contiguous(), xq, xsf)
+            B.moe_route_prologue(ws.shape, idx, ws.route)
+            B.moe_forward_fp8(ws.shape, xq, xsf, self.W1_fp8, self.W1_sf, self.W2_fp8, self.W2_sf, w, ws.route,
+                              ws.saved, y)
+        return y
+
+    __call__ = forward
+
+
 def train_step_from_host(x_h, topk_idx_h, topk_w_h, dY_h, W1, W2, ws: MoEWorkspace, outs: dict):
     """One forward+backward of the layer fed from pinned HOST buffers.
 

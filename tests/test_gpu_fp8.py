@@ -206,3 +206,23 @@ def test_dequantize_bit_exact(T, H):
     torch.cuda.synchronize()
     ref = _dequantized_bf16(q.cpu().numpy(), sf.cpu().numpy())
     assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_fp8_experts_wrapper_matches_abi():
+    """layer.FP8Experts (weights quantized once, x cast per call) gives the
+    bytes of the ABI sequence it marshals, with and without a workspace."""
+    from routed_grouped_gemm_routing_gb300.layer import FP8Experts, MoEWorkspace
+    T, H, I, E, k = 300, 256, 128, 6, 3
+    inp, (q, sf, w1q, w1sf, w2q, w2sf), _ = fp8_layer_inputs(T, H, I, E, k, seed=45)
+    run = GpuRun(T, H, I, E, k)
+    B.moe_route_prologue(run.shape, inp["topk_idx"], run.route)
+    B.moe_forward_fp8(run.shape, q, sf, w1q, w1sf, w2q, w2sf, inp["topk_w"], run.route, run.saved, run.y)
+    experts = FP8Experts(inp["W1"], inp["W2"])
+    assert torch.equal(experts.W1_fp8, w1q) and torch.equal(experts.W2_sf, w2sf)
+    y = experts(inp["x"], inp["topk_idx"].long(), inp["topk_w"])
+    ws = MoEWorkspace(T, H, I, E, k)
+    y2 = experts(inp["x"], inp["topk_idx"], inp["topk_w"], workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y, run.y) and torch.equal(y2, run.y)
+    with pytest.raises(ValueError):
+        FP8Experts(inp["W1"][:, :, :192].contiguous(), inp["W2"][:, :96].contiguous())
