@@ -457,6 +457,94 @@ class LayerBench:
         }
 
 
+def fp8_forward_times(shape, inp, ws, y, dev, peaks):
+    """The FP8 forward (E4M3 input per token, E4M3 W1 and W2 per column, UE8M0
+    scales per 32 elements of K, block-scaled MMA in both GEMMs, a quantized
+    between them), timed beside the bf16 forward on the same inputs: an
+    inference variant, not the layer step.  The weights are quantized once
+    beforehand (a weight transform), timed on their own.  None when H or I is
+    not a multiple of 128."""
+    import torch
+
+    from routed_grouped_gemm_routing_gb300 import binding as B
+
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    if H % 128 or I % 128:
+        return None
+    xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    xsf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    w1q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+    w1sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
+    w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+    w2sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device=dev)
+
+    def quantize_weights():
+        B.moe_quantize_weights_fp8(ws.shape, inp["W1"], w1q, w1sf)
+        B.moe_quantize_w2_fp8(ws.shape, inp["W2"], w2q, w2sf)
+
+    quantize_weights()
+    torch.cuda.synchronize()
+    wtrace = B.KernelTrace(max_launches=2 * 3)
+    with wtrace:
+        for _ in range(3):
+            quantize_weights()
+    torch.cuda.synchronize()
+    wq = {}
+    for kn, d in wtrace.durations_ms():
+        wq.setdefault(kn, []).append(d)
+    wq_ms = {kn: statistics.median(v) for kn, v in wq.items()}
+
+    def fwd_fp8():
+        B.moe_quantize_fp8(ws.shape, inp["x"], xq, xsf)
+        B.moe_forward_fp8(ws.shape, xq, xsf, w1q, w1sf, w2q, w2sf, inp["topk_w"], ws.route, ws.saved, y)
+
+    def fwd_bf16():
+        B.moe_forward(ws.shape, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
+
+    B.moe_route_prologue(ws.shape, inp["topk_idx"], ws.route)
+    per = {}
+    for name, fn in (("fp8", fwd_fp8), ("bf16", fwd_bf16)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ftrace = B.KernelTrace(max_launches=8 * 10)
+        with ftrace:
+            for _ in range(10):
+                fn()
+        torch.cuda.synchronize()
+        kk = {}
+        for kn, d in ftrace.durations_ms():
+            kk.setdefault(kn, []).append(d)
+        per[name] = {kn: statistics.median(v) for kn, v in kk.items()}
+    tk = T * k
+    q_bytes = T * H * 2 + T * H + T * H // 32
+    l1_ms = per["fp8"]["gemm_l1_fwd_fp8"]
+    l2_ms = per["fp8"]["gemm_l2_fwd_fp8"]
+    # W1 and its scales, x and its scales, h (bf16), a (E4M3) and its scales
+    l1_bytes = E * 2 * I * H * (1 + 1 / 32) + T * H * (1 + 1 / 32) + 2.0 * tk * 2 * I + tk * I * (1 + 1 / 32)
+    # W2 and its scales, a and its scales, o (bf16)
+    l2_bytes = E * H * I * (1 + 1 / 32) + tk * I * (1 + 1 / 32) + 2.0 * tk * H
+    hbm = float(peaks["hbm_gbs"])
+    out = {"forward_ms": sum(per["fp8"].values()), "bf16_forward_ms": sum(per["bf16"].values()),
+           "kernels_ms": per["fp8"], "bf16_kernels_ms": per["bf16"],
+           "quantize_gbs": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9,
+           "quantize_frac_of_hbm": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9 / hbm,
+           "l1_fp8_gbs": l1_bytes / (l1_ms / 1e3) / 1e9,
+           "l1_fp8_frac_of_hbm": l1_bytes / (l1_ms / 1e3) / 1e9 / hbm,
+           "l1_fp8_tflops": 4.0 * H * I * tk / (l1_ms / 1e3) / 1e12,
+           "l2_fp8_gbs": l2_bytes / (l2_ms / 1e3) / 1e9,
+           "l2_fp8_frac_of_hbm": l2_bytes / (l2_ms / 1e3) / 1e9 / hbm,
+           "l2_fp8_tflops": 2.0 * H * I * tk / (l2_ms / 1e3) / 1e12,
+           "forward_tflops": 6.0 * H * I * tk / (sum(per["fp8"].values()) / 1e3) / 1e12,
+           "weight_quantize_ms": wq_ms,
+           "note": "median of 10 runs of moe_quantize_fp8 + moe_forward_fp8 (and of moe_forward) on the "
+                   "workload; both GEMMs multiply E4M3 operands (W1 and W2 quantized once beforehand, "
+                   "weight_quantize_ms) with block-scaled tcgen05.mma, a quantized to E4M3 in the L1 "
+                   "epilogue; not part of the step"}
+    del w1q, w1sf, w2q, w2sf
+    return out
+
+
 def run_other_configs(args, dev, world, rank, peaks, peaks_src):
     """Every other BASELINE workload on this GPU, one after another; the
     V3-shaped headline's buffers are already freed."""
@@ -479,6 +567,10 @@ def run_other_configs(args, dev, world, rank, peaks, peaks_src):
         r["expert_load"] = {"min": int(counts.min()), "mean": float(counts.mean()), "max": int(counts.max()),
                             "below_block_m": int(((counts > 0) & (counts < 128)).sum()),
                             "empty": int((counts == 0).sum()), "top5": sorted(counts.tolist())[-5:][::-1]}
+        # the FP8 forward once per shape: on the forward-only line when there is one
+        fwd_only = {c for _, c, b, _, _, _ in OTHER_CONFIGS if not b}
+        if not args.no_fp8 and (not backward or cname not in fwd_only):
+            r["fp8_forward"] = fp8_forward_times(shape, lb.inp, lb.ws, lb.y, dev, peaks)
         if rank == 0 and world == 1 and not args.no_cpu_baseline and backward:
             whole = n_exp == 0
             r["cpu_baseline"] = time_oracle(shape, lb.inp, n_tok=shape.T if whole else n_tok,
@@ -614,84 +706,9 @@ def run_ours(args):
                   "note": "median of 20 runs of moe_router_topk (router kernel + routing prologue) on the "
                           "workload's logits; not part of the layer step"}
 
-    # the FP8 forward (E4M3 input per token, E4M3 W1 and W2 per column, UE8M0
-    # scales per 32 elements of K, block-scaled MMA in both GEMMs, a
-    # quantized between them), timed beside the bf16 forward: an inference
-    # variant, not the layer step.  The weights are quantized once
-    # beforehand (a weight transform), timed on their own.
     fp8 = None
-    if not args.no_fp8 and H % 128 == 0 and I % 128 == 0:
-        xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
-        xsf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
-        w1q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
-        w1sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device=dev)
-        w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
-        w2sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device=dev)
-
-        def quantize_weights():
-            B.moe_quantize_weights_fp8(ws.shape, inp["W1"], w1q, w1sf)
-            B.moe_quantize_w2_fp8(ws.shape, inp["W2"], w2q, w2sf)
-
-        quantize_weights()
-        torch.cuda.synchronize()
-        wtrace = B.KernelTrace(max_launches=2 * 3)
-        with wtrace:
-            for _ in range(3):
-                quantize_weights()
-        torch.cuda.synchronize()
-        wq = {}
-        for kn, d in wtrace.durations_ms():
-            wq.setdefault(kn, []).append(d)
-        wq_ms = {kn: statistics.median(v) for kn, v in wq.items()}
-
-        def fwd_fp8():
-            B.moe_quantize_fp8(ws.shape, inp["x"], xq, xsf)
-            B.moe_forward_fp8(ws.shape, xq, xsf, w1q, w1sf, w2q, w2sf, inp["topk_w"], ws.route, ws.saved, y)
-
-        def fwd_bf16():
-            B.moe_forward(ws.shape, inp["x"], inp["W1"], inp["W2"], inp["topk_w"], ws.route, ws.saved, y)
-
-        B.moe_route_prologue(ws.shape, inp["topk_idx"], ws.route)
-        per = {}
-        for name, fn in (("fp8", fwd_fp8), ("bf16", fwd_bf16)):
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            ftrace = B.KernelTrace(max_launches=8 * 10)
-            with ftrace:
-                for _ in range(10):
-                    fn()
-            torch.cuda.synchronize()
-            kk = {}
-            for kn, d in ftrace.durations_ms():
-                kk.setdefault(kn, []).append(d)
-            per[name] = {kn: statistics.median(v) for kn, v in kk.items()}
-        tk = T * k
-        q_bytes = T * H * 2 + T * H + T * H // 32
-        l1_ms = per["fp8"]["gemm_l1_fwd_fp8"]
-        l2_ms = per["fp8"]["gemm_l2_fwd_fp8"]
-        # W1 and its scales, x and its scales, h (bf16), a (E4M3) and its scales
-        l1_bytes = E * 2 * I * H * (1 + 1 / 32) + T * H * (1 + 1 / 32) + 2.0 * tk * 2 * I + tk * I * (1 + 1 / 32)
-        # W2 and its scales, a and its scales, o (bf16)
-        l2_bytes = E * H * I * (1 + 1 / 32) + tk * I * (1 + 1 / 32) + 2.0 * tk * H
-        hbm = float(peaks["hbm_gbs"])
-        fp8 = {"forward_ms": sum(per["fp8"].values()), "bf16_forward_ms": sum(per["bf16"].values()),
-               "kernels_ms": per["fp8"], "bf16_kernels_ms": per["bf16"],
-               "quantize_gbs": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9,
-               "quantize_frac_of_hbm": q_bytes / (per["fp8"]["quantize_fp8"] / 1e3) / 1e9 / hbm,
-               "l1_fp8_gbs": l1_bytes / (l1_ms / 1e3) / 1e9,
-               "l1_fp8_frac_of_hbm": l1_bytes / (l1_ms / 1e3) / 1e9 / hbm,
-               "l1_fp8_tflops": 4.0 * H * I * tk / (l1_ms / 1e3) / 1e12,
-               "l2_fp8_gbs": l2_bytes / (l2_ms / 1e3) / 1e9,
-               "l2_fp8_frac_of_hbm": l2_bytes / (l2_ms / 1e3) / 1e9 / hbm,
-               "l2_fp8_tflops": 2.0 * H * I * tk / (l2_ms / 1e3) / 1e12,
-               "forward_tflops": 6.0 * H * I * tk / (sum(per["fp8"].values()) / 1e3) / 1e12,
-               "weight_quantize_ms": wq_ms,
-               "note": "median of 10 runs of moe_quantize_fp8 + moe_forward_fp8 (and of moe_forward) on the "
-                       "workload; both GEMMs multiply E4M3 operands (W1 and W2 quantized once beforehand, "
-                       "weight_quantize_ms) with block-scaled tcgen05.mma, a quantized to E4M3 in the L1 "
-                       "epilogue; not part of the step"}
-        del w1q, w1sf, w2q, w2sf
+    if not args.no_fp8:
+        fp8 = fp8_forward_times(shape, inp, ws, y, dev, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
