@@ -58,7 +58,7 @@ constexpr int kT2ABytes = 128 * kBK * 2;  // this CTA's 128 features x 64 of K
 constexpr int kT2BBytes = 128 * kBK * 2;  // up to 128 routed rows x 64 of K
 constexpr int kT2InBytes = 3 * 2048;      // L2 dgrad epilogue inputs per warp: h gate, h up, a boxes
 constexpr int kUR = 4;                    // slots of the unit ring
-constexpr int kT2NumBars = 2 * kT2Stages + 9 + 2 * kEpiWarps + 2 * kUR + 1;
+constexpr int kT2NumBars = 2 * kT2Stages + 9 + 2 * kEpiWarps + 2 * kUR + 1 + 4;
 constexpr int kT2TailBytes = 512;         // barriers, TMEM address, abort flag, unit ring
 constexpr int kT2RingOff = (8 * kT2NumBars + 8 + 15) & ~15;
 static_assert(kT2RingOff + 16 * kUR <= kT2TailBytes, "barrier area");
@@ -87,6 +87,13 @@ struct T2Bars {
     // L2 dgrad epilogue: the input boxes of warp w's buffer b have landed
     __device__ __forceinline__ uint32_t ein(int w, uint32_t b) const {
         return b == 0 ? ein(w) : base + 8u * (2 * kT2Stages + 9 + kEpiWarps + 2 * kUR + 1 + w);
+    }
+    // FP8 L1 epilogue: gate values handed from warp i to warp 2 + i
+    __device__ __forceinline__ uint32_t gfull(int i) const {
+        return base + 8u * (2 * kT2Stages + 9 + 2 * kEpiWarps + 2 * kUR + 1 + i);
+    }
+    __device__ __forceinline__ uint32_t gempty(int i) const {
+        return base + 8u * (2 * kT2Stages + 9 + 2 * kEpiWarps + 2 * kUR + 3 + i);
     }
 };
 
@@ -989,28 +996,30 @@ __device__ __forceinline__ int fp8_group_exponent_bits(uint32_t m) {
     return e < -127 ? -127 : e;
 }
 
-// The FP8 L1's activations a of one 32-row chunk (v[j] = a of row row0 + j
-// at feature col + lane) as E4M3 rows with one UE8M0 scale per row and 32
-// features, the rule of the input's quantization: scale 2^e with the
-// smallest e such that 448 2^e >= max |a| over the warp's 32 features
+// The FP8 L1's activations a of R (16 or 32) rows of one chunk (v[j] = a of
+// row row0 + j at feature col + lane) as E4M3 rows with one UE8M0 scale per
+// row and 32 features, the rule of the input's quantization: scale 2^e with
+// the smallest e such that 448 2^e >= max |a| over the warp's 32 features
 // (NaN left out of the maximum), codes rounded to nearest even and
-// saturating (a times 2^-e is exact, as in ldexpf).  Lane l writes byte
-// col + l of each row (32 consecutive bytes a row per warp) and the scale
-// byte of row row0 + l.
-__device__ __forceinline__ void store_a_e4m3(const GemmArgs& p, const float (&v)[32], int row0, int col, int lane) {
+// saturating (a times 2^-e is exact, as in ldexpf).  Lane l writes byte col
+// + l of each row (32 consecutive bytes a row per warp) and lane j < R the
+// scale byte of row row0 + j.
+template <int R>
+__device__ __forceinline__ void store_a_e4m3(const GemmArgs& p, const float (&v)[R], int row0, int col, int lane) {
+    static_assert(R == 16 || R == 32, "16 or 32 rows");
     const int I = p.I;
-    // the maximum of row j over the warp's features, kept by lane j: a
-    // transposing reduction (at offset S the lanes with bit S set keep rows
-    // i + S, the others rows i, each taking the larger with its partner),
-    // 31 shuffles for the 32 rows instead of 32 warp reductions
-    uint32_t t[32];
+    // the maximum of row j over the warp's features, kept by lane j (and
+    // lane j + 16 when R = 16): a transposing reduction (at offset S the
+    // lanes with bit S set keep rows i + S, the others rows i, each taking
+    // the larger with its partner), R - 1 shuffles for the R rows (+ 1)
+    uint32_t t[R];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < R; ++j) {
         const uint32_t b = __float_as_uint(fabsf(v[j]));
         t[j] = b > 0x7f800000u ? 0u : b;
     }
 #pragma unroll
-    for (int S = 16; S > 0; S >>= 1) {
+    for (int S = R / 2; S > 0; S >>= 1) {
         const bool upper = (lane & S) != 0;
 #pragma unroll
         for (int i = 0; i < S; ++i) {
@@ -1019,19 +1028,20 @@ __device__ __forceinline__ void store_a_e4m3(const GemmArgs& p, const float (&v)
             t[i] = max(keep, __shfl_xor_sync(0xffffffffu, send, S));
         }
     }
-    const uint32_t mine = t[0];
+    uint32_t mine = t[0];
+    if constexpr (R == 16) mine = max(mine, __shfl_xor_sync(0xffffffffu, mine, 16));
     // lane j: the exponent of row j; each row's 2^-e comes back by shuffle
     const int ex = fp8_group_exponent_bits(mine);
     const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
     uint8_t* q = p.q_out + (size_t)row0 * (size_t)I + (size_t)(col + lane);
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
+    for (int j = 0; j < R; j += 2) {
         const float s0 = __shfl_sync(0xffffffffu, inv, j), s1 = __shfl_sync(0xffffffffu, inv, j + 1);
         const uint32_t two = __nv_cvt_float2_to_fp8x2(make_float2(v[j] * s0, v[j + 1] * s1), __NV_SATFINITE, __NV_E4M3);
         q[(size_t)j * (size_t)I] = (uint8_t)(two & 0xffu);
         q[(size_t)(j + 1) * (size_t)I] = (uint8_t)(two >> 8);
     }
-    p.sf_out[(size_t)(row0 + lane) * (size_t)(I >> 5) + (size_t)(col >> 5)] = (uint8_t)(ex + 127);
+    if (lane < R) p.sf_out[(size_t)(row0 + lane) * (size_t)(I >> 5) + (size_t)(col >> 5)] = (uint8_t)(ex + 127);
 }
 
 // ---------------------------------------------------------------- epilogue
@@ -1078,7 +1088,75 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
             const int row0 = t.r0 + 32 * c32;
             float v[32];
             tmem_ld32(tacc + 32 * c32, v);
-            if constexpr (t2_is_l1<F>()) {
+            if constexpr (F == L1_FWD_MX) {
+                // The FP8 L1: the gate warp pr and the up warp 2 + pr split the
+                // chunk's rows for SwiGLU and the quantization of a: the up warp
+                // hands the gate warp its values of rows 0-15 and takes the
+                // gate values of rows 16-31 (through the upper half of the up
+                // warp's staging buffer); each then computes and quantizes its
+                // 16 rows.  (The FP8 forward has no activation clamp.)
+                const int I = p.I;
+                const int pr = warp & 1;
+                const int col = t.f0 + 32 * pr;
+                const uint32_t xa = stage_of_warp0 + (uint32_t)(2 + pr) * kStageEpiBytes + 4096u;  // up rows 0-15
+                const uint32_t xb = xa + 2048u;                                                   // gate rows 16-31
+                float o[16];  // the other warp's values of this warp's 16 rows
+                if (warp >= 2) {
+                    if (!warp_wait(bars.xempty(pr), (xchunk & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(xa + (uint32_t)(j * 32 + lane) * 4u), "f"(v[j])
+                                     : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.xfull(pr));
+                } else {
+                    if (!warp_wait(bars.gempty(pr), (xchunk & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(xb + (uint32_t)(j * 32 + lane) * 4u),
+                                     "f"(v[16 + j])
+                                     : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.gfull(pr));
+                }
+                // h (this warp's half: gate or up) leaves by TMA store
+                const uint32_t buf = stage + (nstore & 1u) * 2048u;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                stage_col_sw64(buf, lane, v);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && col < I) {
+                    tma_store_2d(om.c0, (warp >= 2 ? I : 0) + col, row0, buf);
+                    bulk_commit();
+                }
+                const uint32_t from = warp >= 2 ? xb : xa;
+                if (!warp_wait(warp >= 2 ? bars.gfull(pr) : bars.xfull(pr), xchunk & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(o[j]) : "r"(from + (uint32_t)(j * 32 + lane) * 4u)
+                                 : "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(warp >= 2 ? bars.gempty(pr) : bars.xempty(pr));
+                float a16[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float g = warp >= 2 ? o[j] : v[j];
+                    const float u = warp >= 2 ? v[16 + j] : o[j];
+                    a16[j] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                }
+                if (col < I) store_a_e4m3<16>(p, a16, row0 + (warp >= 2 ? 16 : 0), col, lane);
+                ++xchunk;
+            } else if constexpr (t2_is_l1<F>()) {
                 // lanes 0-63: gate features f0..f0+63, lanes 64-127: up features f0..f0+63
                 const int I = p.I;
                 const int pr = warp & 1;
@@ -1149,17 +1227,12 @@ __device__ void t2_role_epilogue(const GemmArgs& p, OutMaps om, const CUtensorMa
                             v[j] = __fdividef(g, 1.0f + __expf(-g)) * clamp_in(u[j], p.clamp);
                         }
                     }
-                    const bool a8 = F == L1_FWD_MX && p.q_out != nullptr;
-                    if (a8) {
-                        if (col < I) store_a_e4m3(p, v, row0, col, lane);
-                    } else {
-                        stage_col_sw64(buf + 2048, lane, v);
-                    }
+                    stage_col_sw64(buf + 2048, lane, v);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && col < I) {
                         tma_store_2d(om.c0, col, row0, buf);
-                        if (!a8) tma_store_2d(om.c1, col, row0, buf + 2048);
+                        tma_store_2d(om.c1, col, row0, buf + 2048);
                         bulk_commit();
                     }
                 }
@@ -1295,6 +1368,8 @@ __global__ void __launch_bounds__(kT2Threads, 1)
             mbar_init(bars.tempty(a), 2 * kEpiWarps * T2<F>::kEpiHalves);
             mbar_init(bars.xfull(a), 1);
             mbar_init(bars.xempty(a), 1);
+            mbar_init(bars.gfull(a), 1);
+            mbar_init(bars.gempty(a), 1);
         }
         mbar_init(bars.drain(), 1);
         for (int w = 0; w < kEpiWarps; ++w) {
