@@ -35,9 +35,8 @@ constexpr int kStageEpiBytes = 8192;  // per epilogue warp: TMA-store staging
 //   DW2       dW2[e] = aw^T . gather(dY)       (K = the expert's rows)
 //   DW1_MG, DW2_MG  the same, added in FP32 to the caller's FP32 main gradient
 //   L1_FWD_MX   L1_FWD on E4M3 weights and gathered E4M3 rows with UE8M0
-//               scales per 32 elements of K (block-scaled MMA); with q_out
-//               set, a leaves as E4M3 rows with a UE8M0 scale per 32
-//               features instead of bf16
+//               scales per 32 elements of K (block-scaled MMA); a leaves as
+//               E4M3 rows with a UE8M0 scale per 32 features (q_out, sf_out)
 //   L2_FWD_MX   L2_FWD on E4M3 W2 and those E4M3 rows of a
 enum Flavour : int {
     L1_FWD = 0, L2_FWD = 1, L2_DGRAD = 2, L1_DGRAD = 3, DW1 = 4, DW2 = 5, DW1_MG = 6, DW2_MG = 7, L1_FWD_MX = 8,
@@ -68,7 +67,7 @@ struct GemmArgs {
     const uint8_t* gsrc8;       // L1_FWD_MX: E4M3 rows [T, H]
     const uint8_t* gsf;         // UE8M0 scales of the E4M3 B rows: L1_FWD_MX [T, H / 32],
                                 // L2_FWD_MX [rows_cap, I / 32] (those of a)
-    uint8_t* q_out;             // L1_FWD_MX: a as E4M3 [rows_cap, I] (null: a in bf16)
+    uint8_t* q_out;             // L1_FWD_MX: a as E4M3 [rows_cap, I] (required)
     uint8_t* sf_out;            // L1_FWD_MX: the scales of q_out [rows_cap, I / 32]
 };
 
