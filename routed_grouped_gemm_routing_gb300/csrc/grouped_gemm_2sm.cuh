@@ -321,8 +321,10 @@ struct T2<L1_FWD> {
 // j at byte 16 (r % 32) + 4 (r / 32) + j, the order in which TMEM holds
 // them: lane r % 32 of every 32-lane quadrant, column r / 32, byte j): one
 // atom for this CTA's weights (by TMA, stored in that layout) and two for
-// the unit's up to 256 rows (gathered; both CTAs hold all of them), copied
-// into TMEM by the MMA thread before the stage's four MMAs.
+// the unit's up to 256 rows (gathered; both CTAs hold all of them, since
+// each CTA's half of the MMA reads the B scales of every column from its
+// own TMEM), copied into TMEM by the MMA thread before the stage's four
+// MMAs.
 template <>
 struct T2<L1_FWD_MX> : T2<L1_FWD> {
     static constexpr bool kAMN = false;
