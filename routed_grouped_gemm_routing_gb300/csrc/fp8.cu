@@ -4,10 +4,19 @@
 // transformed once for its low-precision kernel): the quantization kernels
 // of the input and of the weights, and the instantiations of the two GEMMs
 // on E4M3 operands.
+#include <climits>
+
 #include "grouped_gemm_2sm.cuh"
 
 namespace moe {
 namespace {
+
+// 2^-e for a group exponent e in [-127, 127] (the subnormal 2^-127 for e =
+// 127): x times it is exact up to the one rounding of x / 2^e, the value
+// ldexpf(x, -e) gives.
+__device__ __forceinline__ float fp8_inv_scale(int e) {
+    return e >= 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - e) << 23);
+}
 
 // One warp per 256 consecutive elements of x (row-major [T, H], H a multiple
 // of 32, so no 32-element group straddles two rows): lane l takes elements
@@ -32,6 +41,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* 
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const int e = fp8_group_exponent(amax);
+        const float inv = fp8_inv_scale(e);
         if (ok) {
             uint32_t word[2];
 #pragma unroll
@@ -39,7 +49,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* 
                 uint32_t acc = 0;
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const float2 f = make_float2(ldexpf(v[4 * h + 2 * j], -e), ldexpf(v[4 * h + 2 * j + 1], -e));
+                    const float2 f = make_float2(v[4 * h + 2 * j] * inv, v[4 * h + 2 * j + 1] * inv);
                     const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
                     acc |= (uint32_t)two << (16 * j);
                 }
@@ -80,68 +90,97 @@ __global__ void __launch_bounds__(256) dequantize_fp8_kernel(const uint8_t* __re
 //     / 64, r = 64 (f >= I) + (f mod I) % 64, G = I / 64 (a CTA of the L1
 //     GEMM holds 64 gate and the matching 64 up features);
 //   W2 [E][I][H]: column h has g = h / 128, r = h % 128, G = H / 128.
-// One block of 128 threads per 32 rows of k x 128 columns: the tile comes in
-// coalesced through shared memory and each thread quantizes one column's
-// group.  The same rule as the input (smallest power of two with 448 2^e >=
-// max|group|, round to nearest even, saturate).
+// One block of 256 threads per tile of 128 k x 64 columns: the tile comes in
+// as 128-byte rows (16-byte loads, the next tile's already in flight while
+// this one is quantized), each thread quantizes one column's 32-k group
+// (column tid % 64, group tid / 64) into a shared-memory copy of the
+// output tile, and the tile leaves as 64 rows of 128 K-major bytes, so
+// that both the reads and the writes are whole 128-byte lines.  The same
+// rule as the input (smallest power of two with 448 2^e >= max|group|,
+// round to nearest even, saturate).  HBM-bound: 2 bytes read and 33/32
+// bytes written per element.
+constexpr int kQwK = 128, kQwC = 64, kQwThreads = 256, kQwBlocksPerSm = 4;
 template <bool kW1>
-__global__ void __launch_bounds__(128) quantize_w_fp8_kernel(const __nv_bfloat16* __restrict__ W, int E, int K, int C,
-                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ atoms) {
-    __shared__ __align__(16) __nv_bfloat16 tile[32][128];
-    const int ncol = C / 128, nrow = K / 32, nkb = K / 128;
+__global__ void __launch_bounds__(kQwThreads, 4) quantize_w_fp8_kernel(const __nv_bfloat16* __restrict__ W, int E, int K,
+                                                                    int C, uint8_t* __restrict__ q,
+                                                                    uint8_t* __restrict__ atoms) {
+    // rows padded by 16 bytes: the column reads and the 16-byte row writes
+    // of a warp spread over all banks
+    __shared__ __align__(16) __nv_bfloat16 tile[kQwK][kQwC + 8];
+    __shared__ __align__(16) uint8_t out[kQwC][kQwK + 16];
+    const int ncol = C / kQwC, nkt = K / kQwK;
     const int I = C / 2;  // kW1 only
-    const long long ntiles = (long long)E * nrow * ncol;
+    const int ntiles = E * nkt * ncol;  // below 2^31 (checked at launch)
     const int tid = threadIdx.x;
-    for (long long ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
-        const int cb = (int)(ti % ncol);
-        const int kr = (int)((ti / ncol) % nrow);
-        const int e = (int)(ti / ((long long)ncol * nrow));
-        const int c0 = cb * 128, k0 = kr * 32;
-        __syncthreads();  // the previous tile has been read
+    // 16-byte chunk i of a tile: row tid / 8 + 32 i, columns 8 (tid % 8) ..
+    const int lr = tid >> 3, lc = (tid & 7) * 8;
+    auto load = [&](int ti, uint4 (&v)[4]) {
+        const int cb = ti % ncol;
+        const int kt = (ti / ncol) % nkt;
+        const int e = ti / (ncol * nkt);
+        const __nv_bfloat16* src = W + ((size_t)e * K + (size_t)kt * kQwK + lr) * (size_t)C + (size_t)cb * kQwC + lc;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int ch = tid + 128 * i;  // 16-byte chunk: row ch / 16, columns 8 (ch % 16)
-            const int rr = ch >> 4, cc = (ch & 15) * 8;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(W + ((size_t)e * K + k0 + rr) * (size_t)C + c0 + cc));
-            *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
-        }
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(src + (size_t)(32 * i) * C));
+    };
+    uint4 nxt[4];
+    if ((int)blockIdx.x < ntiles) load((int)blockIdx.x, nxt);
+    for (int ti = (int)blockIdx.x; ti < ntiles; ti += (int)gridDim.x) {
+        const int cb = ti % ncol;
+        const int kt = (ti / ncol) % nkt;
+        const int e = ti / (ncol * nkt);
+        const int c0 = cb * kQwC, k0 = kt * kQwK;
+        __syncthreads();  // the previous tile's shared memory has been read
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(&tile[lr + 32 * i][lc]) = nxt[i];
         __syncthreads();
-        float v[32];
+        if (ti + (int)gridDim.x < ntiles) load(ti + (int)gridDim.x, nxt);
+        const int c = tid & (kQwC - 1), g = tid / kQwC;
+        // the group is read twice from shared memory (maximum, then codes)
+        // rather than held in registers
+        const __nv_bfloat16* col = &tile[32 * g][c];
         float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            v[j] = __bfloat162float(tile[j][tid]);
-            amax = fmaxf(amax, fabsf(v[j]));
-        }
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(__bfloat162float(col[j * (kQwC + 8)])));
         const int ex = fp8_group_exponent(amax);
+        const float inv = fp8_inv_scale(ex);
         uint32_t w[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             uint32_t acc = 0;
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
-                const float2 f = make_float2(ldexpf(v[4 * j + 2 * m], -ex), ldexpf(v[4 * j + 2 * m + 1], -ex));
+                const int r = 4 * j + 2 * m;
+                const float2 f = make_float2(__bfloat162float(col[r * (kQwC + 8)]) * inv,
+                                             __bfloat162float(col[(r + 1) * (kQwC + 8)]) * inv);
                 acc |= (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3) << (16 * m);
             }
             w[j] = acc;
         }
-        const int c = c0 + tid;
-        uint8_t* dst = q + ((size_t)e * (size_t)C + c) * (size_t)K + k0;
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        int g, r, G;
+        *reinterpret_cast<uint4*>(&out[c][32 * g]) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(&out[c][32 * g + 16]) = make_uint4(w[4], w[5], w[6], w[7]);
+        const int cg = c0 + c;
+        int ag, r, G;
         if constexpr (kW1) {
-            const int fi = c < I ? c : c - I;
-            g = fi >> 6;
-            r = (c < I ? 0 : 64) + (fi & 63);
+            const int fi = cg < I ? cg : cg - I;
+            ag = fi >> 6;
+            r = (cg < I ? 0 : 64) + (fi & 63);
             G = I / 64;
         } else {
-            g = c >> 7;
-            r = c & 127;
+            ag = cg >> 7;
+            r = cg & 127;
             G = C / 128;
         }
-        const int kb = kr >> 2, js = kr & 3;
-        atoms[(((size_t)e * G + g) * nkb + kb) * 512 + 16 * (r & 31) + 4 * (r >> 5) + js] = (uint8_t)(ex + 127);
+        // 32-k group 4 kt + g: atom block kt, step g
+        atoms[(((size_t)e * G + ag) * nkt + kt) * 512 + 16 * (r & 31) + 4 * (r >> 5) + g] = (uint8_t)(ex + 127);
+        __syncthreads();
+        // 64 rows of 128 bytes: q[e][c0 + row][k0 ..]
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int ch = tid + kQwThreads * i;
+            const int row = ch >> 3, part = ch & 7;
+            *reinterpret_cast<uint4*>(q + ((size_t)e * C + c0 + row) * (size_t)K + k0 + 16 * part) =
+                *reinterpret_cast<const uint4*>(&out[row][16 * part]);
+        }
     }
 }
 
@@ -149,19 +188,23 @@ __global__ void __launch_bounds__(128) quantize_w_fp8_kernel(const __nv_bfloat16
 
 int launch_quantize_w1_fp8(const __nv_bfloat16* W1, int E, int H, int I, uint8_t* q, uint8_t* atoms, int num_sms,
                            cudaStream_t st) {
-    const long long ntiles = (long long)E * (H / 32) * (2 * I / 128);
+    const long long ntiles = (long long)E * (H / kQwK) * (2 * I / kQwC);
     if (ntiles <= 0) return 0;
-    const long long cap = (long long)num_sms * 16;
-    quantize_w_fp8_kernel<true><<<(unsigned)(ntiles < cap ? ntiles : cap), 128, 0, st>>>(W1, E, H, 2 * I, q, atoms);
+    if (ntiles > INT_MAX) return (int)cudaErrorInvalidValue;
+    const long long cap = (long long)num_sms * kQwBlocksPerSm;  // resident blocks
+    quantize_w_fp8_kernel<true><<<(unsigned)(ntiles < cap ? ntiles : cap), kQwThreads, 0, st>>>(W1, E, H, 2 * I, q,
+                                                                                              atoms);
     return (int)cudaGetLastError();
 }
 
 int launch_quantize_w2_fp8(const __nv_bfloat16* W2, int E, int H, int I, uint8_t* q, uint8_t* atoms, int num_sms,
                            cudaStream_t st) {
-    const long long ntiles = (long long)E * (I / 32) * (H / 128);
+    const long long ntiles = (long long)E * (I / kQwK) * (H / kQwC);
     if (ntiles <= 0) return 0;
-    const long long cap = (long long)num_sms * 16;
-    quantize_w_fp8_kernel<false><<<(unsigned)(ntiles < cap ? ntiles : cap), 128, 0, st>>>(W2, E, I, H, q, atoms);
+    if (ntiles > INT_MAX) return (int)cudaErrorInvalidValue;
+    const long long cap = (long long)num_sms * kQwBlocksPerSm;
+    quantize_w_fp8_kernel<false><<<(unsigned)(ntiles < cap ? ntiles : cap), kQwThreads, 0, st>>>(W2, E, I, H, q,
+                                                                                               atoms);
     return (int)cudaGetLastError();
 }
 
