@@ -119,13 +119,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_pairs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // per expert: exclusive prefix over blocks (in place) and the total
+    // per expert: exclusive prefix over blocks (in place) and the total; the
+    // counts of 8 blocks are loaded before any of them is rewritten, so that
+    // their loads are in flight together
     for (int e = tid; e < E; e += kThreads) {
         int acc = 0;
-        for (int b = 0; b < nblk; ++b) {
-            const int v = bcnt[(size_t)b * E + e];
-            bcnt[(size_t)b * E + e] = acc;
-            acc += v;
+        for (int b0 = 0; b0 < nblk; b0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = b0 + i < nblk ? bcnt[(size_t)(b0 + i) * E + e] : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (b0 + i < nblk) bcnt[(size_t)(b0 + i) * E + e] = acc;
+                acc += v[i];
+            }
         }
         cnt[e] = acc;
     }

@@ -45,6 +45,8 @@ def _random_idx(T, E, k, seed, p_drop=0.0, p_bad=0.0):
     (8192, 256, 8, 2),     # the V3 routing size: 64 blocks
     (20000, 1024, 5, 3),   # E = 1024
     (3000, 1, 1, 4),       # E = 1
+    (5000, 101, 4, 6),     # 8 lanes per expert in the block scan, 808 of them: a partly used warp
+    (6000, 600, 7, 7),     # one lane per expert, 600 of the 1024 threads
 ])
 def test_random_ids(T, E, k, seed):
     _tables(T, E, k, _random_idx(T, E, k, seed, p_drop=0.05, p_bad=0.02))
