@@ -318,7 +318,8 @@ def run_reference(args):
 
 
 FWD_KERNELS = ("route_hist", "route_scan", "route_place", "gemm_l1_fwd", "gemm_l2_fwd", "combine_fwd")
-# every other BASELINE workload, timed after the headline one, one at a time
+# the other workloads (tiny, V2-Lite-, wide- and skewed-V3-shaped layers),
+# timed after the headline one, one at a time
 # (each one's buffers are freed before the next is drawn): (name, config,
 # backward, timed steps, oracle sample tokens, oracle sample experts)
 OTHER_CONFIGS = (("tiny", "tiny", True, 100, 64, 0), ("v2lite", "v2lite", True, 20, 32, 2),
@@ -546,7 +547,7 @@ def fp8_forward_times(shape, inp, ws, y, dev, peaks):
 
 
 def run_other_configs(args, dev, world, rank, peaks, peaks_src):
-    """Every other BASELINE workload on this GPU, one after another; the
+    """The other workloads (OTHER_CONFIGS) on this GPU, one after another; the
     V3-shaped headline's buffers are already freed."""
     import numpy as np
     import torch
