@@ -73,7 +73,7 @@ def oracle_all(inp, E, clamp=0.0):
     return dict(y=y, dx=dx, dtopk_w=dw, dW1=dW1, dW2=dW2)
 
 
-def oracle_tokens(inp, E, toks):
+def oracle_tokens(inp, E, toks, clamp=0.0):
     """y, dx, dtopk_w rows of the listed tokens, from a sub-problem holding
     only those tokens and the experts they route to."""
     toks = np.asarray(toks, np.int64)
@@ -88,12 +88,12 @@ def oracle_tokens(inp, E, toks):
     W1s, W2s = bf16_bits(inp["W1"][it]), bf16_bits(inp["W2"][it])
     xs, dYs = bf16_bits(inp["x"][tt]), bf16_bits(inp["dY"][tt])
     w = inp["topk_w"][tt].cpu().numpy().astype(np.float32)
-    y = oracle.forward(xs, W1s, W2s, idx_sub, w)
-    dx, dw = oracle.backward_tokens(xs, W1s, W2s, idx_sub, w, dYs)
+    y = oracle.forward(xs, W1s, W2s, idx_sub, w, clamp=clamp)
+    dx, dw = oracle.backward_tokens(xs, W1s, W2s, idx_sub, w, dYs, clamp=clamp)
     return y, dx, dw
 
 
-def oracle_experts(inp, E, exps):
+def oracle_experts(inp, E, exps, clamp=0.0):
     """dW1, dW2 of the listed experts, from a sub-problem holding every token
     and only those experts' weights."""
     exps = np.asarray(exps, np.int64)
@@ -106,7 +106,7 @@ def oracle_experts(inp, E, exps):
     W1s, W2s = bf16_bits(inp["W1"][et]), bf16_bits(inp["W2"][et])
     x, dY = bf16_bits(inp["x"]), bf16_bits(inp["dY"])
     w = inp["topk_w"].cpu().numpy().astype(np.float32)
-    return oracle.backward_experts(x, W1s, W2s, idx_sub, w, dY)
+    return oracle.backward_experts(x, W1s, W2s, idx_sub, w, dY, clamp=clamp)
 
 
 class GpuRun:
