@@ -226,3 +226,36 @@ def test_fp8_experts_wrapper_matches_abi():
     assert torch.equal(y, run.y) and torch.equal(y2, run.y)
     with pytest.raises(ValueError):
         FP8Experts(inp["W1"][:, :, :192].contiguous(), inp["W2"][:, :96].contiguous())
+
+
+def test_fp8_forward_cuda_graph_replay_matches_eager():
+    """moe_quantize_fp8 + moe_route_prologue + moe_forward_fp8 captured in a
+    CUDA graph (no host synchronisation on the FP8 path) and replayed give
+    the eager output bit for bit."""
+    T, H, I, E, k = 300, 256, 128, 6, 3
+    inp, (q, sf, w1q, w1sf, w2q, w2sf), _ = fp8_layer_inputs(T, H, I, E, k, 70)
+
+    def forward(run, xq, xsf):
+        B.moe_quantize_fp8(run.shape, inp["x"], xq, xsf)
+        B.moe_route_prologue(run.shape, inp["topk_idx"], run.route)
+        B.moe_forward_fp8(run.shape, xq, xsf, w1q, w1sf, w2q, w2sf, inp["topk_w"], run.route, run.saved, run.y)
+
+    eager = GpuRun(T, H, I, E, k)
+    forward(eager, torch.empty_like(q), torch.empty_like(sf))
+    torch.cuda.synchronize()
+    run = GpuRun(T, H, I, E, k)
+    xq, xsf = torch.empty_like(q), torch.empty_like(sf)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        forward(run, xq, xsf)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    run.poison()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        forward(run, xq, xsf)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(run.y, eager.y)

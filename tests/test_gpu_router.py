@@ -96,3 +96,39 @@ def test_deterministic():
     _, _, i1, w1 = _run(lg, 8)
     _, _, i2, w2 = _run(lg, 8)
     assert np.array_equal(i1, i2) and np.array_equal(w1.view(np.int32), w2.view(np.int32))
+
+
+def test_cuda_graph_replay_matches_eager():
+    """The router and the routing prologue captured in a CUDA graph (no host
+    synchronisation inside moe_router_topk) and replayed give the eager
+    results bit for bit, routing tables included."""
+    lg = torch.as_tensor(np.random.default_rng(21).standard_normal((3000, 64)).astype(np.float32), device="cuda")
+    T, E, k = 3000, 64, 6
+    shape = B.shape_of(T, 64, 64, E, k)
+    L = B.moe_workspace_layout(shape)
+
+    def bufs():
+        return (torch.full((T, k), -7, dtype=torch.int32, device="cuda"),
+                torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda"),
+                torch.full((max(L.route_bytes, 16),), 0xFF, dtype=torch.uint8, device="cuda"))
+
+    idx_e, w_e, route_e = bufs()
+    B.moe_router_topk(shape, lg, idx_e, w_e, route_e)
+    idx_g, w_g, route_g = bufs()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        B.moe_router_topk(shape, lg, idx_g, w_g, route_g)  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    idx_g.fill_(-7)
+    w_g.fill_(float("nan"))
+    route_g.fill_(0xFF)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.moe_router_topk(shape, lg, idx_g, w_g, route_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(idx_g, idx_e)
+    assert torch.equal(w_g.view(torch.int32), w_e.view(torch.int32))
+    assert torch.equal(route_g, route_e)
