@@ -256,3 +256,60 @@ def test_full_size_activation_clamp():
         print(f"v3 clamp: dW1[{e}] ({int(counts[e])} rows): {cols.sum()} of {2 * I} columns compared")
         assert cols.sum() >= 0.9 * 2 * I
         compare(f"v3 clamp dW1[{e}]", f32(run.dW1[e])[:, cols], dW1_ref[i][:, cols])
+
+
+def test_full_size_fp8_forward_skewed():
+    """The FP8 forward under the skewed routing at the V3 shape: the most
+    loaded expert (thousands of rows: many 256-row units of one expert in a
+    row, each on accumulator 0) and the least loaded one, their E4M3 rows of
+    a against oracle.forward_fp8 on sub-problems of their slots and
+    dequantized weights, and their weighted L2 rows o within the comparison
+    bar; y finite."""
+    shape = CONFIGS["skew"]
+    T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    inp = make_layer_inputs(shape, seed=0, device="cuda")
+    s = B.shape_of(T, H, I, E, k)
+    q = torch.empty(T, H, dtype=torch.uint8, device="cuda")
+    sf = torch.empty(T, H // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_fp8(s, inp["x"], q, sf)
+    w1q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device="cuda")
+    w1sf = torch.empty(E * 2 * I * H // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_weights_fp8(s, inp["W1"], w1q, w1sf)
+    w2q = torch.empty(E, H, I, dtype=torch.uint8, device="cuda")
+    w2sf = torch.empty(E * H * I // 32, dtype=torch.uint8, device="cuda")
+    B.moe_quantize_w2_fp8(s, inp["W2"], w2q, w2sf)
+    run8 = GpuRun(T, H, I, E, k)
+    B.moe_route_prologue(run8.shape, inp["topk_idx"], run8.route)
+    B.moe_forward_fp8(run8.shape, q, sf, w1q, w1sf, w2q, w2sf, inp["topk_w"], run8.route, run8.saved, run8.y)
+    torch.cuda.synchronize()
+    assert torch.isfinite(run8.y).all()
+    tab = run8.tables()
+    counts, offs, perm = tab["counts"], tab["offs"], tab["perm"]
+    L = B.moe_workspace_layout(run8.shape)
+    sv = run8.saved
+    R = L.rows_cap
+    a8 = sv[L.a: L.a + R * I].view(R, I)
+    asf = sv[L.a + R * I: L.a + R * I + R * (I // 32)].view(R, I // 32)
+    o = sv[L.o: L.o + R * H * 2].view(torch.bfloat16).view(R, H)
+    xq, xsf = q.cpu().numpy(), sf.cpu().numpy()
+    w = inp["topk_w"].cpu().numpy()
+    order = np.argsort(counts, kind="stable")
+    nz = order[counts[order] > 0]
+    per1, per2 = 2 * I * H // 32, H * I // 32
+    for e in dict.fromkeys([int(order[-1]), int(nz[0])]):
+        c = int(counts[e])
+        rows = np.arange(offs[e], offs[e] + c)
+        slots = perm[rows]
+        toks, js = slots // k, slots % k
+        x_sub = oracle.dequantize_fp8(xq[toks], xsf[toks])
+        W1_sub = dequantized_w1(w1q[e:e + 1].cpu().numpy(), w1sf[e * per1:(e + 1) * per1].cpu().numpy(), 1, H,
+                                I).double().numpy()
+        W2_sub = dequantized_w2(w2q[e:e + 1].cpu().numpy(), w2sf[e * per2:(e + 1) * per2].cpu().numpy(), 1, H,
+                                I).double().numpy()
+        y_sub, aq, asf_ref = oracle.forward_fp8(x_sub, W1_sub, W2_sub, np.zeros((c, 1), np.int32),
+                                                w[toks, js].reshape(c, 1))
+        trows = torch.from_numpy(rows).cuda()
+        sf_bad, frac, _ = check_a8_against_oracle(a8[trows].cpu().numpy(), asf[trows].cpu().numpy(),
+                                                  np.arange(c), aq, asf_ref, 1)
+        print(f"skew fp8 expert {e} ({c} rows): scale bytes differing {sf_bad:.1e}, codes differing {frac:.1e}")
+        compare(f"skew fp8 o rows of expert {e} ({c} rows)", f32(o[trows]), y_sub)
